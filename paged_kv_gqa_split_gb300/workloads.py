@@ -1,0 +1,222 @@
+"""Seeded synthetic inputs for paged GQA decode (h32 / kv4 / d128 / page size 1, bf16).
+
+This module only draws inputs. It holds none of the attention arithmetic, so the
+float64 oracle and the CUDA path can both consume what it produces without
+sharing any of the method.
+
+Problem shape, as fixed by the FlashInfer-style problem statement on the
+kernelindex.com page "gqa_paged_decode_h32_kv4_d128_ps1" (its ``run()`` docstring):
+
+* ``q``          [batch, 32, 128] bf16
+* ``k_cache``    [num_pages, 1, 4, 128] bf16
+* ``v_cache``    [num_pages, 1, 4, 128] bf16
+* ``kv_indptr``  [batch + 1] int32, CSR offsets into ``kv_indices``
+* ``kv_indices`` [kv_indptr[-1]] int32, page ids in token order
+* ``sm_scale``   1/sqrt(128)
+
+Draw order for every workload (one ``torch.Generator`` seeded with the
+workload's seed): sequence lengths (and, for the skewed mix, the positions of
+the long sequences), the page permutation, then q, k, v. q, k and v are drawn
+as float32 standard normals and rounded to bf16 (round-to-nearest-even).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional, Sequence
+
+import torch
+
+NUM_QO_HEADS = 32
+NUM_KV_HEADS = 4
+HEAD_DIM = 128
+PAGE_SIZE = 1
+DEFAULT_SM_SCALE = 1.0 / math.sqrt(HEAD_DIM)
+
+# Elements drawn per randn call when filling the page pools; fixed so that the
+# stream of draws (and therefore every value) depends on the seed alone.
+_CHUNK = 1 << 22
+
+
+@dataclass
+class Workload:
+    """One batch of decode inputs, all on the CPU."""
+
+    name: str
+    q: torch.Tensor
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    kv_indptr: torch.Tensor
+    kv_indices: torch.Tensor
+    sm_scale: float
+    lens: List[int] = field(default_factory=list)
+
+    @property
+    def batch(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.kv_indices.shape[0])
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_cache.shape[0])
+
+    def to(self, device, non_blocking: bool = False) -> "Workload":
+        return Workload(
+            self.name,
+            self.q.to(device, non_blocking=non_blocking),
+            self.k_cache.to(device, non_blocking=non_blocking),
+            self.v_cache.to(device, non_blocking=non_blocking),
+            self.kv_indptr.to(device, non_blocking=non_blocking),
+            self.kv_indices.to(device, non_blocking=non_blocking),
+            self.sm_scale,
+            list(self.lens),
+        )
+
+
+def _randn_bf16(shape: Sequence[int], g: torch.Generator, std: float = 1.0) -> torch.Tensor:
+    """float32 N(0, std^2) draws rounded to bf16, produced in fixed-size chunks."""
+    n = 1
+    for s in shape:
+        n *= int(s)
+    out = torch.empty(n, dtype=torch.bfloat16)
+    for lo in range(0, n, _CHUNK):
+        hi = min(n, lo + _CHUNK)
+        x = torch.randn(hi - lo, generator=g, dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        out[lo:hi] = x.to(torch.bfloat16)
+    return out.view(*shape)
+
+
+def make_workload(
+    lens: Sequence[int],
+    seed: int,
+    *,
+    pool_factor: float = 1.0,
+    q_std: float = 1.0,
+    name: str = "custom",
+    sm_scale: float = DEFAULT_SM_SCALE,
+    g: Optional[torch.Generator] = None,
+) -> Workload:
+    """Build a workload from explicit sequence lengths.
+
+    ``num_pages = ceil(pool_factor * sum(lens))`` (at least 1, so the pools are
+    never zero-sized); ``kv_indices`` is the first ``sum(lens)`` entries of a
+    seeded random permutation of the pool, i.e. pages sampled without
+    replacement and scattered at random through the pool.
+    """
+    if g is None:
+        g = torch.Generator().manual_seed(seed)
+    lens = [int(x) for x in lens]
+    if any(x < 0 for x in lens):
+        raise ValueError("sequence lengths must be non-negative")
+    batch = len(lens)
+    total = sum(lens)
+    num_pages = max(1, int(math.ceil(pool_factor * total)))
+    indptr = torch.zeros(batch + 1, dtype=torch.int64)
+    if batch:
+        indptr[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0)
+    perm = torch.randperm(num_pages, generator=g)
+    kv_indices = perm[:total].to(torch.int32).contiguous()
+    q = _randn_bf16((batch, NUM_QO_HEADS, HEAD_DIM), g, q_std)
+    k = _randn_bf16((num_pages, PAGE_SIZE, NUM_KV_HEADS, HEAD_DIM), g)
+    v = _randn_bf16((num_pages, PAGE_SIZE, NUM_KV_HEADS, HEAD_DIM), g)
+    return Workload(name, q, k, v, indptr.to(torch.int32), kv_indices, float(sm_scale), lens)
+
+
+def _tiny(g: torch.Generator) -> List[int]:
+    lens = torch.randint(1, 257, (5,), generator=g).tolist()
+    lens[2] = 0  # the third sequence (0-based index 2) is forced empty
+    return lens
+
+
+def _mid(g: torch.Generator) -> List[int]:
+    return torch.randint(512, 4097, (64,), generator=g).tolist()
+
+
+def _long(g: torch.Generator) -> List[int]:
+    return [131072]
+
+
+def _large(g: torch.Generator) -> List[int]:
+    return torch.randint(1024, 8193, (256,), generator=g).tolist()
+
+
+def _skewed(g: torch.Generator) -> List[int]:
+    batch = 128
+    n_long = int(round(0.1 * batch))  # 13 long sequences, 115 short ones
+    where = torch.randperm(batch, generator=g)[:n_long]
+    lens = torch.randint(64, 513, (batch,), generator=g)
+    lens[where] = torch.randint(32768, 65537, (n_long,), generator=g)
+    return lens.tolist()
+
+
+@dataclass(frozen=True)
+class Config:
+    name: str
+    seed: int
+    lens_fn: object
+    pool_factor: float
+    q_std: float
+    description: str
+
+
+CONFIGS: Dict[str, Config] = {
+    "tiny": Config("tiny", 0, _tiny, 1.0, 1.0,
+                   "batch 5, lens U{1..256}, sequence 2 empty, pool = sum(lens), kv_indices = randperm"),
+    "mid": Config("mid", 1, _mid, 1.0, 1.0,
+                  "batch 64, lens U{512..4096}, pool = sum(lens), kv_indices = randperm"),
+    "long": Config("long", 2, _long, 1.0, 1.0,
+                   "batch 1, one sequence of 131072 tokens, kv_indices = randperm(131072)"),
+    "large": Config("large", 3, _large, 1.25, 1.0,
+                    "batch 256, lens U{1024..8192}, pool = ceil(1.25 sum(lens)), indices sampled without replacement"),
+    "skewed": Config("skewed", 4, _skewed, 2.0, 3.0,
+                     "batch 128, 115 lens U{64..512} + 13 lens U{32768..65536}, pool = 2 sum(lens), q ~ 3 N(0,1)"),
+}
+
+
+def config_lens(name: str) -> List[int]:
+    """Sequence lengths of a named workload, without drawing the tensors."""
+    cfg = CONFIGS[name]
+    g = torch.Generator().manual_seed(cfg.seed)
+    return list(cfg.lens_fn(g))
+
+
+def make_config(name: str) -> Workload:
+    """Draw the named workload (tiny, mid, long, large, skewed) on the CPU."""
+    cfg = CONFIGS[name]
+    g = torch.Generator().manual_seed(cfg.seed)
+    lens = cfg.lens_fn(g)
+    return make_workload(lens, cfg.seed, pool_factor=cfg.pool_factor, q_std=cfg.q_std,
+                         name=cfg.name, g=g)
+
+
+def make_pattern_workload() -> Workload:
+    """A small fixed workload with formula-defined values (no random draws).
+
+    Three sequences of lengths 3, 0 and 5 over a pool of 10 pages; page ids are
+    ``(7 * j + 3) % 10`` for token j of the batch. Every q/k/v entry is a
+    multiple of 1/8 in [-1, 1], exactly representable in bf16, given by
+    ``((a * i + e) % 17 - 8) / 8`` over the flattened index i of the tensor
+    (a, e fixed per tensor). Identical on every machine.
+    """
+    lens = [3, 0, 5]
+    total = sum(lens)
+    indptr = torch.tensor([0, 3, 3, 8], dtype=torch.int32)
+    indices = torch.tensor([(7 * j + 3) % 10 for j in range(total)], dtype=torch.int32)
+
+    def pattern(shape, a, e):
+        n = 1
+        for s in shape:
+            n *= s
+        i = torch.arange(n, dtype=torch.int64)
+        vals = ((a * i + e) % 17 - 8).to(torch.float32) / 8.0
+        return vals.to(torch.bfloat16).view(*shape)
+
+    q = pattern((3, NUM_QO_HEADS, HEAD_DIM), 5, 1)
+    k = pattern((10, PAGE_SIZE, NUM_KV_HEADS, HEAD_DIM), 3, 2)
+    v = pattern((10, PAGE_SIZE, NUM_KV_HEADS, HEAD_DIM), 11, 4)
+    return Workload("pattern", q, k, v, indptr, indices, DEFAULT_SM_SCALE, lens)
