@@ -1,0 +1,470 @@
+"""Benchmark of the GB300 paged GQA decode library (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload large] [--no-workloads] [--no-cpu-baseline]
+
+One step is one full ``gqa_paged_decode`` call (decode kernel + LSE merge
+kernel) over one batch of the workload, inputs resident in HBM. Counted bytes
+per call: 2048 B per cached token (K and V rows of all 4 KV heads) plus, per
+sequence, 8192 B of q, 8192 B of out and 128 B of lse. ``value`` is those bytes
+over the device time of the K timed steps (CUDA events on the launching
+stream, L2 flushed by a 256 MB write between steps, outside the events).
+
+``--impl reference`` times the float64 CPU oracle instead (bounded samples of
+the same workload on the host cores); only rank 0 runs it.
+With N > 1 (torchrun, one rank per GPU) every rank runs its own replica of the
+workload (weak scaling, no collective on the data path); the step time is the
+max over ranks and ``value`` counts the bytes of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_gqa_split_gb300 import _lib  # noqa: E402
+from paged_kv_gqa_split_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged GQA decode: µs/batch and achieved HBM GB/s (% of GB300 peak)"
+WORKLOAD_TEXT = {
+    "tiny": "tiny: batch 5, h32/kv4/d128/ps1 bf16, lens U[1,256], sequence 2 empty, pool = sum(lens), randperm pages",
+    "mid": "mid batch: batch 64, h32/kv4/d128/ps1 bf16, lens U[512,4096], pool = sum(lens), randperm pages",
+    "long": "long context: batch 1, one sequence of 131072 tokens, h32/kv4/d128/ps1 bf16, randperm pages",
+    "large": ("large ragged batch: batch 256, h32/kv4/d128/ps1 bf16, lens U[1024,8192], pool 1.25x sum(lens) "
+              "N(0,1), pages sampled without replacement"),
+    "skewed": ("skewed batch: batch 128, h32/kv4/d128/ps1 bf16, 115 lens U[64,512] + 13 lens U[32768,65536], "
+               "pool 2x sum(lens), q ~ 3 N(0,1)"),
+}
+FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def counted_bytes(lens) -> int:
+    return 2048 * sum(lens) + (8192 + 8192 + 128) * len(lens)
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity with one rank)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("gqa_decode.cu", "gqa_ptx.cuh", "gqa_plan.h"):
+        with open(os.path.join(ROOT, "paged_kv_gqa_split_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, total_tokens: int):
+    """DRAM bytes per decode launch from the committed ncu summary, scaled to this
+    workload's token count, or None if the kernel changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            doc = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if doc.get("kernel_hash") != kernel_source_hash():
+        return None
+    rec = doc.get("captures", {}).get(workload)
+    if rec is None:
+        return None
+    return float(rec["dram_bytes_per_launch"]) * total_tokens / float(rec["total_tokens"])
+
+
+# ------------------------------------------------------------- our GPU arm
+def time_steps(call, steps: int, stream, flush_buf, before=None):
+    """Per-step device time (ms) of `call` with CUDA events on `stream`; L2 is flushed
+    between steps outside the events."""
+    times = []
+    for i in range(steps):
+        flush_buf.zero_()
+        if before is not None:
+            before(i)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in times]
+
+
+def bench_workload_gpu(w, device, steps, warmup, world, with_hooks=True):
+    g = w.to(device)
+    out = torch.empty_like(g.q)
+    lse = torch.empty((w.batch, 32), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def call():
+        _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, w.sm_scale, out=out, lse=lse, stream=stream)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    barrier(world, device)
+    t_wall0 = time.perf_counter()
+    step_ms = time_steps(call, steps, stream, flush)
+    barrier(world, device)
+    wall = time.perf_counter() - t_wall0
+
+    dec_ms = None
+    if with_hooks:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:  # torch creates the underlying cudaEvent_t on first record
+            a.record(stream)
+            b.record(stream)
+
+        def hook(i):
+            _lib.gqa_paged_decode_set_profile_events(evs[i][0].cuda_event, evs[i][1].cuda_event)
+
+        try:
+            time_steps(call, steps, stream, flush, before=hook)
+        finally:
+            _lib.gqa_paged_decode_set_profile_events(None, None)
+        dec_ms = [a.elapsed_time(b) for a, b in evs]
+    del flush
+    return {"step_ms": step_ms, "decode_ms": dec_ms, "wall_s": wall, "gpu": g, "out": out, "lse": lse}
+
+
+def bench_e2e(w, device, steps, warmup):
+    """Same metric through the public API with host buffers: pinned host inputs are
+    copied to the device, the call runs, out/lse come back, all inside the events."""
+    host = [w.q.pin_memory(), w.k_cache.pin_memory(), w.v_cache.pin_memory(), w.kv_indptr.pin_memory(),
+            w.kv_indices.pin_memory()]
+    dev = [torch.empty_like(t, device=device) for t in host]
+    out_h = torch.empty_like(host[0]).pin_memory()
+    lse_h = torch.empty((w.batch, 32), dtype=torch.float32).pin_memory()
+    out_d = torch.empty_like(dev[0])
+    lse_d = torch.empty((w.batch, 32), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def call():
+        for hd, dd in zip(host, dev):
+            dd.copy_(hd, non_blocking=True)
+        _lib.run(dev[0], dev[1], dev[2], dev[3], dev[4], w.sm_scale, out=out_d, lse=lse_d, stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+
+    for _ in range(max(1, warmup)):
+        call()
+    torch.cuda.synchronize()
+    ms = time_steps(call, steps, stream, flush)
+    del flush, dev
+    return ms, h2d, d2h
+
+
+# -------------------------------------------------------------- CPU oracle
+def oracle_sample(w, budget_s: float):
+    """Run the float64 oracle over the workload's sequences in order until about
+    budget_s seconds have passed (at least one non-empty sequence)."""
+    from oracle import gqa_paged_decode_oracle
+    done, t0 = [], time.perf_counter()
+    order = [b for b in range(w.batch) if w.lens[b] > 0] or [0]
+    for b in order:
+        gqa_paged_decode_oracle(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices, w.sm_scale, seqs=[b])
+        done.append(b)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return [w.lens[b] for b in done], dt
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        n = max((d.get("num_threads", 1) for d in info), default=1)
+        return int(n)
+    except Exception:
+        return 1
+
+
+def cpu_baseline(w, budget_s: float = 10.0):
+    lens, dt = oracle_sample(w, budget_s)
+    gbs = counted_bytes(lens) / dt / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{len(lens)} of {w.batch} sequences ({sum(lens)} tokens) of the {w.name} workload, "
+                      f"float64 NumPy oracle, {dt:.2f} s",
+            "host_cores_available": len(os.sched_getaffinity(0))}
+
+
+# ---------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(wl.CONFIGS), default="large")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    warmup = max(3, args.warmup)
+
+    world, rank, local = dist_info()
+    if args.impl == "reference":
+        return main_reference(args, world, rank, warmup)
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    from paged_kv_gqa_split_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    barrier(world, device)
+    _lib.load()
+
+    peak, peak_kind = hbm_peak()
+    w = wl.make_config(args.workload)
+    cb = counted_bytes(w.lens)
+    with ClockSampler(local) as clk:
+        r = bench_workload_gpu(w, device, args.steps, warmup, world)
+    step_ms = statistics.mean(r["step_ms"])
+    step_ms_max = max_over_ranks(step_ms, world, device)
+    dec_ms = statistics.mean(r["decode_ms"])
+    value = world * cb / (step_ms_max * 1e-3) / 1e9
+    achieved = cb / (dec_ms * 1e-3) / 1e9
+
+    # parity spot check on this very run (sampled sequences against the oracle)
+    parity = None
+    if rank == 0 and not args.no_cpu_baseline:
+        parity = spot_parity(w, r["out"], r["lse"])
+    del r
+
+    e2e = None
+    if not args.no_e2e:
+        ms, h2d, d2h = bench_e2e(w, device, max(3, args.steps // 4), 1)
+        e_ms = max_over_ranks(statistics.mean(ms), world, device)
+        e2e = {"value": world * cb / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    table = {}
+    if not args.no_workloads:
+        for name in ["tiny", "mid", "long", "large", "skewed"]:
+            ww = w if name == args.workload else wl.make_config(name)
+            rr = bench_workload_gpu(ww, device, args.steps, warmup, world)
+            ms = statistics.mean(rr["step_ms"])
+            dm = statistics.mean(rr["decode_ms"])
+            b = counted_bytes(ww.lens)
+            table[name] = {"us_per_batch": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9,
+                           "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
+                           "decode_kernel_us": dm * 1e3, "batch": ww.batch, "total_tokens": ww.total_tokens,
+                           "counted_bytes": b}
+            del rr
+            if ww is not w:
+                del ww
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    clocks = clk.summary()
+    traffic = ncu_traffic(args.workload, w.total_tokens)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": warmup,
+        "ms_per_step": step_ms_max,
+        "us_per_batch": step_ms_max * 1e3,
+        "frac_of_peak": value / world / peak,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded torch.Generator, CPU-drawn, copied to HBM before timing)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "batch": w.batch, "total_tokens": w.total_tokens,
+                   "num_pages": w.num_pages, "counted_bytes_per_step": cb,
+                   "l2": "flushed between steps by a 256 MB device write (outside the timed events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "gqa_decode_kernel", "peak_kind": f"{peak_kind} (hbm_gbs)",
+                     "algorithmic_bytes_per_launch": cb},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "parity": parity,
+        "workloads": table,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def spot_parity(w, out, lse, n=4):
+    """Max errors of a few sequences of this run against the float64 oracle."""
+    import numpy as np
+    from oracle import gqa_paged_decode_oracle
+    lens = np.array(w.lens)
+    seqs = sorted(set(np.argsort(lens)[-2:].tolist()) | {0, w.batch // 2})[:n]
+    o_ref, l_ref = gqa_paged_decode_oracle(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices, w.sm_scale,
+                                           seqs=seqs)
+    o = out.float().cpu().double().numpy()[seqs]
+    l = lse.cpu().double().numpy()[seqs]
+    fin = np.isfinite(l_ref[seqs])
+    o_err = float(np.abs(o - o_ref[seqs]).max())
+    l_err = float(np.abs(l[fin] - l_ref[seqs][fin]).max()) if fin.any() else 0.0
+    ok = bool(np.all(np.abs(o - o_ref[seqs]) <= 2e-2 + 2e-2 * np.abs(o_ref[seqs])) and l_err <= 1e-3)
+    return {"sequences": seqs, "max_abs_dO": o_err, "max_abs_dlse": l_err, "within_tolerance": ok}
+
+
+def main_reference(args, world, rank, warmup):
+    if rank != 0:
+        return
+    w = wl.make_config(args.workload)
+    budget = max(0.5, 120.0 / max(1, args.steps + warmup))
+    for _ in range(warmup):
+        oracle_sample(w, budget)
+    rates, secs, lens_done = [], [], []
+    for _ in range(args.steps):
+        lens, dt = oracle_sample(w, budget)
+        rates.append(counted_bytes(lens) / dt / 1e9)
+        secs.append(dt)
+        lens_done = lens
+    value = statistics.mean(rates)
+    ms_equiv = counted_bytes(w.lens) / (value * 1e9) * 1e3
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": warmup,
+        "ms_per_step": ms_equiv,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded torch.Generator)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "batch": w.batch, "total_tokens": w.total_tokens,
+                   "parallelism": "single process"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": blas_threads(),
+                         "sample": f"each step: the first {len(lens_done)} non-empty sequences "
+                                   f"({sum(lens_done)} tokens), about {budget:.1f} s of float64 oracle work; "
+                                   f"ms_per_step is the whole batch at that rate"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,138 @@
+/*
+ * gqa_paged_decode.h -- C ABI of the GB300 (sm_103a) paged-KV GQA decode library.
+ *
+ * The operation is the one stated by the FlashInfer-style problem on the
+ * kernelindex.com page "gqa_paged_decode_h32_kv4_d128_ps1" (its kernel and the
+ * run() docstring): batched decode attention with grouped-query attention,
+ * 32 query heads over 4 KV heads (query head h reads KV head h / 8), head
+ * dimension 128, page size 1, bf16 inputs, KV pages addressed through a CSR
+ * page table. For every sequence b with n_b = kv_indptr[b+1] - kv_indptr[b]
+ * tokens, page p_j = kv_indices[kv_indptr[b] + j] and query head h:
+ *
+ *   s_j       = sm_scale * dot(q[b,h,:], k_cache[p_j,0,h/8,:])
+ *   out[b,h,:] = sum_j softmax(s)_j * v_cache[p_j,0,h/8,:]        (bf16, RNE)
+ *   lse[b,h]  = log2(sum_j exp(s_j))                              (fp32)
+ *
+ * An empty sequence (n_b == 0) gives out[b,:,:] = 0 and lse[b,:] = -inf (the
+ * early-exit step of that page's kernel). The log-sum-exp is base 2 of a
+ * natural-exponent sum, as that kernel stores it.
+ *
+ * Layouts (all row-major, contiguous, device memory owned by the caller):
+ *   q          [batch][32][128]          bf16, 16-byte aligned
+ *   k_cache    [num_pages][1][4][128]    bf16, 16-byte aligned
+ *   v_cache    [num_pages][1][4][128]    bf16, 16-byte aligned
+ *   kv_indptr  [batch + 1]               int32, kv_indptr[0] == 0, non-decreasing
+ *   kv_indices [kv_indptr[batch]]        int32, each in [0, num_pages)
+ *   out        [batch][32][128]          bf16, 16-byte aligned (written)
+ *   lse        [batch][32]               fp32, 8-byte aligned (written)
+ *
+ * k_cache, v_cache and kv_indices may be NULL only when kv_indptr[batch] == 0.
+ *
+ * Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ * stream) and never synchronise the host: the kv_indptr / kv_indices
+ * preconditions are not checked by gqa_paged_decode (see
+ * gqa_paged_decode_checked). The library owns only its workspace (fp32 split
+ * partials); calls that share the library-owned workspace must be ordered on
+ * one stream. Calls on different streams at the same time must each pass
+ * their own workspace through gqa_paged_decode_ws.
+ *
+ * Return codes: 0 success; negative values below. No exception crosses the ABI.
+ */
+#ifndef GQA_PAGED_DECODE_H_
+#define GQA_PAGED_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is struct CUstream_st* */
+
+#define GQA_OK 0
+#define GQA_ERR_INVALID_ARGUMENT (-1)   /* null/misaligned pointer, batch < 0, non-finite sm_scale, bad tuning */
+#define GQA_ERR_WORKSPACE (-2)          /* workspace allocation failed or caller workspace too small */
+#define GQA_ERR_LAUNCH (-3)             /* a CUDA call or kernel launch failed */
+#define GQA_ERR_UNSUPPORTED_DEVICE (-4) /* not a compute capability 10.3 (GB300) device */
+
+/*
+ * Paged GQA decode (the problem's run(q, k_cache, v_cache, kv_indptr,
+ * kv_indices, sm_scale) with caller-allocated out / lse). Launches, in order
+ * on `stream`: the split-KV decode kernel (each CTA streams an equal share of
+ * all cached tokens, split points chosen on the device from kv_indptr) and the
+ * LSE merge kernel (combines the pieces of sequences cut at a CTA boundary and
+ * writes empty sequences). batch == 0 returns 0 without launching anything.
+ * sm_scale is used as given (the problem's default is 1/sqrt(128)).
+ */
+int gqa_paged_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_indptr,
+                     const int32_t* kv_indices, float sm_scale, void* out, float* lse, int batch,
+                     struct CUstream_st* stream);
+
+/*
+ * Workspace bytes gqa_paged_decode_ws needs on the current device with the
+ * current tuning. The split plan bounds the partials by the number of decode
+ * CTAs (two slots each), so the size does not grow with batch or
+ * total_tokens_upper_bound; both are accepted so callers can size for a
+ * workload. Returns 0 if the device cannot be queried.
+ */
+size_t gqa_paged_decode_ws_size(int batch, int64_t total_tokens_upper_bound);
+
+/*
+ * As gqa_paged_decode, with a caller-owned device workspace of at least
+ * gqa_paged_decode_ws_size() bytes (256-byte aligned). Returns
+ * GQA_ERR_WORKSPACE if it is too small. Use one workspace per concurrent stream.
+ */
+int gqa_paged_decode_ws(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_indptr,
+                        const int32_t* kv_indices, float sm_scale, void* out, float* lse, int batch,
+                        struct CUstream_st* stream, void* workspace, size_t workspace_bytes);
+
+/*
+ * Debug variant: first checks on the device that kv_indptr starts at 0 and
+ * never decreases and that every kv_indices entry lies in [0, num_pages).
+ * The result is written to the caller's device int `dev_err` (0 = valid,
+ * otherwise bit 4 = bad page id, bit 8 = bad kv_indptr); if it is nonzero the
+ * decode and merge kernels return without reading K/V or writing out/lse.
+ * Read dev_err after synchronising `stream`. num_pages must be > 0.
+ */
+int gqa_paged_decode_checked(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_indptr,
+                             const int32_t* kv_indices, float sm_scale, void* out, float* lse, int batch,
+                             struct CUstream_st* stream, int num_pages, int* dev_err);
+
+/* Free the library-owned workspace on every device (synchronises those devices). */
+void gqa_paged_decode_release(void);
+
+/* Static description of a return code. */
+const char* gqa_paged_decode_strerror(int code);
+
+/*
+ * Tuning for tests and benchmarks (process-wide; 0 keeps the default):
+ * num_ctas - decode CTAs per call, at most 1536 (default: SMs x CTAs per SM);
+ * min_units_per_cta - smallest share of (token, head group) units a CTA takes
+ *   (default 128); smaller values cut sequences into more pieces;
+ * heads_per_cta - KV heads per CTA: 4 (1 KB page rows), 2 or 1 (256 B rows);
+ * tile, stages - tokens per pipeline stage (16 or 32) and ring depth.
+ * Returns GQA_ERR_INVALID_ARGUMENT for an unsupported combination.
+ */
+int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_per_cta, int tile, int stages);
+
+/*
+ * Profiling hook: when both are non-NULL (cudaEvent_t handles), every later
+ * call records `decode_start` just before and `decode_stop` just after the
+ * decode kernel on its stream (the merge launch then waits for the decode
+ * grid to finish instead of overlapping its launch). Pass NULLs to clear.
+ */
+int gqa_paged_decode_set_profile_events(void* decode_start, void* decode_stop);
+
+/*
+ * Synchronise the current device, then read and clear the sticky device error
+ * word: bit 1 / 2 = a pipeline wait gave up after ~2 s (the kernel returned
+ * early), bit 4 = bad page id, bit 8 = bad kv_indptr. 0 means no error.
+ */
+int gqa_paged_decode_device_error(int* flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_PAGED_DECODE_H_ */

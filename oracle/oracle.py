@@ -96,11 +96,11 @@ def gqa_paged_decode_oracle(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale
         lo, hi = int(indptr[b]), int(indptr[b + 1])
         pages = torch.as_tensor(np.asarray(indices[lo:hi], dtype=np.int64))
         qb = _f64(q[b])                                   # [32, 128]
+        kb = _f64(_gather(k_cache, pages))                # [n, 4, 128]
+        vb = _f64(_gather(v_cache, pages))
         for g in range(NUM_KV_HEADS):
-            k = _f64(_gather(k_cache, pages, g))          # [n, 128]
-            v = _f64(_gather(v_cache, pages, g))
             heads = slice(g * GQA_GROUP, (g + 1) * GQA_GROUP)
-            out[b, heads], lse[b, heads] = attend_rows(qb[heads], k, v, sm_scale)
+            out[b, heads], lse[b, heads] = attend_rows(qb[heads], kb[:, g, :], vb[:, g, :], sm_scale)
     return out, lse
 
 
@@ -123,11 +123,11 @@ def merge_partials(parts: Sequence[Tuple[np.ndarray, np.ndarray]]) -> Tuple[np.n
     return o, lse
 
 
-def _gather(cache, pages: torch.Tensor, g: int):
-    """Rows cache[p, 0, g, :] for the pages of one sequence (page size 1)."""
+def _gather(cache, pages: torch.Tensor):
+    """Pages cache[p, 0, :, :] of one sequence (page size 1): [n, 4, 128]."""
     if isinstance(cache, torch.Tensor):
-        return cache.index_select(0, pages)[:, 0, g, :]
-    return np.asarray(cache)[pages.numpy(), 0, g, :]
+        return cache.index_select(0, pages)[:, 0, :, :]
+    return np.asarray(cache)[pages.numpy(), 0, :, :]
 
 
 def _as_np_int(x) -> np.ndarray:

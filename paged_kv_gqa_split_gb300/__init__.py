@@ -1,0 +1,10 @@
+"""GB300 (sm_103a) paged-KV GQA decode: h32 / kv4 / d128 / page size 1, bf16.
+
+``run(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale=None) -> (out, lse)``
+calls the CUDA library through its C ABI (include/gqa_paged_decode.h). The
+library is built in-tree by ``paged_kv_gqa_split_gb300.build.build()``; it is
+loaded on first use, and every call fails loudly if it is missing.
+"""
+from ._lib import GqaError, run, run_checked  # noqa: F401
+
+__all__ = ["GqaError", "run", "run_checked"]

@@ -1,0 +1,207 @@
+"""ctypes binding of the C ABI in include/gqa_paged_decode.h.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library. The functions named like the C entry points take raw device pointers
+(ints) and return the C status code; ``run`` is the tensor-level convenience
+that mirrors the problem's ``run(q, k_cache, v_cache, kv_indptr, kv_indices,
+sm_scale)`` (kernelindex.com page "gqa_paged_decode_h32_kv4_d128_ps1") with
+caller-visible outputs. There is no CPU path: CPU tensors, or a missing
+library, raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgqa_paged_decode.so")
+
+GQA_OK = 0
+GQA_ERR_INVALID_ARGUMENT = -1
+GQA_ERR_WORKSPACE = -2
+GQA_ERR_LAUNCH = -3
+GQA_ERR_UNSUPPORTED_DEVICE = -4
+
+NUM_QO_HEADS, NUM_KV_HEADS, HEAD_DIM, PAGE_SIZE = 32, 4, 128, 1
+
+_vp = ctypes.c_void_p
+_SIGNATURES = {
+    "gqa_paged_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_int, _vp]),
+    "gqa_paged_decode_ws_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int64]),
+    "gqa_paged_decode_ws": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_int, _vp,
+                                           _vp, ctypes.c_size_t]),
+    "gqa_paged_decode_checked": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_int,
+                                                _vp, ctypes.c_int, _vp]),
+    "gqa_paged_decode_release": (None, []),
+    "gqa_paged_decode_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "gqa_paged_decode_set_tuning": (ctypes.c_int, [ctypes.c_int] * 5),
+    "gqa_paged_decode_set_profile_events": (ctypes.c_int, [_vp, _vp]),
+    "gqa_paged_decode_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class GqaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where} failed with {code}: {strerror(code)}")
+        self.code = code
+
+
+def load() -> ctypes.CDLL:
+    """Load the shared library (built by ``paged_kv_gqa_split_gb300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m paged_kv_gqa_split_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+# ------------------------------------------------------ C entry points, 1:1
+def gqa_paged_decode(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream) -> int:
+    return load().gqa_paged_decode(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream)
+
+
+def gqa_paged_decode_ws_size(batch: int, total_tokens_upper_bound: int) -> int:
+    return load().gqa_paged_decode_ws_size(batch, total_tokens_upper_bound)
+
+
+def gqa_paged_decode_ws(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream,
+                        workspace, workspace_bytes) -> int:
+    return load().gqa_paged_decode_ws(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream,
+                                      workspace, workspace_bytes)
+
+
+def gqa_paged_decode_checked(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream,
+                             num_pages, dev_err) -> int:
+    return load().gqa_paged_decode_checked(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch,
+                                           stream, num_pages, dev_err)
+
+
+def gqa_paged_decode_release() -> None:
+    load().gqa_paged_decode_release()
+
+
+def gqa_paged_decode_strerror(code: int) -> str:
+    return load().gqa_paged_decode_strerror(code).decode()
+
+
+strerror = gqa_paged_decode_strerror
+
+
+def gqa_paged_decode_set_tuning(num_ctas=0, min_units_per_cta=0, heads_per_cta=0, tile=0, stages=0) -> int:
+    return load().gqa_paged_decode_set_tuning(num_ctas, min_units_per_cta, heads_per_cta, tile, stages)
+
+
+def gqa_paged_decode_set_profile_events(decode_start, decode_stop) -> int:
+    return load().gqa_paged_decode_set_profile_events(decode_start, decode_stop)
+
+
+def gqa_paged_decode_device_error() -> int:
+    flags = ctypes.c_int(0)
+    rc = load().gqa_paged_decode_device_error(ctypes.byref(flags))
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_paged_decode_device_error")
+    return flags.value
+
+
+# ------------------------------------------------------------- tensor level
+def _check_inputs(q, k_cache, v_cache, kv_indptr, kv_indices):
+    """Shape / constant checks of the problem's run() wrapper, plus dtype,
+    device and contiguity (no host sync: kv_indptr[-1] is not read)."""
+    tensors = {"q": q, "k_cache": k_cache, "v_cache": v_cache, "kv_indptr": kv_indptr, "kv_indices": kv_indices}
+    for name, t in tensors.items():
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if not t.is_cuda:
+            raise ValueError(f"{name} is on {t.device}: the CUDA library has no CPU path; move inputs to the GPU")
+        if t.device != q.device:
+            raise ValueError(f"all inputs must be on {q.device}; {name} is on {t.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("expected q [B, 32, 128] and k_cache / v_cache [P, 1, 4, 128]")
+    batch, heads, dim = q.shape
+    _, page_size, kv_heads, kdim = k_cache.shape
+    if heads != NUM_QO_HEADS:
+        raise ValueError(f"expected num_qo_heads=32, got {heads}")
+    if kv_heads != NUM_KV_HEADS:
+        raise ValueError(f"expected num_kv_heads=4, got {kv_heads}")
+    if dim != HEAD_DIM or kdim != HEAD_DIM:
+        raise ValueError(f"expected head_dim=128, got {dim}/{kdim}")
+    if page_size != PAGE_SIZE:
+        raise ValueError(f"expected page_size=1, got {page_size}")
+    for name in ("q", "k_cache", "v_cache"):
+        if tensors[name].dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16")
+    for name in ("kv_indptr", "kv_indices"):
+        if tensors[name].dtype != torch.int32:
+            raise ValueError(f"{name} must be int32")
+    if kv_indptr.shape != (batch + 1,):
+        raise ValueError(f"expected kv_indptr shape {(batch + 1,)}, got {tuple(kv_indptr.shape)}")
+    if kv_indices.dim() != 1:
+        raise ValueError("kv_indices must be 1-D")
+    return batch
+
+
+def run(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, kv_indptr: torch.Tensor,
+        kv_indices: torch.Tensor, sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+        lse: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+        workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Paged GQA decode on the GPU. Returns (out [B, 32, 128] bf16, lse [B, 32] fp32, base 2)."""
+    batch = _check_inputs(q, k_cache, v_cache, kv_indptr, kv_indices)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((batch, NUM_QO_HEADS), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() or out.device != q.device:
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q on q's device")
+    if lse.shape != (batch, NUM_QO_HEADS) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor [B, 32]")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        args = (q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), kv_indptr.data_ptr(), kv_indices.data_ptr(),
+                float(sm_scale), out.data_ptr(), lse.data_ptr(), batch, stream.cuda_stream)
+        if workspace is None:
+            rc = gqa_paged_decode(*args)
+            where = "gqa_paged_decode"
+        else:
+            rc = gqa_paged_decode_ws(*args, workspace.data_ptr(), workspace.numel() * workspace.element_size())
+            where = "gqa_paged_decode_ws"
+    if rc != GQA_OK:
+        raise GqaError(rc, where)
+    return out, lse
+
+
+def run_checked(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale=None, out=None, lse=None):
+    """``run`` through the checked entry point. Returns (out, lse, dev_err) with
+    dev_err a device int32 tensor [1] (0 = the page table was valid)."""
+    batch = _check_inputs(q, k_cache, v_cache, kv_indptr, kv_indices)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((batch, NUM_QO_HEADS), dtype=torch.float32, device=q.device)
+    dev_err = torch.zeros(1, dtype=torch.int32, device=q.device)
+    stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        rc = gqa_paged_decode_checked(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), kv_indptr.data_ptr(),
+                                      kv_indices.data_ptr(), float(sm_scale), out.data_ptr(), lse.data_ptr(), batch,
+                                      stream.cuda_stream, int(k_cache.shape[0]), dev_err.data_ptr())
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_paged_decode_checked")
+    return out, lse, dev_err

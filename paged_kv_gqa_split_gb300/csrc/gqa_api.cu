@@ -1,0 +1,301 @@
+// C ABI of the paged GQA decode library: argument checks, device checks,
+// workspace ownership and the launch sequence (decode kernel, then the LSE
+// merge kernel with programmatic dependent launch). Mirrors the run() wrapper
+// of the kernelindex.com page "gqa_paged_decode_h32_kv4_d128_ps1" minus its
+// host-side moves and its kv_indptr[-1].item() synchronisation: every call is
+// asynchronous on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gqa_kernels.h"
+#include "gqa_paged_decode.h"
+#include "gqa_plan.h"
+
+namespace {
+
+using gqa::KernelChoice;
+
+constexpr int kMaxDevices = 64;
+constexpr int kDefaultMinUnits = 128;
+constexpr int kMergeCtasPerBoundary = 2;
+// Merge kernel keeps one LSE per (decode CTA, query head of a head group) in
+// shared memory: 1536 x 32 x 4 B = 192 KB at most.
+constexpr int kMaxDecodeCtas = 1536;
+constexpr int kSmemPerSm = 228 * 1024;
+constexpr int kSmemReservedPerCta = 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DeviceState {
+  bool queried = false;
+  int sm_count = 0;
+  int major = 0;
+  int minor = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+};
+
+struct Tuning {
+  int num_ctas = 0;
+  int min_units = 0;
+  KernelChoice kernel = {4, 16, 5};
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+Tuning g_tune;
+cudaEvent_t g_ev_start = nullptr;
+cudaEvent_t g_ev_stop = nullptr;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Fills *st for the current device (cached). Returns a GQA_* code.
+int current_device(int* dev_out, DeviceState** st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_LAUNCH;
+  DeviceState& s = g_dev[dev];
+  if (!s.queried) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return GQA_ERR_LAUNCH;
+    s.sm_count = prop.multiProcessorCount;
+    s.major = prop.major;
+    s.minor = prop.minor;
+    s.queried = true;
+  }
+  *dev_out = dev;
+  *st = &s;
+  if (s.major != 10 || s.minor != 3) return GQA_ERR_UNSUPPORTED_DEVICE;
+  return GQA_OK;
+}
+
+int decode_ctas(const DeviceState& st, const Tuning& t) {
+  if (t.num_ctas > 0) return t.num_ctas;
+  const int smem = gqa::decode_smem_bytes(t.kernel);
+  int per_sm = kSmemPerSm / (smem + kSmemReservedPerCta);
+  const int cap = gqa::kKvHeads / t.kernel.heads_per_cta;  // same warp count per SM for every NG
+  if (per_sm > cap) per_sm = cap;
+  if (per_sm < 1) per_sm = 1;
+  return st.sm_count * per_sm;
+}
+
+size_t partial_o_floats(int num_ctas, int ng) {
+  return static_cast<size_t>(2) * num_ctas * ng * gqa::kGroup * gqa::kHeadDim;
+}
+
+size_t workspace_bytes(int num_ctas, int ng) {
+  const size_t o = partial_o_floats(num_ctas, ng) * sizeof(float);
+  const size_t l = static_cast<size_t>(2) * num_ctas * ng * gqa::kGroup * sizeof(float);
+  return ((o + 255) & ~size_t(255)) + ((l + 255) & ~size_t(255));
+}
+
+int check_args(const void* q, const void* k, const void* v, const int32_t* indptr, const int32_t* indices,
+               float sm_scale, const void* out, const float* lse, int batch) {
+  if (batch < 0) return GQA_ERR_INVALID_ARGUMENT;
+  if (batch == 0) return GQA_OK;
+  if (q == nullptr || indptr == nullptr || out == nullptr || lse == nullptr) return GQA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(sm_scale)) return GQA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return GQA_ERR_INVALID_ARGUMENT;
+  if (!aligned(lse, 8) || !aligned(indptr, 4) || !aligned(indices, 4)) return GQA_ERR_INVALID_ARGUMENT;
+  return GQA_OK;
+}
+
+int run(const void* q, const void* k, const void* v, const int32_t* indptr, const int32_t* indices, float sm_scale,
+        void* out, float* lse, int batch, cudaStream_t stream, void* user_ws, size_t user_ws_bytes, bool checked,
+        int num_pages, int* dev_err) {
+  int rc = check_args(q, k, v, indptr, indices, sm_scale, out, lse, batch);
+  if (rc != GQA_OK) return rc;
+  if (batch == 0) return GQA_OK;
+  if (checked && (num_pages <= 0 || dev_err == nullptr || !aligned(dev_err, 4))) return GQA_ERR_INVALID_ARGUMENT;
+
+  int dev = 0;
+  DeviceState* st = nullptr;
+  Tuning tune;
+  cudaEvent_t ev0, ev1;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    rc = current_device(&dev, &st);
+    if (rc != GQA_OK) return rc;
+    tune = g_tune;
+    ev0 = g_ev_start;
+    ev1 = g_ev_stop;
+    const int ctas = decode_ctas(*st, tune);
+    const size_t need = workspace_bytes(ctas, tune.kernel.heads_per_cta);
+    if (user_ws != nullptr) {
+      if (user_ws_bytes < need || !aligned(user_ws, 256)) return GQA_ERR_WORKSPACE;
+      ws = user_ws;
+    } else {
+      if (st->ws_bytes < need) {
+        if (st->ws != nullptr) {
+          // calls already queued may still read the old buffer
+          if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_LAUNCH;
+          cudaFree(st->ws);
+          st->ws = nullptr;
+          st->ws_bytes = 0;
+        }
+        if (cudaMalloc(&st->ws, need) != cudaSuccess) {
+          cudaGetLastError();
+          st->ws = nullptr;
+          return GQA_ERR_WORKSPACE;
+        }
+        st->ws_bytes = need;
+      }
+      ws = st->ws;
+    }
+  }
+
+  const int ng = tune.kernel.heads_per_cta;
+  const int ctas = decode_ctas(*st, tune);
+  float* part_o = static_cast<float*>(ws);
+  float* part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                             ((partial_o_floats(ctas, ng) * sizeof(float) + 255) & ~size_t(255)));
+  const int min_units = tune.min_units > 0 ? tune.min_units : kDefaultMinUnits;
+
+  if (checked) {
+    if (cudaMemsetAsync(dev_err, 0, sizeof(int), stream) != cudaSuccess) return GQA_ERR_LAUNCH;
+    if (gqa::launch_validate(indptr, indices, batch, num_pages, dev_err, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
+  }
+
+  gqa::DecodeParams dp;
+  dp.q = q;
+  dp.k_cache = k;
+  dp.v_cache = v;
+  dp.kv_indptr = indptr;
+  dp.kv_indices = indices;
+  dp.out = out;
+  dp.lse = lse;
+  dp.part_o = part_o;
+  dp.part_lse = part_lse;
+  dp.skip_if_set = checked ? dev_err : nullptr;
+  dp.batch = batch;
+  dp.min_units = min_units;
+  dp.scale_log2 = sm_scale * kLog2e;
+  dp.num_pages_check = checked ? num_pages : 0;
+
+  const bool profile = ev0 != nullptr && ev1 != nullptr;
+  if (profile && cudaEventRecord(ev0, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
+  if (gqa::launch_decode(tune.kernel, dp, ctas, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
+  if (profile && cudaEventRecord(ev1, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
+
+  gqa::MergeParams mp;
+  mp.kv_indptr = indptr;
+  mp.part_o = part_o;
+  mp.part_lse = part_lse;
+  mp.out = out;
+  mp.lse = lse;
+  mp.skip_if_set = checked ? dev_err : nullptr;
+  mp.batch = batch;
+  mp.num_decode_ctas = ctas;
+  mp.min_units = min_units;
+  mp.merge_ctas_per_boundary = kMergeCtasPerBoundary;
+  mp.use_pdl = profile ? 0 : 1;
+  if (gqa::launch_merge(ng, mp, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
+  return GQA_OK;
+}
+
+bool valid_kernel(const KernelChoice& k) { return gqa::decode_smem_bytes(k) > 0; }
+
+}  // namespace
+
+extern "C" {
+
+int gqa_paged_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_indptr,
+                     const int32_t* kv_indices, float sm_scale, void* out, float* lse, int batch,
+                     struct CUstream_st* stream) {
+  return run(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream, nullptr, 0, false, 0,
+             nullptr);
+}
+
+size_t gqa_paged_decode_ws_size(int batch, int64_t total_tokens_upper_bound) {
+  (void)batch;
+  (void)total_tokens_upper_bound;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  DeviceState* st = nullptr;
+  const int rc = current_device(&dev, &st);
+  if (rc != GQA_OK && rc != GQA_ERR_UNSUPPORTED_DEVICE) return 0;
+  return workspace_bytes(decode_ctas(*st, g_tune), g_tune.kernel.heads_per_cta);
+}
+
+int gqa_paged_decode_ws(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_indptr,
+                        const int32_t* kv_indices, float sm_scale, void* out, float* lse, int batch,
+                        struct CUstream_st* stream, void* workspace, size_t workspace_bytes_) {
+  if (workspace == nullptr && batch > 0) return GQA_ERR_WORKSPACE;
+  return run(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream, workspace,
+             workspace_bytes_, false, 0, nullptr);
+}
+
+int gqa_paged_decode_checked(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_indptr,
+                             const int32_t* kv_indices, float sm_scale, void* out, float* lse, int batch,
+                             struct CUstream_st* stream, int num_pages, int* dev_err) {
+  return run(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream, nullptr, 0, true,
+             num_pages, dev_err);
+}
+
+void gqa_paged_decode_release(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return;
+  for (int d = 0; d < kMaxDevices; ++d) {
+    if (g_dev[d].ws == nullptr) continue;
+    if (cudaSetDevice(d) == cudaSuccess) {
+      cudaDeviceSynchronize();
+      cudaFree(g_dev[d].ws);
+    }
+    g_dev[d].ws = nullptr;
+    g_dev[d].ws_bytes = 0;
+  }
+  cudaSetDevice(cur);
+}
+
+const char* gqa_paged_decode_strerror(int code) {
+  switch (code) {
+    case GQA_OK:
+      return "success";
+    case GQA_ERR_INVALID_ARGUMENT:
+      return "invalid argument (null or misaligned pointer, negative batch, non-finite sm_scale or bad tuning)";
+    case GQA_ERR_WORKSPACE:
+      return "workspace allocation failed or the caller's workspace is too small";
+    case GQA_ERR_LAUNCH:
+      return "CUDA call or kernel launch failed";
+    case GQA_ERR_UNSUPPORTED_DEVICE:
+      return "unsupported device: the kernels are built for compute capability 10.3 (sm_103a)";
+    default:
+      return "unknown error code";
+  }
+}
+
+int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_per_cta, int tile, int stages) {
+  if (num_ctas < 0 || min_units_per_cta < 0 || heads_per_cta < 0 || tile < 0 || stages < 0)
+    return GQA_ERR_INVALID_ARGUMENT;
+  if (num_ctas > kMaxDecodeCtas) return GQA_ERR_INVALID_ARGUMENT;
+  Tuning t;
+  t.num_ctas = num_ctas;
+  t.min_units = min_units_per_cta;
+  t.kernel.heads_per_cta = heads_per_cta > 0 ? heads_per_cta : 4;
+  t.kernel.tile = tile > 0 ? tile : 16;
+  t.kernel.stages = stages > 0 ? stages : (t.kernel.heads_per_cta == 4 && t.kernel.tile == 16 ? 5 : 4);
+  if (t.kernel.tile == 32 && stages == 0) t.kernel.stages = 3;
+  if (!valid_kernel(t.kernel)) return GQA_ERR_INVALID_ARGUMENT;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_tune = t;
+  return GQA_OK;
+}
+
+int gqa_paged_decode_set_profile_events(void* decode_start, void* decode_stop) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_ev_start = static_cast<cudaEvent_t>(decode_start);
+  g_ev_stop = static_cast<cudaEvent_t>(decode_stop);
+  return GQA_OK;
+}
+
+int gqa_paged_decode_device_error(int* flags) {
+  if (flags == nullptr) return GQA_ERR_INVALID_ARGUMENT;
+  if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_LAUNCH;
+  return gqa::read_and_clear_device_error(flags) == cudaSuccess ? GQA_OK : GQA_ERR_LAUNCH;
+}
+
+}  // extern "C"

@@ -1,0 +1,107 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every
+declared entry point, and rejects bad arguments before touching the device."""
+import os
+import re
+
+import pytest
+
+from paged_kv_gqa_split_gb300 import _lib
+from paged_kv_gqa_split_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa_paged_decode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gqa_paged_decode\w*)\s*\(", text)))
+
+
+def test_header_declares_the_problem_entry_point():
+    names = declared_functions()
+    assert "gqa_paged_decode" in names
+    assert len(names) >= 8
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib._SIGNATURES, f"{name} has no binding"
+
+
+def test_binding_names_match_header():
+    assert sorted(_lib._SIGNATURES) == declared_functions()
+
+
+def test_strerror(lib):
+    assert _lib.strerror(0) == "success"
+    for code in (-1, -2, -3, -4):
+        assert len(_lib.strerror(code)) > 10
+    assert _lib.strerror(-99) == "unknown error code"
+
+
+def test_batch_zero_is_a_noop(lib):
+    assert _lib.gqa_paged_decode(None, None, None, None, None, 0.1, None, None, 0, None) == 0
+
+
+def test_negative_batch_rejected(lib):
+    assert _lib.gqa_paged_decode(16, 16, 16, 16, 16, 0.1, 16, 16, -1, None) == _lib.GQA_ERR_INVALID_ARGUMENT
+
+
+def test_null_pointers_rejected(lib):
+    a = 1 << 20  # a 256-aligned dummy address; never dereferenced on this path
+    args = [a, a, a, a, a, 0.1, a, a, 3, None]
+    for i in (0, 3, 6, 7):
+        bad = list(args)
+        bad[i] = None
+        assert _lib.gqa_paged_decode(*bad) == _lib.GQA_ERR_INVALID_ARGUMENT, i
+
+
+@pytest.mark.parametrize("scale", [float("nan"), float("inf"), float("-inf")])
+def test_non_finite_scale_rejected(lib, scale):
+    a = 1 << 20
+    assert _lib.gqa_paged_decode(a, a, a, a, a, scale, a, a, 3, None) == _lib.GQA_ERR_INVALID_ARGUMENT
+
+
+def test_misaligned_pointers_rejected(lib):
+    a = 1 << 20
+    for i, off in ((0, 8), (1, 2), (2, 4), (6, 8), (7, 4), (3, 2), (4, 1)):
+        args = [a, a, a, a, a, 0.1, a, a, 3, None]
+        args[i] = a + off
+        assert _lib.gqa_paged_decode(*args) == _lib.GQA_ERR_INVALID_ARGUMENT, (i, off)
+
+
+def test_checked_needs_pages_and_flag(lib):
+    a = 1 << 20
+    assert _lib.gqa_paged_decode_checked(a, a, a, a, a, 0.1, a, a, 2, None, 0, a) == _lib.GQA_ERR_INVALID_ARGUMENT
+    assert _lib.gqa_paged_decode_checked(a, a, a, a, a, 0.1, a, a, 2, None, 5, None) == _lib.GQA_ERR_INVALID_ARGUMENT
+
+
+def test_ws_variant_needs_workspace(lib):
+    a = 1 << 20
+    assert _lib.gqa_paged_decode_ws(a, a, a, a, a, 0.1, a, a, 2, None, None, 0) == _lib.GQA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("tuning", [(0, 0, 3, 0, 0), (0, 0, 4, 24, 0), (0, 0, 4, 16, 9), (-1, 0, 0, 0, 0)])
+def test_unsupported_tuning_rejected(lib, tuning):
+    assert _lib.gqa_paged_decode_set_tuning(*tuning) == _lib.GQA_ERR_INVALID_ARGUMENT
+
+
+def test_default_tuning_accepted(lib):
+    assert _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0) == 0
+
+
+def test_cpu_tensors_raise():
+    import torch
+    from paged_kv_gqa_split_gb300 import workloads as wl
+    w = wl.make_workload([3, 4], seed=1)
+    with pytest.raises(ValueError, match="no CPU path"):
+        _lib.run(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices)
+    assert torch.is_tensor(w.q)

@@ -1,0 +1,279 @@
+"""GPU parity: the CUDA library (through its C ABI) against the float64 oracle.
+
+Tolerance (stated for this path): |dO| <= 2e-2 + 2e-2 * |O_ref| elementwise and
+|dlse| <= 1e-3 absolute, with -inf == -inf for empty sequences.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import gqa_paged_decode_oracle
+from paged_kv_gqa_split_gb300 import _lib
+from paged_kv_gqa_split_gb300 import workloads as wl
+from paged_kv_gqa_split_gb300.build import build
+
+pytestmark = pytest.mark.gpu
+
+O_ATOL, O_RTOL, LSE_ATOL = 2e-2, 2e-2, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library(cuda_device):
+    build()
+    _lib.load()
+    yield
+    _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0)
+
+
+@pytest.fixture
+def tuning():
+    """Apply a tuning for one test and restore the defaults afterwards."""
+    def apply(*args):
+        assert _lib.gqa_paged_decode_set_tuning(*args) == 0
+    yield apply
+    assert _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0) == 0
+
+
+def gpu_run(w, dev="cuda"):
+    g = w.to(dev)
+    out, lse = _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, w.sm_scale)
+    torch.cuda.synchronize()
+    return out.float().cpu().double().numpy(), lse.cpu().double().numpy()
+
+
+def check(w, out, lse, seqs=None, ref=None):
+    if ref is None:
+        ref = gqa_paged_decode_oracle(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices, w.sm_scale, seqs=seqs)
+    o_ref, l_ref = ref
+    rows = list(range(w.batch)) if seqs is None else list(seqs)
+    o, l, orf, lrf = out[rows], lse[rows], o_ref[rows], l_ref[rows]
+    err = np.abs(o - orf)
+    bad = err > O_ATOL + O_RTOL * np.abs(orf)
+    assert not bad.any(), f"O mismatch at {np.argwhere(bad)[:5].tolist()}: max err {err.max():.3e}"
+    assert np.array_equal(np.isneginf(l), np.isneginf(lrf)), "empty-sequence LSE mismatch"
+    fin = np.isfinite(lrf)
+    assert np.all(np.isfinite(l[fin]))
+    lerr = np.abs(l[fin] - lrf[fin]) if fin.any() else np.zeros(1)
+    assert lerr.max() <= LSE_ATOL, f"LSE max err {lerr.max():.3e}"
+    for b in rows:
+        if w.lens and w.lens[b] == 0:
+            assert np.all(out[b] == 0.0)
+    return float(err.max()), float(lerr.max())
+
+
+# ------------------------------------------------------------ small fixed cases
+def test_pattern_workload_matches_golden():
+    w = wl.make_pattern_workload()
+    out, lse = gpu_run(w)
+    path = os.path.join(os.path.dirname(__file__), "golden", "pattern_oracle.json")
+    doc = json.load(open(path))
+    want_l = np.array(doc["lse"], dtype=np.float64)
+    assert np.array_equal(np.isneginf(lse), np.isneginf(want_l))
+    fin = np.isfinite(want_l)
+    assert np.abs(lse[fin] - want_l[fin]).max() <= LSE_ATOL
+    for key, row in doc["o_rows"].items():
+        b, h = (int(x) for x in key.split(","))
+        row = np.array(row)
+        assert np.all(np.abs(out[b, h] - row) <= O_ATOL + O_RTOL * np.abs(row))
+    assert np.all(out[1] == 0.0)
+
+
+EDGE_LENS = {
+    "single_token": [1],
+    "one_empty": [0],
+    "all_empty": [0, 0, 0],
+    "ones": [1] * 7,
+    "around_16": [15, 16, 17],
+    "around_32": [31, 32, 33],
+    "ramp_1_40": list(range(1, 41)),
+    "leading_trailing_empty": [0, 0, 5, 0, 300, 0, 0],
+    "around_256": [255, 256, 257, 0, 129],
+    "ragged_mix": [3, 1000, 0, 77, 2049, 1, 16, 600],
+}
+
+
+@pytest.mark.parametrize("name", sorted(EDGE_LENS))
+def test_edge_cases_default(name):
+    w = wl.make_workload(EDGE_LENS[name], seed=100 + len(name), pool_factor=1.5)
+    out, lse = gpu_run(w)
+    check(w, out, lse)
+
+
+VARIANTS = {
+    "ng4_tile16_s4": (0, 0, 4, 16, 4),
+    "ng4_tile32_s3": (0, 0, 4, 32, 3),
+    "ng2_tile16_s4": (0, 0, 2, 16, 4),
+    "ng1_tile16_s4": (0, 0, 1, 16, 4),
+    "ng4_few_ctas": (7, 0, 4, 16, 5),
+    "ng4_small_units": (0, 16, 4, 16, 5),
+    "ng1_small_units": (0, 16, 1, 16, 4),
+    "ng4_tile32_small_units": (0, 16, 4, 32, 3),
+    "one_cta": (1, 0, 4, 16, 5),
+}
+
+
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
+@pytest.mark.parametrize("case", ["ragged_mix", "leading_trailing_empty", "ramp_1_40"])
+def test_kernel_variants(tuning, variant, case):
+    tuning(*VARIANTS[variant])
+    w = wl.make_workload(EDGE_LENS[case], seed=7, pool_factor=1.25)
+    out, lse = gpu_run(w)
+    check(w, out, lse)
+
+
+@pytest.mark.parametrize("num_ctas,min_units", [(152, 16), (40, 16), (300, 1), (3, 1)])
+def test_split_and_merge_paths(tuning, num_ctas, min_units):
+    """One long and several short sequences cut into up to ~300 pieces: both merge paths
+    (<= 16 and > 16 partials per sequence) and many sequences per CTA."""
+    tuning(num_ctas, min_units, 4, 16, 5)
+    w = wl.make_workload([5000, 3, 17, 0, 900, 1, 64], seed=21, pool_factor=1.1)
+    out, lse = gpu_run(w)
+    check(w, out, lse)
+
+
+@pytest.mark.parametrize("variant", [(200, 8, 4, 16, 5), (600, 8, 1, 16, 4), (120, 8, 2, 16, 4), (90, 8, 4, 32, 3)])
+def test_token_count_exact_with_uniform_scores(tuning, variant):
+    """q = 0 makes every score 0: lse must be log2(n) to fp32 precision, which a
+    dropped or doubled token would break (1.44/n >> 2e-5 for n <= 9000), and O
+    must be the mean of the sequence's V rows."""
+    tuning(*variant)
+    lens = [9000, 1, 2, 3, 4000, 0, 17, 1023, 1024, 1025, 5]
+    w = wl.make_workload(lens, seed=33, pool_factor=1.0)
+    w.q.zero_()
+    out, lse = gpu_run(w)
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert np.all(np.isneginf(lse[b]))
+        else:
+            assert np.abs(lse[b] - math.log2(n)).max() < 2e-5, (b, n, lse[b][:4])
+    check(w, out, lse)
+
+
+def test_peaky_softmax_large_scores():
+    w = wl.make_workload([700, 64, 3], seed=44, q_std=30.0)
+    out, lse = gpu_run(w)
+    check(w, out, lse)
+
+
+def test_deterministic_bitwise():
+    w = wl.make_workload([1000, 0, 333, 4096], seed=45)
+    g = w.to("cuda")
+    o1, l1 = _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices)
+    o2, l2 = _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_int64_page_addressing():
+    """Pages above 2^21 sit more than 2^31 bytes into each 1 KB-per-page pool."""
+    num_pages = (1 << 21) + 4096
+    small = wl.make_workload([40, 0, 300], seed=46, pool_factor=1.0)
+    g = torch.Generator().manual_seed(5)
+    high = torch.randperm(num_pages - (1 << 21), generator=g)[: small.total_tokens] + (1 << 21)
+    high[0] = num_pages - 1
+    k = torch.zeros((num_pages, 1, 4, 128), dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(k)
+    k[high.cuda()] = small.k_cache[small.kv_indices.long()].cuda()
+    v[high.cuda()] = small.v_cache[small.kv_indices.long()].cuda()
+    q = small.q.cuda()
+    out, lse = _lib.run(q, k, v, small.kv_indptr.cuda(), high.to(torch.int32).cuda(), small.sm_scale)
+    torch.cuda.synchronize()
+    check(small, out.float().cpu().double().numpy(), lse.cpu().double().numpy())
+    del k, v
+
+
+# ----------------------------------------------------------- entry variants
+def test_workspace_variant_matches_and_rejects_small():
+    w = wl.make_workload([2000, 5, 0, 700], seed=47)
+    g = w.to("cuda")
+    need = _lib.gqa_paged_decode_ws_size(w.batch, w.total_tokens)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    o1, l1 = _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices)
+    o2, l2 = _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    small = torch.empty(need // 2, dtype=torch.uint8, device="cuda")
+    with pytest.raises(_lib.GqaError) as e:
+        _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, workspace=small)
+    assert e.value.code == _lib.GQA_ERR_WORKSPACE
+
+
+def test_checked_valid_matches_unchecked():
+    w = wl.make_workload([129, 0, 64, 1000], seed=48, pool_factor=1.3)
+    g = w.to("cuda")
+    o1, l1 = _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices)
+    o2, l2, err = _lib.run_checked(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_checked_rejects_bad_page_before_reading():
+    w = wl.make_workload([50, 20], seed=49)
+    g = w.to("cuda")
+    bad_idx = g.kv_indices.clone()
+    bad_idx[7] = w.num_pages  # one past the pool
+    out = torch.full_like(g.q, 7.0)
+    lse = torch.full((w.batch, 32), 7.0, device="cuda")
+    _, _, err = _lib.run_checked(g.q, g.k_cache, g.v_cache, g.kv_indptr, bad_idx, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 4
+    assert torch.all(out == 7.0) and torch.all(lse == 7.0)  # nothing was written
+
+
+def test_checked_rejects_decreasing_indptr():
+    w = wl.make_workload([10, 10, 10], seed=50)
+    g = w.to("cuda")
+    bad = g.kv_indptr.clone()
+    bad[1] = 25
+    bad[2] = 12  # decreasing; the last entry still equals len(kv_indices)
+    _, _, err = _lib.run_checked(g.q, g.k_cache, g.v_cache, bad, g.kv_indices)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 8
+
+
+def test_non_default_stream():
+    w = wl.make_workload([300, 7], seed=51)
+    g = w.to("cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out, lse = _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices)
+    s.synchronize()
+    check(w, out.float().cpu().double().numpy(), lse.cpu().double().numpy())
+
+
+# ------------------------------------------------------ the five workloads
+SAMPLES = {"tiny": None, "mid": 12, "long": None, "large": 10, "skewed": 16}
+
+
+def _sample(w, n):
+    if n is None:
+        return None
+    lens = np.array(w.lens)
+    order = np.argsort(lens)
+    pick = set(order[:3].tolist()) | set(order[-3:].tolist())
+    g = np.random.default_rng(0)
+    pick |= set(g.choice(w.batch, size=min(n, w.batch), replace=False).tolist())
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid", "long", "large", "skewed"])
+def test_workload_parity(name):
+    w = wl.make_config(name)
+    out, lse = gpu_run(w)
+    seqs = _sample(w, SAMPLES[name])
+    o_err, l_err = check(w, out, lse, seqs=seqs)
+    print(f"{name}: max |dO| {o_err:.3e}, max |dlse| {l_err:.3e}, sequences checked "
+          f"{w.batch if seqs is None else len(seqs)}")
+    # every row, checked or not, is finite (empty rows: zeros / -inf)
+    assert np.all(np.isfinite(out))
+    assert np.all(np.isfinite(lse) | np.isneginf(lse))
+
+
+def test_no_device_error_flagged():
+    assert _lib.gqa_paged_decode_device_error() == 0
