@@ -169,12 +169,19 @@ def ncu_traffic(workload: str, total_tokens: int):
 
 
 # ------------------------------------------------------------- our GPU arm
+# GPU-side spin before each timed step (~150 us at 2 GHz): the host enqueues the
+# step's launches while the GPU spins, so the events time GPU work, not host
+# latency between the start event and the first launch.
+HOST_LEAD_CYCLES = 300_000
+
+
 def time_steps(call, steps: int, stream, flush_buf, before=None):
     """Per-step device time (ms) of `call` with CUDA events on `stream`; L2 is flushed
     between steps outside the events."""
     times = []
     for i in range(steps):
         flush_buf.zero_()
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
         if before is not None:
             before(i)
         e0 = torch.cuda.Event(enable_timing=True)

@@ -110,11 +110,16 @@ const char* gqa_paged_decode_strerror(int code);
  * num_ctas - decode CTAs per call, at most 1536 (default: SMs x CTAs per SM);
  * min_units_per_cta - smallest share of (token, head group) units a CTA takes
  *   (default 128); smaller values cut sequences into more pieces;
- * heads_per_cta - KV heads per CTA: 4 (1 KB page rows), 2 or 1 (256 B rows);
- * tile, stages - tokens per pipeline stage (16 or 32) and ring depth.
- * Returns GQA_ERR_INVALID_ARGUMENT for an unsupported combination.
+ * heads_per_cta - KV heads per CTA: 4, 2 or 1 (one warp per KV head);
+ * tile, stages - tokens per pipeline stage and ring depth;
+ * gather - 0: every warp gathers its own 256-byte K/V head rows with 16-byte
+ *   cp.async (default: heads 4, tile 16, stages 3, 2 CTAs per SM);
+ *   1: one producer warp per CTA gathers whole page rows with TMA bulk copies
+ *   (tile 16 or 32).
+ * Returns GQA_ERR_INVALID_ARGUMENT for a combination that is not compiled in.
  */
-int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_per_cta, int tile, int stages);
+int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_per_cta, int tile, int stages,
+                                int gather);
 
 /*
  * Profiling hook: when both are non-NULL (cudaEvent_t handles), every later

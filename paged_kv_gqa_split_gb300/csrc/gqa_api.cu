@@ -21,9 +21,7 @@ using gqa::KernelChoice;
 
 constexpr int kMaxDevices = 64;
 constexpr int kDefaultMinUnits = 128;
-constexpr int kMergeCtasPerBoundary = 2;
-// Merge kernel keeps one LSE per (decode CTA, query head of a head group) in
-// shared memory: 1536 x 32 x 4 B = 192 KB at most.
+// Upper bound on decode CTAs a tuning may ask for.
 constexpr int kMaxDecodeCtas = 1536;
 constexpr int kSmemPerSm = 228 * 1024;
 constexpr int kSmemReservedPerCta = 1024;
@@ -41,7 +39,7 @@ struct DeviceState {
 struct Tuning {
   int num_ctas = 0;
   int min_units = 0;
-  KernelChoice kernel = {4, 16, 5};
+  KernelChoice kernel = {gqa::kGatherLsu, 4, 16, 3};
 };
 
 std::mutex g_mu;
@@ -75,7 +73,7 @@ int decode_ctas(const DeviceState& st, const Tuning& t) {
   if (t.num_ctas > 0) return t.num_ctas;
   const int smem = gqa::decode_smem_bytes(t.kernel);
   int per_sm = kSmemPerSm / (smem + kSmemReservedPerCta);
-  const int cap = gqa::kKvHeads / t.kernel.heads_per_cta;  // same warp count per SM for every NG
+  const int cap = gqa::decode_max_ctas_per_sm(t.kernel);
   if (per_sm > cap) per_sm = cap;
   if (per_sm < 1) per_sm = 1;
   return st.sm_count * per_sm;
@@ -159,6 +157,9 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
     if (gqa::launch_validate(indptr, indices, batch, num_pages, dev_err, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
   }
 
+  int* err_word = nullptr;
+  if (gqa::device_error_word(&err_word) != cudaSuccess) return GQA_ERR_LAUNCH;
+
   gqa::DecodeParams dp;
   dp.q = q;
   dp.k_cache = k;
@@ -170,6 +171,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   dp.part_o = part_o;
   dp.part_lse = part_lse;
   dp.skip_if_set = checked ? dev_err : nullptr;
+  dp.err = err_word;
   dp.batch = batch;
   dp.min_units = min_units;
   dp.scale_log2 = sm_scale * kLog2e;
@@ -190,7 +192,6 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   mp.batch = batch;
   mp.num_decode_ctas = ctas;
   mp.min_units = min_units;
-  mp.merge_ctas_per_boundary = kMergeCtasPerBoundary;
   mp.use_pdl = profile ? 0 : 1;
   if (gqa::launch_merge(ng, mp, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
   return GQA_OK;
@@ -268,17 +269,25 @@ const char* gqa_paged_decode_strerror(int code) {
   }
 }
 
-int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_per_cta, int tile, int stages) {
-  if (num_ctas < 0 || min_units_per_cta < 0 || heads_per_cta < 0 || tile < 0 || stages < 0)
+int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_per_cta, int tile, int stages,
+                                int gather) {
+  if (num_ctas < 0 || min_units_per_cta < 0 || heads_per_cta < 0 || tile < 0 || stages < 0 || gather < 0)
     return GQA_ERR_INVALID_ARGUMENT;
   if (num_ctas > kMaxDecodeCtas) return GQA_ERR_INVALID_ARGUMENT;
   Tuning t;
   t.num_ctas = num_ctas;
   t.min_units = min_units_per_cta;
+  t.kernel.gather = gather;
   t.kernel.heads_per_cta = heads_per_cta > 0 ? heads_per_cta : 4;
-  t.kernel.tile = tile > 0 ? tile : 16;
-  t.kernel.stages = stages > 0 ? stages : (t.kernel.heads_per_cta == 4 && t.kernel.tile == 16 ? 5 : 4);
-  if (t.kernel.tile == 32 && stages == 0) t.kernel.stages = 3;
+  if (gather == gqa::kGatherLsu) {
+    t.kernel.tile = tile > 0 ? tile : 16;
+    t.kernel.stages = stages > 0 ? stages : 3;
+  } else if (gather == gqa::kGatherTma) {
+    t.kernel.tile = tile > 0 ? tile : 16;
+    t.kernel.stages = stages > 0 ? stages : (t.kernel.tile == 32 ? 3 : (t.kernel.heads_per_cta == 4 ? 5 : 4));
+  } else {
+    return GQA_ERR_INVALID_ARGUMENT;
+  }
   if (!valid_kernel(t.kernel)) return GQA_ERR_INVALID_ARGUMENT;
   std::lock_guard<std::mutex> lock(g_mu);
   g_tune = t;

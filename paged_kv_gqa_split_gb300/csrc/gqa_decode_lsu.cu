@@ -1,0 +1,280 @@
+// Split-KV paged GQA decode, self-loading warps (the default decode kernel).
+//
+// Problem: the kernelindex.com page "gqa_paged_decode_h32_kv4_d128_ps1" (32
+// query heads over 4 KV heads, head_dim 128, page size 1, bf16, CSR page table,
+// bf16 O and base-2 LSE). Work split: gqa_plan.h (each CTA an equal share of
+// all (token, head group) units; pieces of a sequence cut at CTA boundaries
+// leave fp32 partials for the LSE merge kernel).
+//
+// Each warp owns one KV head of the CTA's head group and runs its own
+// pipeline, with no barrier shared with any other warp:
+//   * a walker cuts the CTA's unit range into 16-token tiles that never cross
+//     a sequence (the kv_indptr window is kept in registers and searched with
+//     warp ballots);
+//   * for each tile the warp gathers the 256-byte K and V rows of its head for
+//     the 16 tokens with 16-byte cp.async (two 256-byte rows per warp
+//     instruction, L2 only), into a D-deep ring of private stages; rows past
+//     the tile's end are zero-filled. Page ids come from a 256-entry ring in
+//     shared memory that is itself filled by cp.async 224 tokens ahead, so no
+//     global load sits on the issue path;
+//   * the tile D - 1 ahead is issued before the warp waits for the current
+//     one, so all D stages are in flight during the wait and D - 1 during the
+//     math;
+//   * a new piece's Q fragments are loaded into registers when its first tile
+//     is issued (or prefetched to L2 if the register set is still in use).
+// Measured on GB300 with random 1 KB pages: 16-byte cp.async gathers from 8
+// warps per SM reach ~94% of the copy bandwidth, TMA bulk copies of the same
+// rows ~60% at any ring depth; hence the LSU path here (the TMA variant is
+// gqa_decode_tma.cu).
+#include <cuda_runtime.h>
+
+#include "gqa_common.cuh"
+#include "gqa_kernels.h"
+
+namespace gqa {
+
+template <int NG, int D>
+struct LsuCfg {
+  static constexpr int kHG = kKvHeads / NG;           // head groups on the unit line
+  static constexpr int kTile = 16;                    // tokens per stage (one mma sub-tile)
+  static constexpr int kRowPitch = kHeadDim * 2 + 16; // 256 B head row + 16 B: ldmatrix rows hit all banks
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTile * kRowPitch;
+  static constexpr int kHdrOff = 2 * kTile * kRowPitch;
+  static constexpr int kStageBytes = kHdrOff + 16;
+  static constexpr int kIdsRing = 256;                // page ids held per warp (tokens)
+  static constexpr int kIdsOff = D * kStageBytes;
+  static constexpr int kWarpBytes = kIdsOff + kIdsRing * 4;
+  static constexpr int kThreads = NG * 32;
+  static constexpr int kSmemBytes = NG * kWarpBytes;
+  static_assert(D >= 2, "at least double buffering");
+  static_assert(kStageBytes % 16 == 0 && kWarpBytes % 16 == 0, "16-byte aligned stages");
+  static_assert(kSmemBytes <= 227 * 1024, "ring exceeds shared memory");
+};
+
+struct Tile {
+  int b, cnt, flags, hg, tt;
+};
+
+template <int NG, int D>
+__global__ void __launch_bounds__(NG * 32) gqa_decode_lsu_kernel(const DecodeParams p) {
+  using C = LsuCfg<NG, D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int w = threadIdx.x >> 5;  // KV head within the head group
+  const int lane = threadIdx.x & 31;
+  uint8_t* wsm = smem + w * C::kWarpBytes;
+  const uint32_t wbase = smem_addr(wsm);
+  const int* ids = reinterpret_cast<const int*>(wsm + C::kIdsOff);
+  const uint32_t ids_base = wbase + C::kIdsOff;
+
+  // The merge grid may become resident now; it waits for this grid to finish.
+  pdl_launch_dependents();
+  if (p.skip_if_set != nullptr && *p.skip_if_set != 0) return;
+
+  const uint8_t* __restrict__ kc = static_cast<const uint8_t*>(p.k_cache);
+  const uint8_t* __restrict__ vc = static_cast<const uint8_t*>(p.v_cache);
+  const __nv_bfloat16* __restrict__ qg = static_cast<const __nv_bfloat16*>(p.q);
+  const int B = p.batch;
+  const int T = __ldg(p.kv_indptr + B);
+  const int64_t W = static_cast<int64_t>(T) * C::kHG;
+  const int64_t q = units_per_cta(W, gridDim.x, p.min_units);
+  const int64_t u0 = static_cast<int64_t>(blockIdx.x) * q;
+  const int64_t u1 = min(u0 + q, W);
+
+  // ------------------------------------------------------------- walker
+  int64_t u_next = u0;      // first unit of the next head-group segment
+  bool seg_open = false, walk_ok = true;
+  int hg = 0, tt = 0, t_stop = 0;  // segment: tokens [tt, t_stop) of head group hg
+  int p_hi = 0, p_flags = 0, pb = 0;  // current piece: sequence pb, tokens up to p_hi
+  int wb = 0, win = 0;      // kv_indptr[wb + lane]
+  int ib = 0;               // page-id ring holds tokens [ib, ib + 256)
+
+  auto request_ids = [&](int pos) {  // page id of token pos into its ring slot (zero past the end)
+    cp_async_4(ids_base + (pos & (C::kIdsRing - 1)) * 4, p.kv_indices + min(pos, T - 1), pos < T ? 4u : 0u);
+  };
+
+  auto next_tile = [&](Tile& tl) -> bool {
+    while (walk_ok) {
+      if (seg_open && tt < t_stop) {
+        if (tt >= p_hi) {  // a new piece starts at tt: find its sequence
+          unsigned m;
+          for (;;) {
+            m = __ballot_sync(0xffffffffu, win <= tt);
+            if (m != 0xffffffffu) break;
+            wb += 31;
+            win = load_indptr_window(p.kv_indptr, B, wb, lane);
+          }
+          if (m == 0) {  // kv_indptr[wb] > tt: a decreasing table
+            if (lane == 0) atomicOr(p.err, kErrBadIndptr);
+            walk_ok = false;
+            break;
+          }
+          const int k = 31 - __clz(m);
+          pb = wb + k;
+          const int seq_lo = __shfl_sync(0xffffffffu, win, k);
+          const int seq_hi = __shfl_sync(0xffffffffu, win, k + 1);
+          p_hi = min(seq_hi, t_stop);
+          p_flags = F_QLOAD | ((tt == seq_lo && p_hi == seq_hi) ? F_FINAL : 0) |
+                    ((static_cast<int64_t>(hg) * T + tt != u0) ? F_SLOT1 : 0);
+        }
+        tl.cnt = min(C::kTile, p_hi - tt);
+        tl.flags = p_flags | ((tt + tl.cnt == p_hi) ? F_END : 0);
+        tl.b = pb;
+        tl.hg = hg;
+        tl.tt = tt;
+        p_flags &= ~F_QLOAD;
+        tt += tl.cnt;
+        return true;
+      }
+      if (u_next >= u1) return false;
+      // open the next head-group segment of the CTA's unit range
+      hg = static_cast<int>(u_next / T);
+      tt = static_cast<int>(u_next - static_cast<int64_t>(hg) * T);
+      t_stop = static_cast<int>(min(static_cast<int64_t>(T), u1 - static_cast<int64_t>(hg) * T));
+      u_next = static_cast<int64_t>(hg) * T + t_stop;
+      seg_open = true;
+      p_hi = tt;
+      wb = warp_find_seq(p.kv_indptr, B, tt, lane);
+      if (wb < 0) {
+        if (lane == 0) atomicOr(p.err, kErrBadIndptr);
+        walk_ok = false;
+        break;
+      }
+      win = load_indptr_window(p.kv_indptr, B, wb, lane);
+      ib = tt & ~31;
+#pragma unroll
+      for (int c = 0; c < C::kIdsRing / 32; ++c) request_ids(ib + 32 * c + lane);
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncwarp();
+    }
+    return false;
+  };
+
+  // -------------------------------------------------------------- issue
+  uint32_t qn[16];        // Q fragments of the next piece, loaded at issue time
+  bool qn_busy = false;
+  int issued = 0;
+  bool more = true;
+  auto issue = [&]() {
+    const uint32_t sb = wbase + (issued % D) * C::kStageBytes;
+    Tile tl;
+    if (more && next_tile(tl)) {
+      // keep the ring at [ib, ib + 256) with tl.tt < ib + 32: the ids this tile
+      // reads were requested >= 12 tiles ago and have completed
+      while (tl.tt >= ib + 32) {
+        request_ids(ib + C::kIdsRing + lane);
+        ib += 32;
+      }
+      int flags = tl.flags;
+      const int64_t hoff = static_cast<int64_t>(tl.hg * NG + w) * (kHeadDim * 2);
+      const int pc = lane & 15;  // 16-byte column of the 256-byte head row
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int tok = 2 * i + (lane >> 4);
+        bool valid = tok < tl.cnt;
+        int pg = valid ? ids[(tl.tt + tok) & (C::kIdsRing - 1)] : 0;
+        if (valid && p.num_pages_check > 0 && static_cast<unsigned>(pg) >= static_cast<unsigned>(p.num_pages_check)) {
+          atomicOr(p.err, kErrBadPage);
+          valid = false;
+          pg = 0;
+        }
+        const int64_t off = static_cast<int64_t>(pg) * kPageBytes + hoff + pc * 16;
+        const uint32_t nbytes = valid ? 16u : 0u;
+        cp_async_16(sb + C::kKOff + tok * C::kRowPitch + pc * 16, kc + off, nbytes);
+        cp_async_16(sb + C::kVOff + tok * C::kRowPitch + pc * 16, vc + off, nbytes);
+      }
+      if (flags & F_QLOAD) {
+        const int h0 = (tl.hg * NG + w) * kGroup;
+        if (!qn_busy) {
+          load_q_frags(qn, qg, tl.b, h0, lane);
+          qn_busy = true;
+          flags |= F_QREG;
+        } else if (lane < 16) {
+          prefetch_l2(qg + (static_cast<int64_t>(tl.b) * kQoHeads + h0) * kHeadDim + lane * 64);
+        }
+      }
+      if (lane == 0) st_shared_v4(sb + C::kHdrOff, tl.b, tl.cnt, flags, tl.hg);
+    } else if (more) {
+      more = false;
+      if (lane == 0) st_shared_v4(sb + C::kHdrOff, 0, 0, F_DONE, 0);
+    }
+    cp_async_commit();  // one group per issue, even when empty
+    ++issued;
+  };
+
+  // ------------------------------------------------------------ compute
+  HeadState st;
+  st.reset();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) st.qf[i] = 0;
+  const uint32_t k_lane = C::kKOff + ((lane & 7) + ((lane >> 3) & 1) * 8) * C::kRowPitch + (lane >> 4) * 16;
+  const uint32_t v_lane = C::kVOff + ((lane & 7) + (lane >> 4) * 8) * C::kRowPitch + ((lane >> 3) & 1) * 16;
+
+#pragma unroll 1
+  for (int i = 0; i < D - 1; ++i) issue();
+#pragma unroll 1
+  for (int k = 0;; ++k) {
+    issue();                 // tile k + D - 1, into the stage tile k - 1 used
+    cp_async_wait<D - 1>();  // tile k has landed (one group per tile)
+    __syncwarp();
+    const uint32_t sb = wbase + (k % D) * C::kStageBytes;
+    int hb, cnt, flags, thg;
+    ld_shared_v4(sb + C::kHdrOff, hb, cnt, flags, thg);
+    if (flags & F_DONE) break;
+    const int h0 = (thg * NG + w) * kGroup;
+    if (flags & F_QLOAD) {
+      if (flags & F_QREG) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) st.qf[i] = qn[i];
+        qn_busy = false;
+      } else {
+        load_q_frags(st.qf, qg, hb, h0, lane);
+      }
+      st.reset();
+    }
+    attend_subtile(st, sb + k_lane, sb + v_lane, cnt, p.scale_log2, lane);
+    if (flags & F_END) {
+      finish_piece<NG>(st, (flags & F_FINAL) != 0, hb, h0, slot_id(blockIdx.x, (flags & F_SLOT1) ? 1 : 0), w,
+                       static_cast<__nv_bfloat16*>(p.out), p.lse, p.part_o, p.part_lse, lane);
+    }
+    __syncwarp();  // every lane is done with this stage before it is refilled
+  }
+  cp_async_wait<0>();
+}
+
+template <int NG, int D>
+static cudaError_t launch_lsu(const DecodeParams& p, int num_ctas, cudaStream_t stream) {
+  using C = LsuCfg<NG, D>;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gqa_decode_lsu_kernel<NG, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  gqa_decode_lsu_kernel<NG, D><<<num_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+#define GQA_LSU_VARIANTS(X) X(4, 3) X(4, 4) X(4, 2) X(2, 3) X(2, 5) X(1, 3) X(1, 6)
+
+int lsu_smem_bytes(int ng, int stages) {
+#define X(NG, D) \
+  if (ng == NG && stages == D) return LsuCfg<NG, D>::kSmemBytes;
+  GQA_LSU_VARIANTS(X)
+#undef X
+  return -1;
+}
+
+cudaError_t launch_decode_lsu(int ng, int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream) {
+#define X(NG, D) \
+  if (ng == NG && stages == D) return launch_lsu<NG, D>(p, num_ctas, stream);
+  GQA_LSU_VARIANTS(X)
+#undef X
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gqa

@@ -25,11 +25,15 @@ struct DecodeParams {
   float* part_o;    // [2 * num_ctas][NG][128 dims][8 heads] fp32
   float* part_lse;  // [2 * num_ctas][NG][8 heads] fp32
   const int* skip_if_set;  // optional: return without work if *skip_if_set != 0
+  int* err;                // device error word (bit flags below)
   int batch;
   int min_units;
   float scale_log2;        // sm_scale * log2(e)
   int num_pages_check;     // > 0: page ids are range-checked against it
 };
+
+// Merge CTAs per boundary between consecutive decode CTAs.
+constexpr int kMergeCtasPerBoundary = 4;
 
 struct MergeParams {
   const int* kv_indptr;
@@ -41,22 +45,47 @@ struct MergeParams {
   int batch;
   int num_decode_ctas;
   int min_units;
-  int merge_ctas_per_boundary;
   int use_pdl;
 };
 
 // Compile-time variant of the decode kernel.
+enum : int { kGatherLsu = 0, kGatherTma = 1 };
+
 struct KernelChoice {
+  int gather;         // kGatherLsu: self-loading warps with cp.async; kGatherTma: producer warp + bulk copies
   int heads_per_cta;  // NG: KV heads per CTA (4, 2 or 1)
-  int tile;           // tokens per pipeline stage (16 or 32)
+  int tile;           // tokens per pipeline stage (16; 32 for the TMA variant)
   int stages;         // pipeline depth
 };
 
-int decode_smem_bytes(const KernelChoice& k);
-cudaError_t launch_decode(const KernelChoice& k, const DecodeParams& p, int num_ctas, cudaStream_t stream);
+int lsu_smem_bytes(int ng, int stages);
+cudaError_t launch_decode_lsu(int ng, int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream);
+int tma_smem_bytes(int ng, int tile, int stages);
+cudaError_t launch_decode_tma(int ng, int tile, int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream);
+
+// Shared memory of a variant, or -1 if it is not compiled in.
+inline int decode_smem_bytes(const KernelChoice& k) {
+  if (k.gather == kGatherLsu) return k.tile == 16 ? lsu_smem_bytes(k.heads_per_cta, k.stages) : -1;
+  if (k.gather == kGatherTma) return tma_smem_bytes(k.heads_per_cta, k.tile, k.stages);
+  return -1;
+}
+
+// Warps a variant runs per CTA and the most CTAs per SM worth launching.
+inline int decode_max_ctas_per_sm(const KernelChoice& k) {
+  // LSU: up to 16 gathering warps per SM; TMA: up to 4 consumer warps per SM.
+  return k.gather == kGatherLsu ? 16 / k.heads_per_cta : 4 / k.heads_per_cta;
+}
+
+inline cudaError_t launch_decode(const KernelChoice& k, const DecodeParams& p, int num_ctas, cudaStream_t stream) {
+  if (k.gather == kGatherLsu) return launch_decode_lsu(k.heads_per_cta, k.stages, p, num_ctas, stream);
+  if (k.gather == kGatherTma) return launch_decode_tma(k.heads_per_cta, k.tile, k.stages, p, num_ctas, stream);
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_merge(int heads_per_cta, const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_validate(const int* indptr, const int* indices, int batch, int num_pages, int* err,
                             cudaStream_t stream);
 cudaError_t read_and_clear_device_error(int* out);
+cudaError_t device_error_word(int** ptr);  // device address of the error word (current device)
 
 }  // namespace gqa

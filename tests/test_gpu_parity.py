@@ -26,7 +26,7 @@ def _library(cuda_device):
     build()
     _lib.load()
     yield
-    _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0)
+    _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0)
 
 
 @pytest.fixture
@@ -35,7 +35,7 @@ def tuning():
     def apply(*args):
         assert _lib.gqa_paged_decode_set_tuning(*args) == 0
     yield apply
-    assert _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0) == 0
+    assert _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0) == 0
 
 
 def gpu_run(w, dev="cuda"):
@@ -103,16 +103,23 @@ def test_edge_cases_default(name):
     check(w, out, lse)
 
 
+# (num_ctas, min_units_per_cta, heads_per_cta, tile, stages, gather): gather 0 = cp.async, 1 = TMA bulk
 VARIANTS = {
-    "ng4_tile16_s4": (0, 0, 4, 16, 4),
-    "ng4_tile32_s3": (0, 0, 4, 32, 3),
-    "ng2_tile16_s4": (0, 0, 2, 16, 4),
-    "ng1_tile16_s4": (0, 0, 1, 16, 4),
-    "ng4_few_ctas": (7, 0, 4, 16, 5),
-    "ng4_small_units": (0, 16, 4, 16, 5),
-    "ng1_small_units": (0, 16, 1, 16, 4),
-    "ng4_tile32_small_units": (0, 16, 4, 32, 3),
-    "one_cta": (1, 0, 4, 16, 5),
+    "lsu_ng4_s3": (0, 0, 4, 16, 3, 0),
+    "lsu_ng4_s4": (0, 0, 4, 16, 4, 0),
+    "lsu_ng4_s2": (0, 0, 4, 16, 2, 0),
+    "lsu_ng2_s3": (0, 0, 2, 16, 3, 0),
+    "lsu_ng2_s5": (0, 0, 2, 16, 5, 0),
+    "lsu_ng1_s3": (0, 0, 1, 16, 3, 0),
+    "lsu_ng1_s6": (0, 0, 1, 16, 6, 0),
+    "lsu_few_ctas": (7, 0, 4, 16, 3, 0),
+    "lsu_small_units": (0, 16, 4, 16, 3, 0),
+    "lsu_ng1_small_units": (0, 16, 1, 16, 3, 0),
+    "lsu_one_cta": (1, 0, 4, 16, 3, 0),
+    "tma_ng4_t16": (0, 0, 4, 16, 5, 1),
+    "tma_ng4_t32": (0, 0, 4, 32, 3, 1),
+    "tma_ng1_t16": (0, 0, 1, 16, 4, 1),
+    "tma_small_units": (0, 16, 4, 32, 3, 1),
 }
 
 
@@ -129,13 +136,14 @@ def test_kernel_variants(tuning, variant, case):
 def test_split_and_merge_paths(tuning, num_ctas, min_units):
     """One long and several short sequences cut into up to ~300 pieces: both merge paths
     (<= 16 and > 16 partials per sequence) and many sequences per CTA."""
-    tuning(num_ctas, min_units, 4, 16, 5)
+    tuning(num_ctas, min_units, 4, 16, 3, 0)
     w = wl.make_workload([5000, 3, 17, 0, 900, 1, 64], seed=21, pool_factor=1.1)
     out, lse = gpu_run(w)
     check(w, out, lse)
 
 
-@pytest.mark.parametrize("variant", [(200, 8, 4, 16, 5), (600, 8, 1, 16, 4), (120, 8, 2, 16, 4), (90, 8, 4, 32, 3)])
+@pytest.mark.parametrize("variant", [(200, 8, 4, 16, 3, 0), (600, 8, 1, 16, 3, 0), (120, 8, 2, 16, 5, 0),
+                                     (90, 8, 4, 32, 3, 1), (300, 8, 4, 16, 5, 1)])
 def test_token_count_exact_with_uniform_scores(tuning, variant):
     """q = 0 makes every score 0: lse must be log2(n) to fp32 precision, which a
     dropped or doubled token would break (1.44/n >> 2e-5 for n <= 9000), and O
