@@ -8,7 +8,8 @@ kernel) over one batch of the workload, inputs resident in HBM. Counted bytes
 per call: 2048 B per cached token (K and V rows of all 4 KV heads) plus, per
 sequence, 8192 B of q, 8192 B of out and 128 B of lse. ``value`` is those bytes
 over the device time of the K timed steps (CUDA events on the launching
-stream, L2 flushed by a 256 MB write between steps, outside the events).
+stream; between steps, outside the events, a 256 MB write and a 256 MB read
+flush the L2).
 
 ``--impl reference`` times the float64 CPU oracle instead (bounded samples of
 the same workload on the host cores); only rank 0 runs it.
@@ -175,12 +176,26 @@ def ncu_traffic(workload: str, total_tokens: int):
 HOST_LEAD_CYCLES = 300_000
 
 
-def time_steps(call, steps: int, stream, flush_buf, before=None):
+class L2Flush:
+    """Evicts the L2 between timed steps: a 256 MB write (more than the 126-129 MB
+    L2), then a 256 MB read of a second buffer, so that the dirty lines of the
+    write are written back before the timed region and do not compete with it."""
+
+    def __init__(self, device):
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
+def time_steps(call, steps: int, stream, flush, before=None):
     """Per-step device time (ms) of `call` with CUDA events on `stream`; L2 is flushed
     between steps outside the events."""
     times = []
     for i in range(steps):
-        flush_buf.zero_()
+        flush()
         torch.cuda._sleep(HOST_LEAD_CYCLES)
         if before is not None:
             before(i)
@@ -199,7 +214,7 @@ def bench_workload_gpu(w, device, steps, warmup, world, with_hooks=True):
     out = torch.empty_like(g.q)
     lse = torch.empty((w.batch, 32), dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
 
     def call():
         _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, w.sm_scale, out=out, lse=lse, stream=stream)
@@ -243,7 +258,7 @@ def bench_e2e(w, device, steps, warmup):
     out_d = torch.empty_like(dev[0])
     lse_d = torch.empty((w.batch, 32), dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
 
@@ -396,7 +411,7 @@ def main():
         "data": "synthetic (seeded torch.Generator, CPU-drawn, copied to HBM before timing)",
         "config": {"workload": WORKLOAD_TEXT[args.workload], "batch": w.batch, "total_tokens": w.total_tokens,
                    "num_pages": w.num_pages, "counted_bytes_per_step": cb,
-                   "l2": "flushed between steps by a 256 MB device write (outside the timed events)",
+                   "l2": "flushed between steps (256 MB device write, then 256 MB read; outside the timed events)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
