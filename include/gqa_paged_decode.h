@@ -130,6 +130,20 @@ int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_p
 int gqa_paged_decode_set_profile_events(void* decode_start, void* decode_stop);
 
 /*
+ * Host-side view of the split plan (no GPU needed): for a host copy of
+ * kv_indptr, the pieces that num_ctas decode CTAs cut the batch into, with the
+ * same arithmetic the decode and merge kernels use. Writes up to `capacity`
+ * rows of 9 int64 to `pieces`: decode CTA, sequence, head group, first and
+ * one-past-last token (sequence-relative to kv_indices), partial slot (-1 for
+ * a whole sequence written directly, else 0 / 1), and the merge kernel's view
+ * of that sequence: first CTA, last CTA, slot of the first CTA's piece.
+ * min_units_per_cta = 0 means the default (128). Returns the number of pieces
+ * (which may exceed capacity) or GQA_ERR_INVALID_ARGUMENT.
+ */
+int64_t gqa_paged_decode_plan(const int32_t* kv_indptr, int batch, int num_ctas, int min_units_per_cta,
+                              int heads_per_cta, int64_t* pieces, int64_t capacity);
+
+/*
  * Synchronise the current device, then read and clear the sticky device error
  * word: bit 1 / 2 = a pipeline wait gave up after ~2 s (the kernel returned
  * early), bit 4 = bad page id, bit 8 = bad kv_indptr. 0 means no error.

@@ -41,6 +41,8 @@ _SIGNATURES = {
     "gqa_paged_decode_set_tuning": (ctypes.c_int, [ctypes.c_int] * 6),
     "gqa_paged_decode_set_profile_events": (ctypes.c_int, [_vp, _vp]),
     "gqa_paged_decode_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
+    "gqa_paged_decode_plan": (ctypes.c_int64, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp,
+                                               ctypes.c_int64]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -109,6 +111,24 @@ def gqa_paged_decode_set_tuning(num_ctas=0, min_units_per_cta=0, heads_per_cta=0
 
 def gqa_paged_decode_set_profile_events(decode_start, decode_stop) -> int:
     return load().gqa_paged_decode_set_profile_events(decode_start, decode_stop)
+
+
+def gqa_paged_decode_plan(kv_indptr, num_ctas: int, min_units_per_cta: int = 0, heads_per_cta: int = 4):
+    """Host-side split plan for a CPU int32 kv_indptr: a list of 9-tuples (decode CTA,
+    sequence, head group, token lo, token hi, slot or -1, merge first CTA, merge last
+    CTA, merge first slot)."""
+    import numpy as np
+    ip = np.ascontiguousarray(np.asarray(kv_indptr, dtype=np.int32))
+    batch = ip.shape[0] - 1
+    ptr = ip.ctypes.data_as(ctypes.c_void_p)
+    n = load().gqa_paged_decode_plan(ptr, batch, num_ctas, min_units_per_cta, heads_per_cta, None, 0)
+    if n < 0:
+        raise GqaError(int(n), "gqa_paged_decode_plan")
+    out = np.zeros((max(n, 1), 9), dtype=np.int64)
+    n2 = load().gqa_paged_decode_plan(ptr, batch, num_ctas, min_units_per_cta, heads_per_cta,
+                                      out.ctypes.data_as(ctypes.c_void_p), n)
+    assert n2 == n
+    return [tuple(int(x) for x in row) for row in out[:n]]
 
 
 def gqa_paged_decode_device_error() -> int:

@@ -301,6 +301,60 @@ int gqa_paged_decode_set_profile_events(void* decode_start, void* decode_stop) {
   return GQA_OK;
 }
 
+int64_t gqa_paged_decode_plan(const int32_t* kv_indptr, int batch, int num_ctas, int min_units_per_cta,
+                              int heads_per_cta, int64_t* pieces, int64_t capacity) {
+  if (kv_indptr == nullptr || batch < 0 || num_ctas <= 0 || min_units_per_cta < 0) return GQA_ERR_INVALID_ARGUMENT;
+  if (heads_per_cta != 1 && heads_per_cta != 2 && heads_per_cta != 4) return GQA_ERR_INVALID_ARGUMENT;
+  if (batch == 0) return 0;
+  if (kv_indptr[0] != 0) return GQA_ERR_INVALID_ARGUMENT;
+  for (int b = 0; b < batch; ++b) {
+    if (kv_indptr[b + 1] < kv_indptr[b]) return GQA_ERR_INVALID_ARGUMENT;
+  }
+  const int64_t T = kv_indptr[batch];
+  const int hg_count = gqa::kKvHeads / heads_per_cta;
+  const int64_t W = T * hg_count;
+  const int64_t q = gqa::units_per_cta(W, num_ctas, min_units_per_cta > 0 ? min_units_per_cta : kDefaultMinUnits);
+  int64_t n = 0;
+  for (int64_t cta = 0; cta < num_ctas; ++cta) {
+    const int64_t u0 = cta * q;
+    const int64_t u1 = u0 + q < W ? u0 + q : W;
+    int64_t u = u0;
+    while (u < u1) {
+      const int64_t hg = u / T;
+      const int64_t t = u - hg * T;
+      const int64_t t_stop = (u1 - hg * T) < T ? (u1 - hg * T) : T;
+      // largest b with kv_indptr[b] <= t (binary search; the table is non-decreasing)
+      int lo = 0, hi = batch - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (kv_indptr[mid] <= t) lo = mid; else hi = mid - 1;
+      }
+      const int b = lo;
+      const int64_t seq_lo = kv_indptr[b], seq_hi = kv_indptr[b + 1];
+      const int64_t t_hi = seq_hi < t_stop ? seq_hi : t_stop;
+      if (t_hi <= t) return GQA_ERR_INVALID_ARGUMENT;  // malformed table
+      const bool whole = (t == seq_lo && t_hi == seq_hi);
+      const int slot = whole ? -1 : (hg * T + t == u0 ? 0 : 1);
+      const gqa::SeqSplit sp = gqa::seq_split(hg * T + seq_lo, hg * T + seq_hi, q);
+      if (n < capacity && pieces != nullptr) {
+        int64_t* row = pieces + 9 * n;
+        row[0] = cta;
+        row[1] = b;
+        row[2] = hg;
+        row[3] = t;
+        row[4] = t_hi;
+        row[5] = slot;
+        row[6] = sp.first_cta;
+        row[7] = sp.last_cta;
+        row[8] = sp.first_slot;
+      }
+      ++n;
+      u = hg * T + t_hi;
+    }
+  }
+  return n;
+}
+
 int gqa_paged_decode_device_error(int* flags) {
   if (flags == nullptr) return GQA_ERR_INVALID_ARGUMENT;
   if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_LAUNCH;
