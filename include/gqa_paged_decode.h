@@ -150,6 +150,33 @@ int64_t gqa_paged_decode_plan(const int32_t* kv_indptr, int batch, int num_ctas,
  */
 int gqa_paged_decode_device_error(int* flags);
 
+/*
+ * The pages this library follows have no counterpart to this entry point: it
+ * is an addition for callers that must not allocate device memory, such as a
+ * serving runtime that reserves all free HBM for its KV-cache pool up front, a
+ * caller inside CUDA stream capture (cudaMalloc cannot be captured), or a
+ * latency-critical loop that cannot take cudaMalloc's device-wide
+ * synchronisation. Same arguments and results as gqa_paged_decode, but the
+ * split partials live in a fixed device array of GQA_NOALLOC_SCRATCH_BYTES
+ * that every GPU loading the library holds until the process exits; the call
+ * allocates nothing (no cudaMalloc / cudaFree, directly or through a library).
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. Returns GQA_ERR_WORKSPACE, without launching, when the current
+ * device and tuning need more scratch than GQA_NOALLOC_SCRATCH_BYTES
+ * (gqa_paged_decode_ws_size() tells how much they need). All calls on a device
+ * share the one array and it keeps the last call's contents (nothing in it
+ * needs to start at zero: every partial a call reads, that call wrote first),
+ * so calls whose kernels overlap on the GPU - different streams, or several
+ * host threads - race on it and give wrong results: order them on one stream.
+ */
+#define GQA_NOALLOC_SCRATCH_BYTES (12u * 1024u * 1024u)
+
+int gqa_paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_indptr,
+                             const int32_t* kv_indices, float sm_scale, void* out, float* lse, int batch,
+                             struct CUstream_st* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -43,6 +43,7 @@ _SIGNATURES = {
     "gqa_paged_decode_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
     "gqa_paged_decode_plan": (ctypes.c_int64, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp,
                                                ctypes.c_int64]),
+    "gqa_paged_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_int, _vp]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -137,6 +138,13 @@ def gqa_paged_decode_device_error() -> int:
     if rc != GQA_OK:
         raise GqaError(rc, "gqa_paged_decode_device_error")
     return flags.value
+
+
+def gqa_paged_decode_noalloc(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream) -> int:
+    """As gqa_paged_decode, with the split partials in the library's fixed device
+    array instead of an allocated workspace (for callers that cannot allocate)."""
+    return load().gqa_paged_decode_noalloc(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch,
+                                           stream)
 
 
 # ------------------------------------------------------------- tensor level
