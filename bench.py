@@ -146,7 +146,7 @@ class ClockSampler:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("gqa_decode.cu", "gqa_ptx.cuh", "gqa_plan.h"):
+    for name in ("gqa_decode_lsu.cu", "gqa_common.cuh", "gqa_ptx.cuh", "gqa_plan.h"):
         with open(os.path.join(ROOT, "paged_kv_gqa_split_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -312,6 +312,44 @@ def cpu_baseline(w, budget_s: float = 10.0):
             "host_cores_available": len(os.sched_getaffinity(0))}
 
 
+# ------------------------------------------------------------- variant sweep
+SWEEP_VARIANTS = [
+    # (num_ctas, min_units_per_cta, heads_per_cta, tile, stages, gather): gather 0 = cp.async, 1 = TMA bulk
+    (0, 0, 4, 16, 3, 0), (0, 0, 4, 16, 2, 0), (0, 0, 4, 16, 4, 0), (0, 0, 2, 16, 3, 0), (0, 0, 2, 16, 2, 0),
+    (0, 0, 1, 16, 3, 0), (0, 0, 1, 16, 2, 0), (0, 0, 1, 16, 4, 0), (0, 32, 4, 16, 3, 0), (0, 0, 4, 16, 5, 1),
+    (0, 0, 4, 32, 3, 1),
+]
+
+
+def sweep(device, steps, warmup, names):
+    """Median µs per call of every decode variant on the named workloads (same timing
+    method as the main line); prints one JSON line per (workload, variant)."""
+    flush = L2Flush(device)
+    stream = torch.cuda.current_stream(device)
+    for name in names:
+        w = wl.make_config(name)
+        g = w.to(device)
+        out = torch.empty_like(g.q)
+        lse = torch.empty((w.batch, 32), dtype=torch.float32, device=device)
+        cb = counted_bytes(w.lens)
+        for v in SWEEP_VARIANTS:
+            if _lib.gqa_paged_decode_set_tuning(*v) != 0:
+                continue
+
+            def call():
+                _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, w.sm_scale, out=out, lse=lse,
+                         stream=stream)
+
+            for _ in range(warmup):
+                call()
+            ms = statistics.median(time_steps(call, steps, stream, flush))
+            print(json.dumps({"sweep": name, "variant": dict(zip(
+                ["num_ctas", "min_units_per_cta", "heads_per_cta", "tile", "stages", "gather"], v)),
+                "us_per_batch": ms * 1e3, "gbs": cb / (ms * 1e-3) / 1e9}), flush=True)
+        _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0)
+        del g, out, lse
+
+
 # ---------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -323,6 +361,7 @@ def main():
     ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="time every decode variant instead of the contract line")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
 
@@ -342,6 +381,10 @@ def main():
         build()
     barrier(world, device)
     _lib.load()
+
+    if args.sweep:
+        sweep(device, args.steps, warmup, ["tiny", "mid", "long", "large", "skewed"])
+        return
 
     peak, peak_kind = hbm_peak()
     w = wl.make_config(args.workload)

@@ -259,7 +259,7 @@ static cudaError_t launch_lsu(const DecodeParams& p, int num_ctas, cudaStream_t 
   return cudaGetLastError();
 }
 
-#define GQA_LSU_VARIANTS(X) X(4, 3) X(4, 4) X(4, 2) X(2, 3) X(2, 5) X(1, 3) X(1, 6)
+#define GQA_LSU_VARIANTS(X) X(4, 3) X(4, 4) X(4, 2) X(2, 3) X(2, 2) X(2, 5) X(1, 3) X(1, 2) X(1, 4) X(1, 6)
 
 int lsu_smem_bytes(int ng, int stages) {
 #define X(NG, D) \

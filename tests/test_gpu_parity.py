@@ -110,6 +110,9 @@ VARIANTS = {
     "lsu_ng4_s2": (0, 0, 4, 16, 2, 0),
     "lsu_ng2_s3": (0, 0, 2, 16, 3, 0),
     "lsu_ng2_s5": (0, 0, 2, 16, 5, 0),
+    "lsu_ng2_s2": (0, 0, 2, 16, 2, 0),
+    "lsu_ng1_s2": (0, 0, 1, 16, 2, 0),
+    "lsu_ng1_s4": (0, 0, 1, 16, 4, 0),
     "lsu_ng1_s3": (0, 0, 1, 16, 3, 0),
     "lsu_ng1_s6": (0, 0, 1, 16, 6, 0),
     "lsu_few_ctas": (7, 0, 4, 16, 3, 0),
