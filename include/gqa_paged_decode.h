@@ -109,7 +109,7 @@ const char* gqa_paged_decode_strerror(int code);
  * Tuning for tests and benchmarks (process-wide; 0 keeps the default):
  * num_ctas - decode CTAs per call, at most 1536 (default: SMs x CTAs per SM);
  * min_units_per_cta - smallest share of (token, head group) units a CTA takes
- *   (default 128); smaller values cut sequences into more pieces;
+ *   (default 32); smaller values cut sequences into more pieces;
  * heads_per_cta - KV heads per CTA: 4, 2 or 1 (one warp per KV head);
  * tile, stages - tokens per pipeline stage and ring depth;
  * gather - 0: every warp gathers its own 256-byte K/V head rows with 16-byte
@@ -137,7 +137,7 @@ int gqa_paged_decode_set_profile_events(void* decode_start, void* decode_stop);
  * one-past-last token (sequence-relative to kv_indices), partial slot (-1 for
  * a whole sequence written directly, else 0 / 1), and the merge kernel's view
  * of that sequence: first CTA, last CTA, slot of the first CTA's piece.
- * min_units_per_cta = 0 means the default (128). Returns the number of pieces
+ * min_units_per_cta = 0 means the default (32). Returns the number of pieces
  * (which may exceed capacity) or GQA_ERR_INVALID_ARGUMENT.
  */
 int64_t gqa_paged_decode_plan(const int32_t* kv_indptr, int batch, int num_ctas, int min_units_per_cta,

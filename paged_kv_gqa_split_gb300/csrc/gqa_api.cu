@@ -20,7 +20,7 @@ namespace {
 using gqa::KernelChoice;
 
 constexpr int kMaxDevices = 64;
-constexpr int kDefaultMinUnits = 128;
+constexpr int kDefaultMinUnits = 32;
 // Upper bound on decode CTAs a tuning may ask for.
 constexpr int kMaxDecodeCtas = 1536;
 constexpr int kSmemPerSm = 228 * 1024;

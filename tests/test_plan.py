@@ -28,7 +28,7 @@ def check_plan(lens, num_ctas, min_units, ng):
     hg_count = 4 // ng
     pieces = _lib.gqa_paged_decode_plan(ip, num_ctas, min_units, ng)
     W = T * hg_count
-    mu = min_units if min_units > 0 else 128
+    mu = min_units if min_units > 0 else 32
     q = max(mu, -(-W // num_ctas), 1)
     # 1) every (head group, sequence) is covered exactly once by contiguous pieces
     cover = {}
@@ -98,7 +98,7 @@ def test_workload_plans(name):
         splits[p[1]] = splits.get(p[1], 0) + 1
     # a long sequence is cut once per CTA boundary it spans
     longest = int(np.argmax(lens))
-    q = max(128, -(-sum(lens) // 304))
+    q = max(32, -(-sum(lens) // 304))
     assert splits[longest] >= lens[longest] // q
 
 
