@@ -130,6 +130,22 @@ int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_p
 int gqa_paged_decode_set_profile_events(void* decode_start, void* decode_stop);
 
 /*
+ * KV-cache append: the step that runs before each decode to store the new
+ * tokens' K and V. The row store of the split-K GQA path on the sigit.si vLLM
+ * "qsa.py" page (_store_qsa_rows_kernel / qsa_store_cache_rows) with page size
+ * 1: for r < num_tokens, if 0 <= slots[r] < num_pages then
+ *   k_cache[slots[r], 0, :, :] = k_new[r, :, :] and v_cache[slots[r], 0, :, :] = v_new[r, :, :];
+ * other slots (for example -1 for padding tokens) store nothing.
+ * k_new, v_new: [num_tokens][4][128] bf16, 16-byte aligned; slots: [num_tokens]
+ * int32; k_cache, v_cache: [num_pages][1][4][128] bf16, 16-byte aligned, updated
+ * in place. Valid slots should be distinct: when two rows name the same page,
+ * which one it keeps is unspecified. Asynchronous on `stream`; num_tokens == 0
+ * returns 0 without launching.
+ */
+int gqa_paged_kv_append(const void* k_new, const void* v_new, const int32_t* slots, void* k_cache, void* v_cache,
+                        int num_tokens, int num_pages, struct CUstream_st* stream);
+
+/*
  * Host-side view of the split plan (no GPU needed): for a host copy of
  * kv_indptr, the pieces that num_ctas decode CTAs cut the batch into, with the
  * same arithmetic the decode and merge kernels use. Writes up to `capacity`

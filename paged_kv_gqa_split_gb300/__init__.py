@@ -5,6 +5,6 @@ calls the CUDA library through its C ABI (include/gqa_paged_decode.h). The
 library is built in-tree by ``paged_kv_gqa_split_gb300.build.build()``; it is
 loaded on first use, and every call fails loudly if it is missing.
 """
-from ._lib import GqaError, run, run_checked  # noqa: F401
+from ._lib import GqaError, kv_append, run, run_checked  # noqa: F401
 
-__all__ = ["GqaError", "run", "run_checked"]
+__all__ = ["GqaError", "kv_append", "run", "run_checked"]

@@ -43,6 +43,7 @@ _SIGNATURES = {
     "gqa_paged_decode_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
     "gqa_paged_decode_plan": (ctypes.c_int64, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp,
                                                ctypes.c_int64]),
+    "gqa_paged_kv_append": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int, _vp]),
     "gqa_paged_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_int, _vp]),
 }
 
@@ -138,6 +139,38 @@ def gqa_paged_decode_device_error() -> int:
     if rc != GQA_OK:
         raise GqaError(rc, "gqa_paged_decode_device_error")
     return flags.value
+
+
+def gqa_paged_kv_append(k_new, v_new, slots, k_cache, v_cache, num_tokens, num_pages, stream) -> int:
+    return load().gqa_paged_kv_append(k_new, v_new, slots, k_cache, v_cache, num_tokens, num_pages, stream)
+
+
+def kv_append(k_new: torch.Tensor, v_new: torch.Tensor, slots: torch.Tensor, k_cache: torch.Tensor,
+              v_cache: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Store each new token's K/V rows into page slots[r] of the caches (in place);
+    slots outside [0, num_pages) are skipped."""
+    for name, t in (("k_new", k_new), ("v_new", v_new), ("slots", slots), ("k_cache", k_cache), ("v_cache", v_cache)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor: the library has no CPU path")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device != k_cache.device:
+            raise ValueError(f"all tensors must be on {k_cache.device}")
+    n = int(slots.shape[0]) if slots.dim() == 1 else -1
+    if n < 0 or tuple(k_new.shape) != (n, NUM_KV_HEADS, HEAD_DIM) or k_new.shape != v_new.shape:
+        raise ValueError("expected k_new / v_new [N, 4, 128] and slots [N]")
+    if k_cache.dim() != 4 or tuple(k_cache.shape[1:]) != (PAGE_SIZE, NUM_KV_HEADS, HEAD_DIM) or \
+            v_cache.shape != k_cache.shape:
+        raise ValueError("expected k_cache / v_cache [P, 1, 4, 128]")
+    if any(t.dtype != torch.bfloat16 for t in (k_new, v_new, k_cache, v_cache)) or slots.dtype != torch.int32:
+        raise ValueError("K/V tensors must be bfloat16 and slots int32")
+    if stream is None:
+        stream = torch.cuda.current_stream(k_cache.device)
+    with torch.cuda.device(k_cache.device):
+        rc = gqa_paged_kv_append(k_new.data_ptr(), v_new.data_ptr(), slots.data_ptr(), k_cache.data_ptr(),
+                                 v_cache.data_ptr(), n, int(k_cache.shape[0]), stream.cuda_stream)
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_paged_kv_append")
 
 
 def gqa_paged_decode_noalloc(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream) -> int:

@@ -301,6 +301,29 @@ int gqa_paged_decode_set_profile_events(void* decode_start, void* decode_stop) {
   return GQA_OK;
 }
 
+int gqa_paged_kv_append(const void* k_new, const void* v_new, const int32_t* slots, void* k_cache, void* v_cache,
+                        int num_tokens, int num_pages, struct CUstream_st* stream) {
+  if (num_tokens < 0) return GQA_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return GQA_OK;
+  if (k_new == nullptr || v_new == nullptr || slots == nullptr || k_cache == nullptr || v_cache == nullptr)
+    return GQA_ERR_INVALID_ARGUMENT;
+  if (num_pages <= 0) return GQA_ERR_INVALID_ARGUMENT;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slots, 4))
+    return GQA_ERR_INVALID_ARGUMENT;
+  int dev = 0;
+  DeviceState* st = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    const int rc = current_device(&dev, &st);
+    if (rc != GQA_OK) return rc;
+  }
+  return gqa::launch_kv_append(k_new, v_new, slots, k_cache, v_cache, num_tokens, num_pages, st->sm_count, stream) ==
+                 cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_LAUNCH;
+}
+
 int64_t gqa_paged_decode_plan(const int32_t* kv_indptr, int batch, int num_ctas, int min_units_per_cta,
                               int heads_per_cta, int64_t* pieces, int64_t capacity) {
   if (kv_indptr == nullptr || batch < 0 || num_ctas <= 0 || min_units_per_cta < 0) return GQA_ERR_INVALID_ARGUMENT;

@@ -85,6 +85,8 @@ inline cudaError_t launch_decode(const KernelChoice& k, const DecodeParams& p, i
 cudaError_t launch_merge(int heads_per_cta, const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_validate(const int* indptr, const int* indices, int batch, int num_pages, int* err,
                             cudaStream_t stream);
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int* slots, void* k_cache, void* v_cache,
+                             int n, int num_pages, int sm_count, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(int* out);
 cudaError_t device_error_word(int** ptr);  // device address of the error word (current device)
 

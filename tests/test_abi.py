@@ -21,7 +21,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gqa_paged_decode\w*)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(gqa_paged_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_problem_entry_point():
@@ -109,3 +109,12 @@ def test_cpu_tensors_raise():
     with pytest.raises(ValueError, match="no CPU path"):
         _lib.run(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices)
     assert torch.is_tensor(w.q)
+
+
+def test_append_argument_checks(lib):
+    a = 1 << 20
+    assert _lib.gqa_paged_kv_append(None, None, None, None, None, 0, 0, None) == 0
+    assert _lib.gqa_paged_kv_append(a, a, a, a, a, -1, 4, None) == _lib.GQA_ERR_INVALID_ARGUMENT
+    assert _lib.gqa_paged_kv_append(a, a, a, a, a, 3, 0, None) == _lib.GQA_ERR_INVALID_ARGUMENT
+    assert _lib.gqa_paged_kv_append(a, None, a, a, a, 3, 4, None) == _lib.GQA_ERR_INVALID_ARGUMENT
+    assert _lib.gqa_paged_kv_append(a + 8, a, a, a, a, 3, 4, None) == _lib.GQA_ERR_INVALID_ARGUMENT
