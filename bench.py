@@ -279,6 +279,33 @@ def bench_e2e(w, device, steps, warmup):
     return ms, h2d, d2h
 
 
+# ------------------------------------------------------------- KV append
+def bench_append(device, steps, warmup, step_tokens, peak):
+    """KV-cache append: a bulk append of 262,144 tokens into a 1 Mi-page pool
+    (2 KB read + 2 KB written per token) and one decode step's append of
+    `step_tokens` tokens. Same timing method as the decode line."""
+    g = torch.Generator(device=device).manual_seed(7)
+    num_pages, bulk = 1 << 20, 1 << 18
+    k = torch.empty(num_pages, 1, 4, 128, dtype=torch.bfloat16, device=device)
+    v = torch.empty_like(k)
+    kn = torch.randn(bulk, 4, 128, generator=g, device=device).to(torch.bfloat16)
+    vn = torch.randn(bulk, 4, 128, generator=g, device=device).to(torch.bfloat16)
+    slots = torch.randperm(num_pages, generator=g, device=device)[:bulk].to(torch.int32)
+    stream = torch.cuda.current_stream(device)
+    flush = L2Flush(device)
+    res = {}
+    for name, n in (("bulk", bulk), ("step", step_tokens)):
+        def call(n=n):
+            _lib.kv_append(kn[:n], vn[:n], slots[:n], k, v, stream=stream)
+        for _ in range(warmup):
+            call()
+        ms = statistics.median(time_steps(call, steps, stream, flush))
+        gbs = 4096 * n / (ms * 1e-3) / 1e9
+        res[name] = {"tokens": n, "us": ms * 1e3, "gbs": gbs, "frac_of_peak": gbs / peak}
+    del k, v, kn, vn, slots, flush
+    return res
+
+
 # -------------------------------------------------------------- CPU oracle
 def oracle_sample(w, budget_s: float):
     """Run the float64 oracle over the workload's sequences in order until about
@@ -428,6 +455,10 @@ def main():
             if ww is not w:
                 del ww
 
+    append = None
+    if not args.no_workloads:
+        append = bench_append(device, args.steps, warmup, w.batch, peak)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
@@ -468,6 +499,7 @@ def main():
         "clocks": clocks,
         "parity": parity,
         "workloads": table,
+        "kv_append": append,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
