@@ -115,11 +115,15 @@ const char* gqa_paged_decode_strerror(int code);
  * gather - 0: every warp gathers its own 256-byte K/V head rows with 16-byte
  *   cp.async (default: heads 4, tile 16, stages 3, 2 CTAs per SM);
  *   1: one producer warp per CTA gathers whole page rows with TMA bulk copies
- *   (tile 16 or 32).
+ *   (tile 16 or 32);
+ * fused_merge_max_splits - a sequence cut into at most this many pieces is
+ *   merged by the decode kernel itself (the warp that finishes its last piece
+ *   combines them; default 16); longer splits go to the merge kernel; -1 sends
+ *   every split sequence to the merge kernel.
  * Returns GQA_ERR_INVALID_ARGUMENT for a combination that is not compiled in.
  */
 int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_per_cta, int tile, int stages,
-                                int gather);
+                                int gather, int fused_merge_max_splits);
 
 /*
  * Profiling hook: when both are non-NULL (cudaEvent_t handles), every later
@@ -183,11 +187,14 @@ int gqa_paged_decode_device_error(int* flags);
  * device and tuning need more scratch than GQA_NOALLOC_SCRATCH_BYTES
  * (gqa_paged_decode_ws_size() tells how much they need). All calls on a device
  * share the one array and it keeps the last call's contents (nothing in it
- * needs to start at zero: every partial a call reads, that call wrote first),
- * so calls whose kernels overlap on the GPU - different streams, or several
- * host threads - race on it and give wrong results: order them on one stream.
+ * needs to start at zero: every partial a call reads, that call wrote first,
+ * and the arrival counters carry a per-call tag), so calls whose kernels
+ * overlap on the GPU - different streams, or several host threads - race on
+ * it and give wrong results: order them on one stream. 32 MiB holds the
+ * partials of every occupancy-limited launch (16 decode warps per SM, two
+ * 4 KB partials each) on a GPU of up to 240 SMs.
  */
-#define GQA_NOALLOC_SCRATCH_BYTES (12u * 1024u * 1024u)
+#define GQA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 int gqa_paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_indptr,
                              const int32_t* kv_indices, float sm_scale, void* out, float* lse, int batch,

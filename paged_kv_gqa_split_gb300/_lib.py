@@ -38,7 +38,7 @@ _SIGNATURES = {
                                                 _vp, ctypes.c_int, _vp]),
     "gqa_paged_decode_release": (None, []),
     "gqa_paged_decode_strerror": (ctypes.c_char_p, [ctypes.c_int]),
-    "gqa_paged_decode_set_tuning": (ctypes.c_int, [ctypes.c_int] * 6),
+    "gqa_paged_decode_set_tuning": (ctypes.c_int, [ctypes.c_int] * 7),
     "gqa_paged_decode_set_profile_events": (ctypes.c_int, [_vp, _vp]),
     "gqa_paged_decode_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
     "gqa_paged_decode_plan": (ctypes.c_int64, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp,
@@ -107,8 +107,9 @@ GATHER_LSU, GATHER_TMA = 0, 1
 
 
 def gqa_paged_decode_set_tuning(num_ctas=0, min_units_per_cta=0, heads_per_cta=0, tile=0, stages=0,
-                                gather=GATHER_LSU) -> int:
-    return load().gqa_paged_decode_set_tuning(num_ctas, min_units_per_cta, heads_per_cta, tile, stages, gather)
+                                gather=GATHER_LSU, fused_merge_max_splits=0) -> int:
+    return load().gqa_paged_decode_set_tuning(num_ctas, min_units_per_cta, heads_per_cta, tile, stages, gather,
+                                              fused_merge_max_splits)
 
 
 def gqa_paged_decode_set_profile_events(decode_start, decode_stop) -> int:

@@ -9,6 +9,8 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
+#include <chrono>
 #include <mutex>
 
 #include "gqa_kernels.h"
@@ -39,7 +41,8 @@ struct DeviceState {
 struct Tuning {
   int num_ctas = 0;
   int min_units = 0;
-  KernelChoice kernel = {gqa::kGatherLsu, 4, 16, 3};
+  int fuse_max_splits = gqa::kDefaultFuseMaxSplits;
+  KernelChoice kernel = {gqa::kGatherLsu, 4, 16, 2};
 };
 
 std::mutex g_mu;
@@ -47,6 +50,13 @@ DeviceState g_dev[kMaxDevices];
 Tuning g_tune;
 cudaEvent_t g_ev_start = nullptr;
 cudaEvent_t g_ev_stop = nullptr;
+// Ticket epoch of each call (never 0; 40 bits), so arrival tickets left by an
+// earlier call on the same workspace read as empty. The counter starts at a
+// value drawn from the clock, so a caller's workspace that holds small-integer
+// or zero data (or tickets of another process) does not look like a live ticket.
+std::atomic<unsigned long long> g_epoch{
+    static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count()) * 0x9E3779B97F4A7C15ull >>
+    24};
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -83,10 +93,16 @@ size_t partial_o_floats(int num_ctas, int ng) {
   return static_cast<size_t>(2) * num_ctas * ng * gqa::kGroup * gqa::kHeadDim;
 }
 
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t partial_lse_bytes(int num_ctas, int ng) {
+  return static_cast<size_t>(2) * num_ctas * ng * gqa::kGroup * sizeof(float);
+}
+
 size_t workspace_bytes(int num_ctas, int ng) {
   const size_t o = partial_o_floats(num_ctas, ng) * sizeof(float);
-  const size_t l = static_cast<size_t>(2) * num_ctas * ng * gqa::kGroup * sizeof(float);
-  return ((o + 255) & ~size_t(255)) + ((l + 255) & ~size_t(255));
+  const size_t tickets = static_cast<size_t>(num_ctas) * ng * sizeof(unsigned long long);
+  return round256(o) + round256(partial_lse_bytes(num_ctas, ng)) + round256(tickets);
 }
 
 int check_args(const void* q, const void* k, const void* v, const int32_t* indptr, const int32_t* indices,
@@ -148,8 +164,11 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   const int ng = tune.kernel.heads_per_cta;
   const int ctas = decode_ctas(*st, tune);
   float* part_o = static_cast<float*>(ws);
-  float* part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) +
-                                             ((partial_o_floats(ctas, ng) * sizeof(float) + 255) & ~size_t(255)));
+  const size_t lse_off = round256(partial_o_floats(ctas, ng) * sizeof(float));
+  float* part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + lse_off);
+  unsigned long long* tickets = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + lse_off +
+                                                                       round256(partial_lse_bytes(ctas, ng)));
+  const unsigned long long epoch = (g_epoch.fetch_add(1) % ((1ull << 40) - 1)) + 1;
   const int min_units = tune.min_units > 0 ? tune.min_units : kDefaultMinUnits;
 
   if (checked) {
@@ -172,6 +191,9 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   dp.part_lse = part_lse;
   dp.skip_if_set = checked ? dev_err : nullptr;
   dp.err = err_word;
+  dp.tickets = tickets;
+  dp.epoch = epoch;
+  dp.fuse_max_splits = tune.fuse_max_splits;
   dp.batch = batch;
   dp.min_units = min_units;
   dp.scale_log2 = sm_scale * kLog2e;
@@ -193,6 +215,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   mp.num_decode_ctas = ctas;
   mp.min_units = min_units;
   mp.use_pdl = profile ? 0 : 1;
+  mp.fuse_max_splits = tune.fuse_max_splits;
   if (gqa::launch_merge(ng, mp, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
   return GQA_OK;
 }
@@ -270,18 +293,20 @@ const char* gqa_paged_decode_strerror(int code) {
 }
 
 int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_per_cta, int tile, int stages,
-                                int gather) {
+                                int gather, int fused_merge_max_splits) {
   if (num_ctas < 0 || min_units_per_cta < 0 || heads_per_cta < 0 || tile < 0 || stages < 0 || gather < 0)
     return GQA_ERR_INVALID_ARGUMENT;
-  if (num_ctas > kMaxDecodeCtas) return GQA_ERR_INVALID_ARGUMENT;
+  if (num_ctas > kMaxDecodeCtas || fused_merge_max_splits < -1) return GQA_ERR_INVALID_ARGUMENT;
   Tuning t;
   t.num_ctas = num_ctas;
   t.min_units = min_units_per_cta;
+  t.fuse_max_splits = fused_merge_max_splits == 0 ? gqa::kDefaultFuseMaxSplits
+                                                  : (fused_merge_max_splits < 0 ? 1 : fused_merge_max_splits);
   t.kernel.gather = gather;
   t.kernel.heads_per_cta = heads_per_cta > 0 ? heads_per_cta : 4;
   if (gather == gqa::kGatherLsu) {
     t.kernel.tile = tile > 0 ? tile : 16;
-    t.kernel.stages = stages > 0 ? stages : 3;
+    t.kernel.stages = stages > 0 ? stages : 2;
   } else if (gather == gqa::kGatherTma) {
     t.kernel.tile = tile > 0 ? tile : 16;
     t.kernel.stages = stages > 0 ? stages : (t.kernel.tile == 32 ? 3 : (t.kernel.heads_per_cta == 4 ? 5 : 4));

@@ -17,6 +17,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "gqa_kernels.h"
 #include "gqa_plan.h"
 #include "gqa_ptx.cuh"
 
@@ -139,14 +140,184 @@ __device__ __forceinline__ void attend_subtile(HeadState& st, uint32_t k_addr, u
   }
 }
 
+// Where a piece's sequence was cut: S pieces held by decode CTAs first_cta ..
+// first_cta + S - 1; the first of them in slot first_slot, the others in slot 0.
+struct SplitInfo {
+  int S;
+  int first_cta;
+  int first_slot;
+};
+
+// Arrival ticket of one split sequence (one per KV head): the word holds
+// (call epoch << 24) | pieces arrived. A word from an earlier call (another
+// epoch) counts as zero, so the tickets need no clearing between calls.
+// Returns the number of pieces arrived including this one, or 0 if the CAS
+// loop did not settle (then the merge kernel is not told and an error is set).
+__device__ __forceinline__ unsigned ticket_arrive(unsigned long long* ticket, unsigned long long epoch, int* err) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ticket);
+  for (int it = 0; it < (1 << 16); ++it) {
+    const unsigned long long nv = ((cur >> 24) == epoch) ? cur + 1 : ((epoch << 24) | 1ull);
+    const unsigned long long prev = atomicCAS(ticket, cur, nv);
+    if (prev == cur) return static_cast<unsigned>(nv & 0xffffffull);
+    cur = prev;
+  }
+  atomicOr(err, kErrTicket);
+  return 0;
+}
+
+// Merge the S fp32 partials of one split sequence for one KV head (8 query
+// heads h0 .. h0+7) with one warp: w_i = 2^(LSE_i - M), O = sum w_i O_i / sum
+// w_i (bf16), LSE = M + log2 sum w_i. Lane l owns dims l, l+32, l+64, l+96.
+template <int NG>
+__device__ __forceinline__ void merge_split_warp(const float* part_o, const float* part_lse, const SplitInfo& si,
+                                                 int w, int64_t b, int h0, __nv_bfloat16* out, float* lse, int lane) {
+  float m[8], den[8], acc[4][8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    m[h] = -INFINITY;
+    den[h] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j][h] = 0.f;
+  }
+#pragma unroll 1
+  for (int s = 0; s < si.S; ++s) {
+    const int64_t sid = slot_id(si.first_cta + s, s == 0 ? si.first_slot : 0);
+    const float4* lr = reinterpret_cast<const float4*>(part_lse + (sid * NG + w) * kGroup);
+    const float4 la = __ldcg(lr), lb = __ldcg(lr + 1);
+    const float l8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+    float4 o[4][2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4* orow = reinterpret_cast<const float4*>(part_o + ((sid * NG + w) * kHeadDim + lane + 32 * j) * kGroup);
+      o[j][0] = __ldcg(orow);
+      o[j][1] = __ldcg(orow + 1);
+    }
+    float sc[8], wt[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      const float mn = fmaxf(m[h], l8[h]);
+      sc[h] = ex2(m[h] - mn);  // 0 while nothing has been added (m = -inf)
+      wt[h] = ex2(l8[h] - mn);
+      den[h] = den[h] * sc[h] + wt[h];
+      m[h] = mn;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float o8[8] = {o[j][0].x, o[j][0].y, o[j][0].z, o[j][0].w, o[j][1].x, o[j][1].y, o[j][1].z, o[j][1].w};
+#pragma unroll
+      for (int h = 0; h < 8; ++h) acc[j][h] = acc[j][h] * sc[h] + wt[h] * o8[h];
+    }
+  }
+  __nv_bfloat16* ob = out + (b * kQoHeads + h0) * kHeadDim;
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    const float inv = 1.f / den[h];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ob[h * kHeadDim + lane + 32 * j] = __float2bfloat16_rn(acc[j][h] * inv);
+  }
+  if (lane < 8) {
+    float mm = m[0], dd = den[0];
+#pragma unroll
+    for (int h = 1; h < 8; ++h) {
+      if (lane == h) {
+        mm = m[h];
+        dd = den[h];
+      }
+    }
+    lse[b * kQoHeads + h0 + lane] = mm + log2f(dd);
+  }
+}
+
+// Bytes one staged partial takes in shared memory: O [128 dims][8 heads] fp32 + 8 LSEs.
+constexpr int kStagedPartialBytes = kHeadDim * kGroup * 4 + kGroup * 4;
+
+// merge_split_warp with the partials staged through this warp's shared memory
+// (free once its pipeline has drained): up to `cap` partials are fetched with
+// cp.async in one round trip, then folded in with the same running-max update.
+template <int NG>
+__device__ __forceinline__ void merge_split_warp_staged(const float* part_o, const float* part_lse, const SplitInfo& si,
+                                                        int w, int64_t b, int h0, __nv_bfloat16* out, float* lse,
+                                                        uint32_t stage_smem, const uint8_t* stage_ptr, int cap,
+                                                        int lane) {
+  float m[8], den[8], acc[4][8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    m[h] = -INFINITY;
+    den[h] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j][h] = 0.f;
+  }
+  for (int s0 = 0; s0 < si.S; s0 += cap) {
+    const int n = min(cap, si.S - s0);
+    for (int i = 0; i < n; ++i) {
+      const int s = s0 + i;
+      const int64_t sid = slot_id(si.first_cta + s, s == 0 ? si.first_slot : 0);
+      const float* src_o = part_o + (sid * NG + w) * (kHeadDim * kGroup);
+      const uint32_t dst = stage_smem + i * kStagedPartialBytes;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) cp_async_16(dst + (c * 32 + lane) * 16, src_o + (c * 32 + lane) * 4, 16u);
+      if (lane < 2) cp_async_16(dst + kHeadDim * kGroup * 4 + lane * 16, part_lse + (sid * NG + w) * kGroup + lane * 4, 16u);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncwarp();
+    for (int i = 0; i < n; ++i) {
+      const float* sp = reinterpret_cast<const float*>(stage_ptr + i * kStagedPartialBytes);
+      const float4 la = *reinterpret_cast<const float4*>(sp + kHeadDim * kGroup);
+      const float4 lb = *reinterpret_cast<const float4*>(sp + kHeadDim * kGroup + 4);
+      const float l8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+      float sc[8], wt[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const float mn = fmaxf(m[h], l8[h]);
+        sc[h] = ex2(m[h] - mn);  // 0 while nothing has been added (m = -inf)
+        wt[h] = ex2(l8[h] - mn);
+        den[h] = den[h] * sc[h] + wt[h];
+        m[h] = mn;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 x = *reinterpret_cast<const float4*>(sp + (lane + 32 * j) * kGroup);
+        const float4 y = *reinterpret_cast<const float4*>(sp + (lane + 32 * j) * kGroup + 4);
+        const float o8[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int h = 0; h < 8; ++h) acc[j][h] = acc[j][h] * sc[h] + wt[h] * o8[h];
+      }
+    }
+    __syncwarp();  // the staging area is reused by the next batch
+  }
+  __nv_bfloat16* ob = out + (b * kQoHeads + h0) * kHeadDim;
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    const float inv = 1.f / den[h];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ob[h * kHeadDim + lane + 32 * j] = __float2bfloat16_rn(acc[j][h] * inv);
+  }
+  if (lane < 8) {
+    float mm = m[0], dd = den[0];
+#pragma unroll
+    for (int h = 1; h < 8; ++h) {
+      if (lane == h) {
+        mm = m[h];
+        dd = den[h];
+      }
+    }
+    lse[b * kQoHeads + h0 + lane] = mm + log2f(dd);
+  }
+}
+
 // Normalise and write a finished piece: bf16 O rows q-heads h0 .. h0+7 of
 // sequence b plus their LSE (final), or an fp32 partial (O_i, LSE_i) into
-// slot `sid` (layout [sid][NG][128 dims][8 heads], LSE [sid][NG][8]).
+// slot `sid` (layout [sid][NG][128 dims][8 heads], LSE [sid][NG][8]). A
+// partial of a sequence cut into at most fuse_max_splits pieces also takes
+// that sequence's ticket. Returns true when this warp brought the last piece:
+// it then owes the merge (merge_split_warp), which it runs after its main loop
+// so that the merge's registers do not compete with the pipeline's.
 template <int NG>
-__device__ __forceinline__ void finish_piece(const HeadState& st, bool final_piece, int64_t b, int h0, int64_t sid,
-                                             int w, __nv_bfloat16* out, float* lse, float* part_o, float* part_lse,
-                                             int lane) {
+__device__ __forceinline__ bool finish_piece(const HeadState& st, bool final_piece, int64_t b, int h0, int64_t sid,
+                                             int w, const SplitInfo& si, const DecodeParams& p, int lane) {
   const int r = lane >> 2, c = lane & 3;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
   float lt0 = st.l0, lt1 = st.l1;
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
@@ -167,18 +338,31 @@ __device__ __forceinline__ void finish_piece(const HeadState& st, bool final_pie
       *reinterpret_cast<uint32_t*>(ob + r * kHeadDim + mt * 16 + 2 * c) = x;
       *reinterpret_cast<uint32_t*>(ob + r * kHeadDim + mt * 16 + 8 + 2 * c) = y;
     }
-    if (r == 0) *reinterpret_cast<float2*>(lse + b * kQoHeads + h0 + 2 * c) = make_float2(lse0, lse1);
-  } else {
-    float* po = part_o + (sid * NG + w) * (kHeadDim * kGroup);
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      *reinterpret_cast<float2*>(po + (mt * 16 + r) * kGroup + 2 * c) =
-          make_float2(st.acc[mt][0] * i0, st.acc[mt][1] * i1);
-      *reinterpret_cast<float2*>(po + (mt * 16 + 8 + r) * kGroup + 2 * c) =
-          make_float2(st.acc[mt][2] * i0, st.acc[mt][3] * i1);
-    }
-    if (r == 0) *reinterpret_cast<float2*>(part_lse + (sid * NG + w) * kGroup + 2 * c) = make_float2(lse0, lse1);
+    if (r == 0) *reinterpret_cast<float2*>(p.lse + b * kQoHeads + h0 + 2 * c) = make_float2(lse0, lse1);
+    return false;
   }
+  float* po = p.part_o + (sid * NG + w) * (kHeadDim * kGroup);
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    *reinterpret_cast<float2*>(po + (mt * 16 + r) * kGroup + 2 * c) = make_float2(st.acc[mt][0] * i0, st.acc[mt][1] * i1);
+    *reinterpret_cast<float2*>(po + (mt * 16 + 8 + r) * kGroup + 2 * c) =
+        make_float2(st.acc[mt][2] * i0, st.acc[mt][3] * i1);
+  }
+  if (r == 0) *reinterpret_cast<float2*>(p.part_lse + (sid * NG + w) * kGroup + 2 * c) = make_float2(lse0, lse1);
+  if (si.S > p.fuse_max_splits) return false;  // the merge kernel combines this sequence
+  __threadfence();  // this lane's partial is visible device-wide before the ticket moves
+  __syncwarp();
+  unsigned arrived = 0;
+  if (lane == 0) arrived = ticket_arrive(p.tickets + static_cast<int64_t>(si.first_cta) * NG + w, p.epoch, p.err);
+  arrived = __shfl_sync(0xffffffffu, arrived, 0);
+  return arrived == static_cast<unsigned>(si.S);
 }
+
+// A merge a warp owes (see finish_piece): at most two per warp, since only the
+// first and the last piece of a CTA's range can be partials.
+struct OwedMerge {
+  SplitInfo si;
+  int b, h0;
+};
 
 }  // namespace gqa

@@ -41,7 +41,7 @@ struct LsuCfg {
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kTile * kRowPitch;
   static constexpr int kHdrOff = 2 * kTile * kRowPitch;
-  static constexpr int kStageBytes = kHdrOff + 16;
+  static constexpr int kStageBytes = kHdrOff + 32;    // tile header: 8 ints
   static constexpr int kIdsRing = 256;                // page ids held per warp (tokens)
   static constexpr int kIdsOff = D * kStageBytes;
   static constexpr int kWarpBytes = kIdsOff + kIdsRing * 4;
@@ -54,10 +54,11 @@ struct LsuCfg {
 
 struct Tile {
   int b, cnt, flags, hg, tt;
+  SplitInfo si;
 };
 
 template <int NG, int D>
-__global__ void __launch_bounds__(NG * 32) gqa_decode_lsu_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const DecodeParams p) {
   using C = LsuCfg<NG, D>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int w = threadIdx.x >> 5;  // KV head within the head group
@@ -86,6 +87,7 @@ __global__ void __launch_bounds__(NG * 32) gqa_decode_lsu_kernel(const DecodePar
   bool seg_open = false, walk_ok = true;
   int hg = 0, tt = 0, t_stop = 0;  // segment: tokens [tt, t_stop) of head group hg
   int p_hi = 0, p_flags = 0, pb = 0;  // current piece: sequence pb, tokens up to p_hi
+  SplitInfo p_si = {1, 0, 0};         // how the piece's sequence is cut across CTAs
   int wb = 0, win = 0;      // kv_indptr[wb + lane]
   int ib = 0;               // page-id ring holds tokens [ib, ib + 256)
 
@@ -116,12 +118,18 @@ __global__ void __launch_bounds__(NG * 32) gqa_decode_lsu_kernel(const DecodePar
           p_hi = min(seq_hi, t_stop);
           p_flags = F_QLOAD | ((tt == seq_lo && p_hi == seq_hi) ? F_FINAL : 0) |
                     ((static_cast<int64_t>(hg) * T + tt != u0) ? F_SLOT1 : 0);
+          const int64_t base_u = static_cast<int64_t>(hg) * T;
+          const SeqSplit sp = seq_split(base_u + seq_lo, base_u + seq_hi, q);
+          p_si.S = static_cast<int>(sp.last_cta - sp.first_cta + 1);
+          p_si.first_cta = static_cast<int>(sp.first_cta);
+          p_si.first_slot = sp.first_slot;
         }
         tl.cnt = min(C::kTile, p_hi - tt);
         tl.flags = p_flags | ((tt + tl.cnt == p_hi) ? F_END : 0);
         tl.b = pb;
         tl.hg = hg;
         tl.tt = tt;
+        tl.si = p_si;
         p_flags &= ~F_QLOAD;
         tt += tl.cnt;
         return true;
@@ -194,7 +202,10 @@ __global__ void __launch_bounds__(NG * 32) gqa_decode_lsu_kernel(const DecodePar
           prefetch_l2(qg + (static_cast<int64_t>(tl.b) * kQoHeads + h0) * kHeadDim + lane * 64);
         }
       }
-      if (lane == 0) st_shared_v4(sb + C::kHdrOff, tl.b, tl.cnt, flags, tl.hg);
+      if (lane == 0) {
+        st_shared_v4(sb + C::kHdrOff, tl.b, tl.cnt, flags, tl.hg);
+        st_shared_v4(sb + C::kHdrOff + 16, tl.si.S, tl.si.first_cta, tl.si.first_slot, 0);
+      }
     } else if (more) {
       more = false;
       if (lane == 0) st_shared_v4(sb + C::kHdrOff, 0, 0, F_DONE, 0);
@@ -211,6 +222,8 @@ __global__ void __launch_bounds__(NG * 32) gqa_decode_lsu_kernel(const DecodePar
   const uint32_t k_lane = C::kKOff + ((lane & 7) + ((lane >> 3) & 1) * 8) * C::kRowPitch + (lane >> 4) * 16;
   const uint32_t v_lane = C::kVOff + ((lane & 7) + (lane >> 4) * 8) * C::kRowPitch + ((lane >> 3) & 1) * 16;
 
+  OwedMerge owed[2];
+  int n_owed = 0;
 #pragma unroll 1
   for (int i = 0; i < D - 1; ++i) issue();
 #pragma unroll 1
@@ -221,6 +234,9 @@ __global__ void __launch_bounds__(NG * 32) gqa_decode_lsu_kernel(const DecodePar
     const uint32_t sb = wbase + (k % D) * C::kStageBytes;
     int hb, cnt, flags, thg;
     ld_shared_v4(sb + C::kHdrOff, hb, cnt, flags, thg);
+    SplitInfo si;
+    int unused;
+    ld_shared_v4(sb + C::kHdrOff + 16, si.S, si.first_cta, si.first_slot, unused);
     if (flags & F_DONE) break;
     const int h0 = (thg * NG + w) * kGroup;
     if (flags & F_QLOAD) {
@@ -235,12 +251,25 @@ __global__ void __launch_bounds__(NG * 32) gqa_decode_lsu_kernel(const DecodePar
     }
     attend_subtile(st, sb + k_lane, sb + v_lane, cnt, p.scale_log2, lane);
     if (flags & F_END) {
-      finish_piece<NG>(st, (flags & F_FINAL) != 0, hb, h0, slot_id(blockIdx.x, (flags & F_SLOT1) ? 1 : 0), w,
-                       static_cast<__nv_bfloat16*>(p.out), p.lse, p.part_o, p.part_lse, lane);
+      if (finish_piece<NG>(st, (flags & F_FINAL) != 0, hb, h0, slot_id(blockIdx.x, (flags & F_SLOT1) ? 1 : 0), w,
+                           si, p, lane)) {
+        owed[n_owed < 2 ? n_owed : 1] = {si, hb, h0};
+        ++n_owed;
+      }
     }
     __syncwarp();  // every lane is done with this stage before it is refilled
   }
   cp_async_wait<0>();
+  // merges this warp owes: every other piece's partial is visible by now; the
+  // warp's drained ring stages the partials
+  constexpr int kStageCap = C::kWarpBytes / kStagedPartialBytes;
+  static_assert(kStageCap >= 2, "ring too small to stage partials");
+#pragma unroll 1
+  for (int i = 0; i < n_owed && i < 2; ++i) {
+    __threadfence();
+    merge_split_warp_staged<NG>(p.part_o, p.part_lse, owed[i].si, w, owed[i].b, owed[i].h0,
+                                static_cast<__nv_bfloat16*>(p.out), p.lse, wbase, wsm, kStageCap, lane);
+  }
 }
 
 template <int NG, int D>

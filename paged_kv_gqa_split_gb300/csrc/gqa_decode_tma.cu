@@ -36,7 +36,7 @@ struct TmaCfg {
   static constexpr int kQOff = 2 * TILE * kRowPitch;
   static constexpr int kQBytes = NG * kGroup * kHeadDim * 2;
   static constexpr int kHdrOff = kQOff + kQBytes;
-  static constexpr int kStageBytes = (kHdrOff + 16 + 127) / 128 * 128;
+  static constexpr int kStageBytes = (kHdrOff + 32 + 127) / 128 * 128;  // header: 8 ints
   static constexpr int kBarOff = STAGES * kStageBytes;
   static constexpr int kSmemBytes = kBarOff + 2 * STAGES * 8 + 16;
   static constexpr int kThreads = (NG + 1) * 32;
@@ -91,7 +91,7 @@ __device__ __forceinline__ void tma_producer(const DecodeParams& p, uint32_t sba
   bool ok = true;
 
   // Issue one tile: tokens [tt, tt + cnt) of sequence b, head group hg.
-  auto emit = [&](int b, int hg, int tt, int cnt, int flags, int page) -> bool {
+  auto emit = [&](int b, int hg, int tt, int cnt, int flags, int page, const SplitInfo& si) -> bool {
     const int stage = tiles % STAGES;
     const uint32_t par = (tiles / STAGES) & 1u;
     if (!wait_bounded(empty0 + 8 * stage, par ^ 1u, abort_s, p.err, kErrTimeoutEmpty)) return false;
@@ -100,9 +100,8 @@ __device__ __forceinline__ void tma_producer(const DecodeParams& p, uint32_t sba
     const int nrows = (cnt + 15) & ~15;
     const uint32_t bytes = 2u * nrows * C::kRowBytes + ((flags & F_QLOAD) ? C::kQBytes : 0u);
     if (lane == 0) {
-      asm volatile("st.shared.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(sb + C::kHdrOff), "r"(b), "r"(cnt), "r"(flags),
-                   "r"(hg)
-                   : "memory");
+      st_shared_v4(sb + C::kHdrOff, b, cnt, flags, hg);
+      st_shared_v4(sb + C::kHdrOff + 16, si.S, si.first_cta, si.first_slot, 0);
       mbar_arrive_expect_tx(bar, bytes);
     }
     __syncwarp();
@@ -189,6 +188,9 @@ __device__ __forceinline__ void tma_producer(const DecodeParams& p, uint32_t sba
       int pflags = 0;
       if (t == seq_lo && p_hi == seq_hi) pflags |= F_FINAL;
       if (static_cast<int64_t>(hg) * T + t != u0) pflags |= F_SLOT1;
+      const SeqSplit sp = seq_split(static_cast<int64_t>(hg) * T + seq_lo, static_cast<int64_t>(hg) * T + seq_hi, q);
+      const SplitInfo si = {static_cast<int>(sp.last_cta - sp.first_cta + 1), static_cast<int>(sp.first_cta),
+                            sp.first_slot};
 
       for (int tt = t; tt < p_hi; tt += TILE) {
         const int cnt = min(TILE, p_hi - tt);
@@ -205,7 +207,7 @@ __device__ __forceinline__ void tma_producer(const DecodeParams& p, uint32_t sba
         const int pa = __shfl_sync(0xffffffffu, ix0, off & 31);
         const int pb = __shfl_sync(0xffffffffu, ix1, off & 31);
         const int page = off < 32 ? pa : pb;
-        if (!emit(b, hg, tt, cnt, flags, page)) {
+        if (!emit(b, hg, tt, cnt, flags, page, si)) {
           ok = false;
           break;
         }
@@ -270,6 +272,9 @@ __device__ __forceinline__ void tma_consumer(const DecodeParams& p, uint32_t sba
     const uint32_t sb = sbase + stage * C::kStageBytes;
     int hb, cnt, flags, hg;
     ld_shared_v4(sb + C::kHdrOff, hb, cnt, flags, hg);
+    SplitInfo si;
+    int unused;
+    ld_shared_v4(sb + C::kHdrOff + 16, si.S, si.first_cta, si.first_slot, unused);
     if (flags & F_DONE) return;
     if (flags & F_QLOAD) {
 #pragma unroll
@@ -289,8 +294,11 @@ __device__ __forceinline__ void tma_consumer(const DecodeParams& p, uint32_t sba
     if (lane == 0) mbar_arrive(empty0 + 8 * stage);
     if (flags & F_END) {
       const int h0 = (hg * NG + w) * kGroup;
-      finish_piece<NG>(st, (flags & F_FINAL) != 0, hb, h0, slot_id(blockIdx.x, (flags & F_SLOT1) ? 1 : 0), w,
-                       static_cast<__nv_bfloat16*>(p.out), p.lse, p.part_o, p.part_lse, lane);
+      if (finish_piece<NG>(st, (flags & F_FINAL) != 0, hb, h0, slot_id(blockIdx.x, (flags & F_SLOT1) ? 1 : 0), w,
+                           si, p, lane)) {
+        __threadfence();
+        merge_split_warp<NG>(p.part_o, p.part_lse, si, w, hb, h0, static_cast<__nv_bfloat16*>(p.out), p.lse, lane);
+      }
     }
   }
 }

@@ -13,6 +13,7 @@ constexpr int kErrTimeoutFull = 1;   // a consumer waited too long for a stage's
 constexpr int kErrTimeoutEmpty = 2;  // the producer waited too long for a free stage
 constexpr int kErrBadPage = 4;       // a kv_indices entry outside [0, num_pages)
 constexpr int kErrBadIndptr = 8;     // kv_indptr not starting at 0 / decreasing
+constexpr int kErrTicket = 16;       // a split sequence's arrival ticket did not settle
 
 struct DecodeParams {
   const void* q;
@@ -26,14 +27,21 @@ struct DecodeParams {
   float* part_lse;  // [2 * num_ctas][NG][8 heads] fp32
   const int* skip_if_set;  // optional: return without work if *skip_if_set != 0
   int* err;                // device error word (bit flags below)
+  unsigned long long* tickets;  // [num_ctas][NG] arrival tickets of split sequences
+  unsigned long long epoch;     // this call's ticket epoch (never 0, < 2^40)
   int batch;
   int min_units;
   float scale_log2;        // sm_scale * log2(e)
   int num_pages_check;     // > 0: page ids are range-checked against it
+  int fuse_max_splits;     // split sequences of at most this many pieces are merged by the decode kernel
 };
 
+// Default: sequences cut into at most this many pieces are merged inside the
+// decode kernel; longer splits go to the merge kernel.
+constexpr int kDefaultFuseMaxSplits = 16;
+
 // Merge CTAs per boundary between consecutive decode CTAs.
-constexpr int kMergeCtasPerBoundary = 4;
+constexpr int kMergeCtasPerBoundary = 1;
 
 struct MergeParams {
   const int* kv_indptr;
@@ -46,6 +54,7 @@ struct MergeParams {
   int num_decode_ctas;
   int min_units;
   int use_pdl;
+  int fuse_max_splits;  // sequences of at most this many pieces were merged by the decode kernel
 };
 
 // Compile-time variant of the decode kernel.

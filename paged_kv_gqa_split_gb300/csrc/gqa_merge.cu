@@ -20,7 +20,9 @@ namespace gqa {
 __device__ int g_device_error;
 
 // -------------------------------------------------------------------- merge
-// kMergeCtasPerBoundary CTAs per boundary between decode CTAs j and j + 1.
+// One CTA per boundary between decode CTAs j and j + 1; it merges the sequence
+// cut there only if that sequence has more pieces than the decode kernel
+// merges itself (fuse_max_splits).
 // They hold no shared memory and few registers, so they sit beside the decode
 // CTAs (programmatic dependent launch) and run their prologue - locating the
 // sequence cut at their boundary - while the decode grid is still running.
@@ -29,6 +31,11 @@ __device__ int g_device_error;
 // no second pass.
 constexpr int kMergeThreads = 128;
 constexpr int kMergeWarps = kMergeThreads / 32;
+// Split counts up to this use the CTA-per-item path (warps share the splits);
+// above it, lanes share the splits of one (head, dim) item.
+constexpr int kMergeMediumSplits = 64;
+// Split counts up to this: one warp per (head, 32-dim chunk) item, all splits.
+constexpr int kMergeSmallSplits = 16;
 
 template <int NG>
 __device__ __forceinline__ const float* partial_lse_row(const MergeParams& p, const SeqSplit& sp, int s, int g) {
@@ -73,6 +80,8 @@ template <int NG>
 __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const MergeParams p) {
   constexpr int kHG = kKvHeads / NG;
   constexpr int kH8 = NG * kGroup;  // query heads per head group
+  // cross-warp combine buffer of the medium-split path: one lane's state at a time
+  __shared__ float xw[32][3 * kGroup];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (p.skip_if_set != nullptr && *p.skip_if_set != 0) return;
@@ -90,8 +99,7 @@ __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const MergePar
   const int T = __ldg(p.kv_indptr + B);
   const int64_t W = static_cast<int64_t>(T) * kHG;
   const int64_t q = units_per_cta(W, p.num_decode_ctas, p.min_units);
-  const int j = blockIdx.x / kMergeCtasPerBoundary;  // boundary between decode CTAs j and j + 1
-  const int sub = blockIdx.x - j * kMergeCtasPerBoundary;
+  const int j = blockIdx.x;  // boundary between decode CTAs j and j + 1
   const int64_t u = static_cast<int64_t>(j + 1) * q;
   if (u >= W) return;
   const int hg = static_cast<int>(u / T);
@@ -104,22 +112,19 @@ __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const MergePar
   const int64_t base_u = static_cast<int64_t>(hg) * T;
   const SeqSplit sp = seq_split(base_u + seq_lo, base_u + seq_hi, q);
   const int S = static_cast<int>(sp.last_cta - sp.first_cta + 1);
+  if (S <= p.fuse_max_splits) return;  // the decode kernel merged it
   const int rank = j - static_cast<int>(sp.first_cta);  // which of this sequence's S - 1 boundaries
   const int nranks = S - 1;
-  // items are dealt boundary-fastest, so every CTA of the sequence (hence
-  // every SM holding one) gets a share rather than only the first few
-  const int nworkers = nranks * kMergeCtasPerBoundary;
-  const int first_item = warp * nworkers + sub * nranks + rank;
-  const int item_step = kMergeWarps * nworkers;
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(b) * kQoHeads + hg * kH8) * kHeadDim;
   float* lo = p.lse + static_cast<int64_t>(b) * kQoHeads + hg * kH8;
 
   // Everything below reads the decode kernel's partials.
   pdl_wait();
 
-  if (S <= 16) {
-    // item = (KV head g, 32-dim chunk): lane = one dim of all 8 heads, all splits
-    for (int it = first_item; it < NG * 4; it += item_step) {
+  if (S <= kMergeSmallSplits) {
+    // (reached when the decode kernel's own merge is turned down by tuning)
+    // warp item = (KV head g, 32-dim chunk): lane = one dim of all 8 heads, all splits
+    for (int it = warp * nranks + rank; it < NG * 4; it += kMergeWarps * nranks) {
       const int g = it >> 2;
       const int d = (it & 3) * 32 + lane;
       MergeAcc ma;
@@ -137,8 +142,57 @@ __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const MergePar
         for (int h = 0; h < 8; ++h) lo[g * kGroup + h] = ma.m[h] + log2f(ma.den[h]);
       }
     }
+  } else if (S <= kMergeMediumSplits) {
+    // CTA item = (KV head g, 32-dim chunk): lane = one dim of all 8 heads; the
+    // four warps take every fourth split, then fold their states together
+    for (int it = rank; it < NG * 4; it += nranks) {
+      const int g = it >> 2;
+      const int d = (it & 3) * 32 + lane;
+      MergeAcc ma;
+      ma.init();
+#pragma unroll 4
+      for (int s = warp; s < S; s += kMergeWarps) {
+        const float4* lr = reinterpret_cast<const float4*>(partial_lse_row<NG>(p, sp, s, g));
+        const float4* orow = reinterpret_cast<const float4*>(partial_o_row<NG>(p, sp, s, g, d));
+        ma.add(lr[0], lr[1], __ldcg(orow), __ldcg(orow + 1));
+      }
+      for (int src = 1; src < kMergeWarps; ++src) {
+        __syncthreads();
+        if (warp == src) {
+#pragma unroll
+          for (int h = 0; h < 8; ++h) {
+            xw[lane][h] = ma.m[h];
+            xw[lane][8 + h] = ma.den[h];
+            xw[lane][16 + h] = ma.acc[h];
+          }
+        }
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+          for (int h = 0; h < 8; ++h) {
+            const float m2 = xw[lane][h];
+            const float mn = fmaxf(ma.m[h], m2);
+            const float s1 = ex2(ma.m[h] - mn), s2 = ex2(m2 - mn);  // a warp that saw no split has m = -inf
+            ma.den[h] = ma.den[h] * s1 + xw[lane][8 + h] * s2;
+            ma.acc[h] = ma.acc[h] * s1 + xw[lane][16 + h] * s2;
+            ma.m[h] = mn;
+          }
+        }
+      }
+      if (warp == 0) {
+#pragma unroll
+        for (int h = 0; h < 8; ++h) ob[(g * kGroup + h) * kHeadDim + d] = __float2bfloat16_rn(ma.acc[h] / ma.den[h]);
+        if ((it & 3) == 0 && lane == 0) {
+#pragma unroll
+          for (int h = 0; h < 8; ++h) lo[g * kGroup + h] = ma.m[h] + log2f(ma.den[h]);
+        }
+      }
+    }
   } else {
-    // item = (KV head g, dim d): lanes stride over the splits, then one warp reduction
+    // warp item = (KV head g, dim d): lanes stride over the splits, then one warp
+    // reduction; items are dealt boundary-fastest over all of this sequence's CTAs
+    const int first_item = warp * nranks + rank;
+    const int item_step = kMergeWarps * nranks;
     for (int it = first_item; it < NG * kHeadDim; it += item_step) {
       const int g = it / kHeadDim;
       const int d = it - g * kHeadDim;

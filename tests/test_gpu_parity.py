@@ -135,18 +135,24 @@ def test_kernel_variants(tuning, variant, case):
     check(w, out, lse)
 
 
-@pytest.mark.parametrize("num_ctas,min_units", [(152, 16), (40, 16), (300, 1), (3, 1)])
-def test_split_and_merge_paths(tuning, num_ctas, min_units):
-    """One long and several short sequences cut into up to ~300 pieces: both merge paths
-    (<= 16 and > 16 partials per sequence) and many sequences per CTA."""
-    tuning(num_ctas, min_units, 4, 16, 3, 0)
+@pytest.mark.parametrize("ng,stages", [(4, 3), (4, 2), (1, 2)])
+@pytest.mark.parametrize("fuse", [0, -1, 64, 2, 5])
+@pytest.mark.parametrize("num_ctas,min_units", [(152, 16), (40, 16), (300, 1), (3, 1), (90, 1)])
+def test_split_and_merge_paths(tuning, num_ctas, min_units, fuse, ng, stages):
+    """One long and several short sequences cut into 2 to ~300 pieces, with the merge
+    done in the decode kernel (up to `fuse` pieces; 0 = default 16, -1 = never; the
+    warp stages 4 partials per round trip, so 5 and 16 take several batches) or by
+    the merge kernel (warp path up to 16 pieces, CTA path up to 64, lanes-over-splits
+    path above)."""
+    tuning(num_ctas, min_units, ng, 16, stages, 0, fuse)
     w = wl.make_workload([5000, 3, 17, 0, 900, 1, 64], seed=21, pool_factor=1.1)
     out, lse = gpu_run(w)
     check(w, out, lse)
 
 
 @pytest.mark.parametrize("variant", [(200, 8, 4, 16, 3, 0), (600, 8, 1, 16, 3, 0), (120, 8, 2, 16, 5, 0),
-                                     (90, 8, 4, 32, 3, 1), (300, 8, 4, 16, 5, 1)])
+                                     (90, 8, 4, 32, 3, 1), (300, 8, 4, 16, 5, 1), (200, 8, 4, 16, 3, 0, -1),
+                                     (600, 8, 1, 16, 3, 0, 64), (300, 8, 4, 16, 5, 1, -1)])
 def test_token_count_exact_with_uniform_scores(tuning, variant):
     """q = 0 makes every score 0: lse must be log2(n) to fp32 precision, which a
     dropped or doubled token would break (1.44/n >> 2e-5 for n <= 9000), and O
