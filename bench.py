@@ -343,14 +343,16 @@ def cpu_baseline(w, budget_s: float = 10.0):
 
 # ------------------------------------------------------------- variant sweep
 SWEEP_VARIANTS = [
-    # (num_ctas, min_units_per_cta, heads_per_cta, tile, stages, gather[, fused_merge_max_splits]):
-    # gather 0 = cp.async, 1 = TMA bulk; fused-merge threshold 0 = default, -1 = every split
-    # sequence to the merge kernel
-    (0, 0, 4, 16, 2, 0), (0, 0, 4, 16, 3, 0), (0, 0, 4, 16, 4, 0), (0, 0, 2, 16, 2, 0), (0, 0, 2, 16, 3, 0),
-    (0, 0, 1, 16, 2, 0), (0, 0, 1, 16, 4, 0), (0, 16, 4, 16, 2, 0), (0, 64, 4, 16, 2, 0), (0, 0, 4, 16, 5, 1),
-    (0, 0, 4, 32, 3, 1),
-    (0, 0, 4, 16, 2, 0, -1), (0, 0, 4, 16, 2, 0, 4), (0, 0, 4, 16, 2, 0, 8), (0, 0, 4, 16, 2, 0, 32),
-    (0, 0, 4, 16, 2, 0, 64), (0, 0, 4, 16, 3, 0, -1), (0, 0, 1, 16, 2, 0, -1),
+    # (num_ctas, min_units_per_cta, heads_per_cta, tile, stages, gather[, fused_merge_max_splits, tier2_ctas,
+    # tier2_permille, tier2_min_units]): gather 0 = cp.async, 1 = TMA bulk; 0 = default; fused-merge threshold
+    # -1 = every split sequence to the merge kernel; tier2_ctas -1 = one tier
+    (0, 0, 4, 16, 2, 0), (0, 0, 4, 16, 3, 0), (0, 0, 2, 16, 2, 0), (0, 0, 1, 16, 2, 0), (0, 0, 4, 16, 5, 1),
+    (0, 0, 4, 16, 2, 0, 0, -1), (0, 0, 4, 16, 3, 0, 0, -1),
+    (0, 0, 4, 16, 2, 0, 0, 912), (0, 0, 4, 16, 2, 0, 0, 3648),
+    (0, 0, 4, 16, 2, 0, 0, 0, 50), (0, 0, 4, 16, 2, 0, 0, 0, 150), (0, 0, 4, 16, 2, 0, 0, 0, 200),
+    (0, 0, 4, 16, 2, 0, 0, 0, 0, 16), (0, 0, 4, 16, 2, 0, 0, 0, 0, 32), (0, 0, 4, 16, 2, 0, 0, 0, 0, 128),
+    (0, 0, 4, 16, 2, 0, 0, 0, 150, 32), (0, 0, 4, 16, 2, 0, 0, 3648, 150, 32),
+    (0, 0, 4, 16, 2, 0, 4), (0, 0, 4, 16, 2, 0, 16),
 ]
 
 
@@ -378,7 +380,8 @@ def sweep(device, steps, warmup, names):
             ms = statistics.median(time_steps(call, steps, stream, flush))
             print(json.dumps({"sweep": name, "variant": dict(zip(
                 ["num_ctas", "min_units_per_cta", "heads_per_cta", "tile", "stages", "gather",
-                 "fused_merge_max_splits"], tuple(v) + (0,) * (7 - len(v)))),
+                 "fused_merge_max_splits", "tier2_ctas", "tier2_permille", "tier2_min_units"],
+                tuple(v) + (0,) * (10 - len(v)))),
                 "us_per_batch": ms * 1e3, "gbs": cb / (ms * 1e-3) / 1e9}), flush=True)
         _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0)
         del g, out, lse

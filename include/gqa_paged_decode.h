@@ -107,23 +107,33 @@ const char* gqa_paged_decode_strerror(int code);
 
 /*
  * Tuning for tests and benchmarks (process-wide; 0 keeps the default):
- * num_ctas - decode CTAs per call, at most 1536 (default: SMs x CTAs per SM);
- * min_units_per_cta - smallest share of (token, head group) units a CTA takes
- *   (default 32); smaller values cut sequences into more pieces;
+ * num_ctas - tier-1 decode CTAs per call, at most 1536 (default: SMs x CTAs
+ *   per SM, one resident wave);
+ * min_units_per_cta - smallest share of (token, head group) units a tier-1
+ *   CTA takes (default 32); smaller values cut sequences into more pieces;
  * heads_per_cta - KV heads per CTA: 4, 2 or 1 (one warp per KV head);
  * tile, stages - tokens per pipeline stage and ring depth;
  * gather - 0: every warp gathers its own 256-byte K/V head rows with 16-byte
- *   cp.async (default: heads 4, tile 16, stages 3, 2 CTAs per SM);
+ *   cp.async (default: heads 4, tile 16, stages 2, 3 CTAs per SM);
  *   1: one producer warp per CTA gathers whole page rows with TMA bulk copies
  *   (tile 16 or 32);
  * fused_merge_max_splits - a sequence cut into at most this many pieces is
  *   merged by the decode kernel itself (the warp that finishes its last piece
- *   combines them; default 16); longer splits go to the merge kernel; -1 sends
- *   every split sequence to the merge kernel.
- * Returns GQA_ERR_INVALID_ARGUMENT for a combination that is not compiled in.
+ *   combines them); longer splits go to the merge kernel; default and -1: every
+ *   split sequence goes to the merge kernel;
+ * tier2_ctas - CTAs of the second tier, which takes the last tier2_permille
+ *   thousandths of the units in small ranges that SMs finishing their tier-1
+ *   range early pick up (default 2 per tier-1 CTA; -1: one tier only, at most
+ *   65536);
+ * tier2_permille - share of the units set aside for tier 2 (default 100,
+ *   at most 900);
+ * tier2_min_units - smallest share a tier-2 CTA takes (default 64).
+ * Returns GQA_ERR_INVALID_ARGUMENT for a combination that is not compiled in
+ * or a value out of range.
  */
 int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_per_cta, int tile, int stages,
-                                int gather, int fused_merge_max_splits);
+                                int gather, int fused_merge_max_splits, int tier2_ctas, int tier2_permille,
+                                int tier2_min_units);
 
 /*
  * Profiling hook: when both are non-NULL (cudaEvent_t handles), every later
@@ -151,8 +161,10 @@ int gqa_paged_kv_append(const void* k_new, const void* v_new, const int32_t* slo
 
 /*
  * Host-side view of the split plan (no GPU needed): for a host copy of
- * kv_indptr, the pieces that num_ctas decode CTAs cut the batch into, with the
- * same arithmetic the decode and merge kernels use. Writes up to `capacity`
+ * kv_indptr, the pieces that num_ctas tier-1 plus tier2_ctas tier-2 decode
+ * CTAs cut the batch into, with the same arithmetic the decode and merge
+ * kernels use (tier2_ctas = 0: one tier; tier2_permille and tier2_min_units
+ * as in gqa_paged_decode_set_tuning, 0 = default). Writes up to `capacity`
  * rows of 9 int64 to `pieces`: decode CTA, sequence, head group, first and
  * one-past-last token (sequence-relative to kv_indices), partial slot (-1 for
  * a whole sequence written directly, else 0 / 1), and the merge kernel's view
@@ -161,7 +173,8 @@ int gqa_paged_kv_append(const void* k_new, const void* v_new, const int32_t* slo
  * (which may exceed capacity) or GQA_ERR_INVALID_ARGUMENT.
  */
 int64_t gqa_paged_decode_plan(const int32_t* kv_indptr, int batch, int num_ctas, int min_units_per_cta,
-                              int heads_per_cta, int64_t* pieces, int64_t capacity);
+                              int heads_per_cta, int tier2_ctas, int tier2_permille, int tier2_min_units,
+                              int64_t* pieces, int64_t capacity);
 
 /*
  * Synchronise the current device, then read and clear the sticky device error
@@ -183,16 +196,18 @@ int gqa_paged_decode_device_error(int* flags);
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture. Returns GQA_ERR_WORKSPACE, without launching, when the current
- * device and tuning need more scratch than GQA_NOALLOC_SCRATCH_BYTES
- * (gqa_paged_decode_ws_size() tells how much they need). All calls on a device
+ * capture. When the current device and tuning need more scratch than
+ * GQA_NOALLOC_SCRATCH_BYTES (gqa_paged_decode_ws_size() tells how much), the
+ * call uses fewer tier-2 CTAs so that its partials fit (results agree with
+ * gqa_paged_decode's to rounding); it returns GQA_ERR_WORKSPACE, without
+ * launching, only if even the tier-1 partials do not fit. All calls on a device
  * share the one array and it keeps the last call's contents (nothing in it
  * needs to start at zero: every partial a call reads, that call wrote first,
  * and the arrival counters carry a per-call tag), so calls whose kernels
  * overlap on the GPU - different streams, or several host threads - race on
  * it and give wrong results: order them on one stream. 32 MiB holds the
- * partials of every occupancy-limited launch (16 decode warps per SM, two
- * 4 KB partials each) on a GPU of up to 240 SMs.
+ * tier-1 partials of every occupancy-limited launch (16 decode warps per SM,
+ * two 4 KB partials each) on a GPU of up to 240 SMs.
  */
 #define GQA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 

@@ -38,11 +38,10 @@ _SIGNATURES = {
                                                 _vp, ctypes.c_int, _vp]),
     "gqa_paged_decode_release": (None, []),
     "gqa_paged_decode_strerror": (ctypes.c_char_p, [ctypes.c_int]),
-    "gqa_paged_decode_set_tuning": (ctypes.c_int, [ctypes.c_int] * 7),
+    "gqa_paged_decode_set_tuning": (ctypes.c_int, [ctypes.c_int] * 10),
     "gqa_paged_decode_set_profile_events": (ctypes.c_int, [_vp, _vp]),
     "gqa_paged_decode_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
-    "gqa_paged_decode_plan": (ctypes.c_int64, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp,
-                                               ctypes.c_int64]),
+    "gqa_paged_decode_plan": (ctypes.c_int64, [_vp] + [ctypes.c_int] * 7 + [_vp, ctypes.c_int64]),
     "gqa_paged_kv_append": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int, _vp]),
     "gqa_paged_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_int, _vp]),
 }
@@ -107,29 +106,31 @@ GATHER_LSU, GATHER_TMA = 0, 1
 
 
 def gqa_paged_decode_set_tuning(num_ctas=0, min_units_per_cta=0, heads_per_cta=0, tile=0, stages=0,
-                                gather=GATHER_LSU, fused_merge_max_splits=0) -> int:
+                                gather=GATHER_LSU, fused_merge_max_splits=0, tier2_ctas=0, tier2_permille=0,
+                                tier2_min_units=0) -> int:
     return load().gqa_paged_decode_set_tuning(num_ctas, min_units_per_cta, heads_per_cta, tile, stages, gather,
-                                              fused_merge_max_splits)
+                                              fused_merge_max_splits, tier2_ctas, tier2_permille, tier2_min_units)
 
 
 def gqa_paged_decode_set_profile_events(decode_start, decode_stop) -> int:
     return load().gqa_paged_decode_set_profile_events(decode_start, decode_stop)
 
 
-def gqa_paged_decode_plan(kv_indptr, num_ctas: int, min_units_per_cta: int = 0, heads_per_cta: int = 4):
+def gqa_paged_decode_plan(kv_indptr, num_ctas: int, min_units_per_cta: int = 0, heads_per_cta: int = 4,
+                          tier2_ctas: int = 0, tier2_permille: int = 0, tier2_min_units: int = 0):
     """Host-side split plan for a CPU int32 kv_indptr: a list of 9-tuples (decode CTA,
     sequence, head group, token lo, token hi, slot or -1, merge first CTA, merge last
-    CTA, merge first slot)."""
+    CTA, merge first slot). num_ctas tier-1 CTAs plus tier2_ctas tier-2 CTAs."""
     import numpy as np
     ip = np.ascontiguousarray(np.asarray(kv_indptr, dtype=np.int32))
     batch = ip.shape[0] - 1
     ptr = ip.ctypes.data_as(ctypes.c_void_p)
-    n = load().gqa_paged_decode_plan(ptr, batch, num_ctas, min_units_per_cta, heads_per_cta, None, 0)
+    args = (ptr, batch, num_ctas, min_units_per_cta, heads_per_cta, tier2_ctas, tier2_permille, tier2_min_units)
+    n = load().gqa_paged_decode_plan(*args, None, 0)
     if n < 0:
         raise GqaError(int(n), "gqa_paged_decode_plan")
     out = np.zeros((max(n, 1), 9), dtype=np.int64)
-    n2 = load().gqa_paged_decode_plan(ptr, batch, num_ctas, min_units_per_cta, heads_per_cta,
-                                      out.ctypes.data_as(ctypes.c_void_p), n)
+    n2 = load().gqa_paged_decode_plan(*args, out.ctypes.data_as(ctypes.c_void_p), n)
     assert n2 == n
     return [tuple(int(x) for x in row) for row in out[:n]]
 

@@ -23,8 +23,14 @@ using gqa::KernelChoice;
 
 constexpr int kMaxDevices = 64;
 constexpr int kDefaultMinUnits = 32;
-// Upper bound on decode CTAs a tuning may ask for.
+// Upper bound on tier-1 decode CTAs a tuning may ask for.
 constexpr int kMaxDecodeCtas = 1536;
+// Tier 2 by default: 2 CTAs per tier-1 CTA over the last 10 % of the units,
+// at least 64 units each.
+constexpr int kDefaultTier2PerTier1 = 2;
+constexpr int kDefaultTier2Permille = 100;
+constexpr int kDefaultTier2MinUnits = 64;
+constexpr int kMaxTier2Ctas = 1 << 16;
 constexpr int kSmemPerSm = 228 * 1024;
 constexpr int kSmemReservedPerCta = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -41,6 +47,9 @@ struct DeviceState {
 struct Tuning {
   int num_ctas = 0;
   int min_units = 0;
+  int tier2_ctas = 0;       // -1: one tier; 0: kDefaultTier2PerTier1 per tier-1 CTA; > 0: this many
+  int tier2_permille = kDefaultTier2Permille;
+  int tier2_min_units = kDefaultTier2MinUnits;
   int fuse_max_splits = gqa::kDefaultFuseMaxSplits;
   KernelChoice kernel = {gqa::kGatherLsu, 4, 16, 2};
 };
@@ -89,6 +98,17 @@ int decode_ctas(const DeviceState& st, const Tuning& t) {
   return st.sm_count * per_sm;
 }
 
+// The plan of a call; the grid is tier1_ctas + tier2_ctas CTAs.
+gqa::PlanConfig plan_config(const DeviceState& st, const Tuning& t) {
+  gqa::PlanConfig c;
+  c.tier1_ctas = decode_ctas(st, t);
+  c.tier2_ctas = t.tier2_ctas > 0 ? t.tier2_ctas : (t.tier2_ctas == 0 ? kDefaultTier2PerTier1 * c.tier1_ctas : 0);
+  c.min_units = t.min_units > 0 ? t.min_units : kDefaultMinUnits;
+  c.tier2_permille = t.tier2_permille;
+  c.tier2_min_units = t.tier2_min_units;
+  return c;
+}
+
 size_t partial_o_floats(int num_ctas, int ng) {
   return static_cast<size_t>(2) * num_ctas * ng * gqa::kGroup * gqa::kHeadDim;
 }
@@ -99,10 +119,15 @@ size_t partial_lse_bytes(int num_ctas, int ng) {
   return static_cast<size_t>(2) * num_ctas * ng * gqa::kGroup * sizeof(float);
 }
 
+size_t tickets_bytes(int num_ctas, int ng) { return static_cast<size_t>(num_ctas) * ng * sizeof(unsigned long long); }
+
+size_t split_rec_bytes(int num_ctas) { return static_cast<size_t>(num_ctas) * 16; }
+
+// Layout: partial O | partial LSE | arrival tickets | split records, each 256-byte aligned.
 size_t workspace_bytes(int num_ctas, int ng) {
   const size_t o = partial_o_floats(num_ctas, ng) * sizeof(float);
-  const size_t tickets = static_cast<size_t>(num_ctas) * ng * sizeof(unsigned long long);
-  return round256(o) + round256(partial_lse_bytes(num_ctas, ng)) + round256(tickets);
+  return round256(o) + round256(partial_lse_bytes(num_ctas, ng)) + round256(tickets_bytes(num_ctas, ng)) +
+         round256(split_rec_bytes(num_ctas));
 }
 
 int check_args(const void* q, const void* k, const void* v, const int32_t* indptr, const int32_t* indices,
@@ -116,9 +141,11 @@ int check_args(const void* q, const void* k, const void* v, const int32_t* indpt
   return GQA_OK;
 }
 
+// fit_ws: a caller workspace too small for the tuned plan makes the plan use
+// fewer tier-2 CTAs (down to none) instead of failing.
 int run(const void* q, const void* k, const void* v, const int32_t* indptr, const int32_t* indices, float sm_scale,
         void* out, float* lse, int batch, cudaStream_t stream, void* user_ws, size_t user_ws_bytes, bool checked,
-        int num_pages, int* dev_err) {
+        int num_pages, int* dev_err, bool fit_ws = false) {
   int rc = check_args(q, k, v, indptr, indices, sm_scale, out, lse, batch);
   if (rc != GQA_OK) return rc;
   if (batch == 0) return GQA_OK;
@@ -127,6 +154,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   int dev = 0;
   DeviceState* st = nullptr;
   Tuning tune;
+  gqa::PlanConfig cfg;
   cudaEvent_t ev0, ev1;
   void* ws = nullptr;
   {
@@ -136,8 +164,17 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
     tune = g_tune;
     ev0 = g_ev_start;
     ev1 = g_ev_stop;
-    const int ctas = decode_ctas(*st, tune);
-    const size_t need = workspace_bytes(ctas, tune.kernel.heads_per_cta);
+    cfg = plan_config(*st, tune);
+    const int ng = tune.kernel.heads_per_cta;
+    if (fit_ws && user_ws != nullptr) {
+      while (cfg.tier2_ctas > 0 && workspace_bytes(cfg.tier1_ctas + cfg.tier2_ctas, ng) > user_ws_bytes) {
+        const size_t per_cta = workspace_bytes(2, ng) - workspace_bytes(1, ng);
+        const size_t over = workspace_bytes(cfg.tier1_ctas + cfg.tier2_ctas, ng) - user_ws_bytes;
+        const int drop = static_cast<int>(over / (per_cta > 0 ? per_cta : 1)) + 1;
+        cfg.tier2_ctas = cfg.tier2_ctas > drop ? cfg.tier2_ctas - drop : 0;
+      }
+    }
+    const size_t need = workspace_bytes(cfg.tier1_ctas + cfg.tier2_ctas, ng);
     if (user_ws != nullptr) {
       if (user_ws_bytes < need || !aligned(user_ws, 256)) return GQA_ERR_WORKSPACE;
       ws = user_ws;
@@ -162,14 +199,14 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   }
 
   const int ng = tune.kernel.heads_per_cta;
-  const int ctas = decode_ctas(*st, tune);
+  const int ctas = cfg.tier1_ctas + cfg.tier2_ctas;
   float* part_o = static_cast<float*>(ws);
   const size_t lse_off = round256(partial_o_floats(ctas, ng) * sizeof(float));
   float* part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + lse_off);
-  unsigned long long* tickets = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + lse_off +
-                                                                       round256(partial_lse_bytes(ctas, ng)));
+  const size_t tickets_off = lse_off + round256(partial_lse_bytes(ctas, ng));
+  unsigned long long* tickets = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + tickets_off);
+  int4* split_rec = reinterpret_cast<int4*>(static_cast<char*>(ws) + tickets_off + round256(tickets_bytes(ctas, ng)));
   const unsigned long long epoch = (g_epoch.fetch_add(1) % ((1ull << 40) - 1)) + 1;
-  const int min_units = tune.min_units > 0 ? tune.min_units : kDefaultMinUnits;
 
   if (checked) {
     if (cudaMemsetAsync(dev_err, 0, sizeof(int), stream) != cudaSuccess) return GQA_ERR_LAUNCH;
@@ -193,9 +230,10 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   dp.err = err_word;
   dp.tickets = tickets;
   dp.epoch = epoch;
+  dp.split_rec = split_rec;
   dp.fuse_max_splits = tune.fuse_max_splits;
   dp.batch = batch;
-  dp.min_units = min_units;
+  dp.plan = cfg;
   dp.scale_log2 = sm_scale * kLog2e;
   dp.num_pages_check = checked ? num_pages : 0;
 
@@ -212,8 +250,9 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   mp.lse = lse;
   mp.skip_if_set = checked ? dev_err : nullptr;
   mp.batch = batch;
-  mp.num_decode_ctas = ctas;
-  mp.min_units = min_units;
+  mp.plan = cfg;
+  mp.split_rec = split_rec;
+  mp.epoch = epoch;
   mp.use_pdl = profile ? 0 : 1;
   mp.fuse_max_splits = tune.fuse_max_splits;
   if (gqa::launch_merge(ng, mp, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
@@ -223,6 +262,18 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
 bool valid_kernel(const KernelChoice& k) { return gqa::decode_smem_bytes(k) > 0; }
 
 }  // namespace
+
+namespace gqa {
+
+int decode_in_scratch(const void* q, const void* k_cache, const void* v_cache, const int* kv_indptr,
+                      const int* kv_indices, float sm_scale, void* out, float* lse, int batch, cudaStream_t stream,
+                      void* scratch, size_t scratch_bytes) {
+  if (scratch == nullptr && batch > 0) return GQA_ERR_WORKSPACE;
+  return run(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream, scratch, scratch_bytes,
+             false, 0, nullptr, true);
+}
+
+}  // namespace gqa
 
 extern "C" {
 
@@ -241,7 +292,8 @@ size_t gqa_paged_decode_ws_size(int batch, int64_t total_tokens_upper_bound) {
   DeviceState* st = nullptr;
   const int rc = current_device(&dev, &st);
   if (rc != GQA_OK && rc != GQA_ERR_UNSUPPORTED_DEVICE) return 0;
-  return workspace_bytes(decode_ctas(*st, g_tune), g_tune.kernel.heads_per_cta);
+  const gqa::PlanConfig c = plan_config(*st, g_tune);
+  return workspace_bytes(c.tier1_ctas + c.tier2_ctas, g_tune.kernel.heads_per_cta);
 }
 
 int gqa_paged_decode_ws(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_indptr,
@@ -293,13 +345,20 @@ const char* gqa_paged_decode_strerror(int code) {
 }
 
 int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_per_cta, int tile, int stages,
-                                int gather, int fused_merge_max_splits) {
+                                int gather, int fused_merge_max_splits, int tier2_ctas, int tier2_permille,
+                                int tier2_min_units) {
   if (num_ctas < 0 || min_units_per_cta < 0 || heads_per_cta < 0 || tile < 0 || stages < 0 || gather < 0)
     return GQA_ERR_INVALID_ARGUMENT;
   if (num_ctas > kMaxDecodeCtas || fused_merge_max_splits < -1) return GQA_ERR_INVALID_ARGUMENT;
+  if (tier2_ctas < -1 || tier2_ctas > kMaxTier2Ctas || tier2_permille < 0 || tier2_permille > 900 ||
+      tier2_min_units < 0)
+    return GQA_ERR_INVALID_ARGUMENT;
   Tuning t;
   t.num_ctas = num_ctas;
   t.min_units = min_units_per_cta;
+  t.tier2_ctas = tier2_ctas;
+  t.tier2_permille = tier2_permille > 0 ? tier2_permille : kDefaultTier2Permille;
+  t.tier2_min_units = tier2_min_units > 0 ? tier2_min_units : kDefaultTier2MinUnits;
   t.fuse_max_splits = fused_merge_max_splits == 0 ? gqa::kDefaultFuseMaxSplits
                                                   : (fused_merge_max_splits < 0 ? 1 : fused_merge_max_splits);
   t.kernel.gather = gather;
@@ -350,8 +409,12 @@ int gqa_paged_kv_append(const void* k_new, const void* v_new, const int32_t* slo
 }
 
 int64_t gqa_paged_decode_plan(const int32_t* kv_indptr, int batch, int num_ctas, int min_units_per_cta,
-                              int heads_per_cta, int64_t* pieces, int64_t capacity) {
+                              int heads_per_cta, int tier2_ctas, int tier2_permille, int tier2_min_units,
+                              int64_t* pieces, int64_t capacity) {
   if (kv_indptr == nullptr || batch < 0 || num_ctas <= 0 || min_units_per_cta < 0) return GQA_ERR_INVALID_ARGUMENT;
+  if (tier2_ctas < 0 || tier2_ctas > kMaxTier2Ctas || tier2_permille < 0 || tier2_permille > 900 ||
+      tier2_min_units < 0)
+    return GQA_ERR_INVALID_ARGUMENT;
   if (heads_per_cta != 1 && heads_per_cta != 2 && heads_per_cta != 4) return GQA_ERR_INVALID_ARGUMENT;
   if (batch == 0) return 0;
   if (kv_indptr[0] != 0) return GQA_ERR_INVALID_ARGUMENT;
@@ -361,11 +424,17 @@ int64_t gqa_paged_decode_plan(const int32_t* kv_indptr, int batch, int num_ctas,
   const int64_t T = kv_indptr[batch];
   const int hg_count = gqa::kKvHeads / heads_per_cta;
   const int64_t W = T * hg_count;
-  const int64_t q = gqa::units_per_cta(W, num_ctas, min_units_per_cta > 0 ? min_units_per_cta : kDefaultMinUnits);
+  gqa::PlanConfig cfg;
+  cfg.tier1_ctas = num_ctas;
+  cfg.tier2_ctas = tier2_ctas;
+  cfg.min_units = min_units_per_cta > 0 ? min_units_per_cta : kDefaultMinUnits;
+  cfg.tier2_permille = tier2_permille > 0 ? tier2_permille : kDefaultTier2Permille;
+  cfg.tier2_min_units = tier2_min_units > 0 ? tier2_min_units : kDefaultTier2MinUnits;
+  const gqa::Plan pl = gqa::make_plan(W, cfg);
   int64_t n = 0;
-  for (int64_t cta = 0; cta < num_ctas; ++cta) {
-    const int64_t u0 = cta * q;
-    const int64_t u1 = u0 + q < W ? u0 + q : W;
+  for (int64_t cta = 0; cta < static_cast<int64_t>(num_ctas) + tier2_ctas; ++cta) {
+    const int64_t u0 = pl.begin(cta);
+    const int64_t u1 = pl.end(cta);
     int64_t u = u0;
     while (u < u1) {
       const int64_t hg = u / T;
@@ -383,7 +452,7 @@ int64_t gqa_paged_decode_plan(const int32_t* kv_indptr, int batch, int num_ctas,
       if (t_hi <= t) return GQA_ERR_INVALID_ARGUMENT;  // malformed table
       const bool whole = (t == seq_lo && t_hi == seq_hi);
       const int slot = whole ? -1 : (hg * T + t == u0 ? 0 : 1);
-      const gqa::SeqSplit sp = gqa::seq_split(hg * T + seq_lo, hg * T + seq_hi, q);
+      const gqa::SeqSplit sp = gqa::seq_split(pl, hg * T + seq_lo, hg * T + seq_hi);
       if (n < capacity && pieces != nullptr) {
         int64_t* row = pieces + 9 * n;
         row[0] = cta;

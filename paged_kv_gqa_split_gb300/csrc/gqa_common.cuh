@@ -308,11 +308,10 @@ __device__ __forceinline__ void merge_split_warp_staged(const float* part_o, con
 
 // Normalise and write a finished piece: bf16 O rows q-heads h0 .. h0+7 of
 // sequence b plus their LSE (final), or an fp32 partial (O_i, LSE_i) into
-// slot `sid` (layout [sid][NG][128 dims][8 heads], LSE [sid][NG][8]). A
-// partial of a sequence cut into at most fuse_max_splits pieces also takes
-// that sequence's ticket. Returns true when this warp brought the last piece:
-// it then owes the merge (merge_split_warp), which it runs after its main loop
-// so that the merge's registers do not compete with the pipeline's.
+// slot `sid` (layout [sid][NG][128 dims][8 heads], LSE [sid][NG][8]). Returns
+// true for a partial of a sequence cut into at most fuse_max_splits pieces:
+// the warp must count its arrival (arrive_pieces) after its main loop, and
+// merges the sequence if its arrival was the last.
 template <int NG>
 __device__ __forceinline__ bool finish_piece(const HeadState& st, bool final_piece, int64_t b, int h0, int64_t sid,
                                              int w, const SplitInfo& si, const DecodeParams& p, int lane) {
@@ -349,20 +348,46 @@ __device__ __forceinline__ bool finish_piece(const HeadState& st, bool final_pie
         make_float2(st.acc[mt][2] * i0, st.acc[mt][3] * i1);
   }
   if (r == 0) *reinterpret_cast<float2*>(p.part_lse + (sid * NG + w) * kGroup + 2 * c) = make_float2(lse0, lse1);
-  if (si.S > p.fuse_max_splits) return false;  // the merge kernel combines this sequence
-  __threadfence();  // this lane's partial is visible device-wide before the ticket moves
-  __syncwarp();
-  unsigned arrived = 0;
-  if (lane == 0) arrived = ticket_arrive(p.tickets + static_cast<int64_t>(si.first_cta) * NG + w, p.epoch, p.err);
-  arrived = __shfl_sync(0xffffffffu, arrived, 0);
-  return arrived == static_cast<unsigned>(si.S);
+  return si.S <= p.fuse_max_splits;  // else the merge kernel combines this sequence
 }
 
-// A merge a warp owes (see finish_piece): at most two per warp, since only the
-// first and the last piece of a CTA's range can be partials.
+// Split record of decode CTA `cta`: how the sequence holding the last unit of
+// its range is cut (sequence b of head group hg, pieces first_cta .. first_cta
+// + S - 1, slot of the first piece), tagged with the low 32 bits of the call's
+// epoch. The merge kernel's CTA for the boundary after `cta` reads it instead
+// of searching kv_indptr.
+__device__ __forceinline__ void write_split_rec(int4* rec, int cta, unsigned long long epoch, int b, int hg,
+                                                const SplitInfo& si) {
+  rec[cta] = make_int4(static_cast<int>(static_cast<unsigned>(epoch)), b, si.first_cta,
+                       (si.S << 3) | (hg << 1) | si.first_slot);
+}
+
+// A split piece whose arrival a warp still has to count (see finish_piece): at
+// most two per warp, since only the first and the last piece of a CTA's range
+// can be partials.
 struct OwedMerge {
   SplitInfo si;
   int b, h0;
 };
+
+// After its main loop, a warp counts the arrivals of its (at most two) pending
+// pieces: one fence makes all of its partials visible device-wide, then lanes
+// 0 and 1 move the two tickets in parallel. Bit i of the result is set when
+// pending piece i was the last of its sequence to arrive, so this warp owes
+// that sequence's merge. Deferring the arrivals keeps the fence and the atomic
+// round trips out of the streaming loop.
+template <int NG>
+__device__ __forceinline__ unsigned arrive_pieces(const OwedMerge (&pend)[2], int n, int w, const DecodeParams& p,
+                                                  int lane) {
+  __threadfence();
+  __syncwarp();
+  bool last = false;
+  if (lane < n) {
+    const SplitInfo si = lane == 0 ? pend[0].si : pend[1].si;
+    const unsigned arrived = ticket_arrive(p.tickets + static_cast<int64_t>(si.first_cta) * NG + w, p.epoch, p.err);
+    last = arrived == static_cast<unsigned>(si.S);
+  }
+  return __ballot_sync(0xffffffffu, last);
+}
 
 }  // namespace gqa

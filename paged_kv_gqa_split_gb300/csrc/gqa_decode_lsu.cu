@@ -44,13 +44,31 @@ struct LsuCfg {
   static constexpr int kStageBytes = kHdrOff + 32;    // tile header: 8 ints
   static constexpr int kIdsRing = 256;                // page ids held per warp (tokens)
   static constexpr int kIdsOff = D * kStageBytes;
-  static constexpr int kWarpBytes = kIdsOff + kIdsRing * 4;
+  static constexpr int kPlanOff = kIdsOff + kIdsRing * 4;  // the warp's copy of the plan (SmemPlan)
+  static constexpr int kWarpBytes = kPlanOff + 32;
   static constexpr int kThreads = NG * 32;
   static constexpr int kSmemBytes = NG * kWarpBytes;
   static_assert(D >= 2, "at least double buffering");
   static_assert(kStageBytes % 16 == 0 && kWarpBytes % 16 == 0, "16-byte aligned stages");
   static_assert(kSmemBytes <= 227 * 1024, "ring exceeds shared memory");
 };
+
+// What the walker needs of the plan when a piece starts (where the piece's
+// sequence is cut), kept in shared memory so that it holds no registers in
+// the streaming loop.
+struct SmemPlan {
+  int64_t W1, q1, q2;
+  int P1, unused;
+};
+
+__device__ __forceinline__ SeqSplit seq_split_smem(const SmemPlan* sp, int64_t u_lo, int64_t u_hi) {
+  Plan pl;
+  pl.W1 = sp->W1;
+  pl.q1 = sp->q1;
+  pl.q2 = sp->q2;
+  pl.P1 = sp->P1;
+  return seq_split(pl, u_lo, u_hi);
+}
 
 struct Tile {
   int b, cnt, flags, hg, tt;
@@ -77,10 +95,15 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
   const __nv_bfloat16* __restrict__ qg = static_cast<const __nv_bfloat16*>(p.q);
   const int B = p.batch;
   const int T = __ldg(p.kv_indptr + B);
-  const int64_t W = static_cast<int64_t>(T) * C::kHG;
-  const int64_t q = units_per_cta(W, gridDim.x, p.min_units);
-  const int64_t u0 = static_cast<int64_t>(blockIdx.x) * q;
-  const int64_t u1 = min(u0 + q, W);
+  SmemPlan* splan = reinterpret_cast<SmemPlan*>(wsm + C::kPlanOff);
+  int64_t u0, u1;
+  {
+    const Plan pl = make_plan(static_cast<int64_t>(T) * C::kHG, p.plan);
+    u0 = pl.begin(blockIdx.x);
+    u1 = pl.end(blockIdx.x);
+    if (lane == 0) *splan = SmemPlan{pl.W1, pl.q1, pl.q2, pl.P1, 0};
+    __syncwarp();
+  }
 
   // ------------------------------------------------------------- walker
   int64_t u_next = u0;      // first unit of the next head-group segment
@@ -119,7 +142,7 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
           p_flags = F_QLOAD | ((tt == seq_lo && p_hi == seq_hi) ? F_FINAL : 0) |
                     ((static_cast<int64_t>(hg) * T + tt != u0) ? F_SLOT1 : 0);
           const int64_t base_u = static_cast<int64_t>(hg) * T;
-          const SeqSplit sp = seq_split(base_u + seq_lo, base_u + seq_hi, q);
+          const SeqSplit sp = seq_split_smem(splan, base_u + seq_lo, base_u + seq_hi);
           p_si.S = static_cast<int>(sp.last_cta - sp.first_cta + 1);
           p_si.first_cta = static_cast<int>(sp.first_cta);
           p_si.first_slot = sp.first_slot;
@@ -142,19 +165,21 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
       u_next = static_cast<int64_t>(hg) * T + t_stop;
       seg_open = true;
       p_hi = tt;
+      // the page ids depend on tt alone: request them first, so that their
+      // round trip overlaps the search of kv_indptr
+      ib = tt & ~31;
+#pragma unroll
+      for (int c = 0; c < C::kIdsRing / 32; ++c) request_ids(ib + 32 * c + lane);
+      cp_async_commit();
       wb = warp_find_seq(p.kv_indptr, B, tt, lane);
+      if (wb >= 0) win = load_indptr_window(p.kv_indptr, B, wb, lane);
+      cp_async_wait<0>();
+      __syncwarp();
       if (wb < 0) {
         if (lane == 0) atomicOr(p.err, kErrBadIndptr);
         walk_ok = false;
         break;
       }
-      win = load_indptr_window(p.kv_indptr, B, wb, lane);
-      ib = tt & ~31;
-#pragma unroll
-      for (int c = 0; c < C::kIdsRing / 32; ++c) request_ids(ib + 32 * c + lane);
-      cp_async_commit();
-      cp_async_wait<0>();
-      __syncwarp();
     }
     return false;
   };
@@ -222,8 +247,8 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
   const uint32_t k_lane = C::kKOff + ((lane & 7) + ((lane >> 3) & 1) * 8) * C::kRowPitch + (lane >> 4) * 16;
   const uint32_t v_lane = C::kVOff + ((lane & 7) + (lane >> 4) * 8) * C::kRowPitch + ((lane >> 3) & 1) * 16;
 
-  OwedMerge owed[2];
-  int n_owed = 0;
+  OwedMerge pend[2];  // split pieces whose arrival is counted after the loop
+  int n_pend = 0;
 #pragma unroll 1
   for (int i = 0; i < D - 1; ++i) issue();
 #pragma unroll 1
@@ -253,21 +278,26 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
     if (flags & F_END) {
       if (finish_piece<NG>(st, (flags & F_FINAL) != 0, hb, h0, slot_id(blockIdx.x, (flags & F_SLOT1) ? 1 : 0), w,
                            si, p, lane)) {
-        owed[n_owed < 2 ? n_owed : 1] = {si, hb, h0};
-        ++n_owed;
+        pend[n_pend < 2 ? n_pend : 1] = {si, hb, h0};
+        n_pend = min(n_pend + 1, 2);
       }
     }
     __syncwarp();  // every lane is done with this stage before it is refilled
   }
   cp_async_wait<0>();
-  // merges this warp owes: every other piece's partial is visible by now; the
-  // warp's drained ring stages the partials
+  if (w == 0 && lane == 0 && u0 < u1 && walk_ok) write_split_rec(p.split_rec, blockIdx.x, p.epoch, pb, hg, p_si);
+  if (n_pend == 0) return;
+  // count the pending arrivals; for each that came last, merge the sequence
+  // (every other piece's partial is visible by then), staging the partials
+  // through the warp's drained ring
+  const unsigned owe = arrive_pieces<NG>(pend, n_pend, w, p, lane);
   constexpr int kStageCap = C::kWarpBytes / kStagedPartialBytes;
   static_assert(kStageCap >= 2, "ring too small to stage partials");
 #pragma unroll 1
-  for (int i = 0; i < n_owed && i < 2; ++i) {
+  for (int i = 0; i < 2; ++i) {
+    if (!((owe >> i) & 1u)) continue;
     __threadfence();
-    merge_split_warp_staged<NG>(p.part_o, p.part_lse, owed[i].si, w, owed[i].b, owed[i].h0,
+    merge_split_warp_staged<NG>(p.part_o, p.part_lse, pend[i].si, w, pend[i].b, pend[i].h0,
                                 static_cast<__nv_bfloat16*>(p.out), p.lse, wbase, wsm, kStageCap, lane);
   }
 }

@@ -82,10 +82,9 @@ __device__ __forceinline__ void tma_producer(const DecodeParams& p, uint32_t sba
 
   const int B = p.batch;
   const int T = __ldg(p.kv_indptr + B);
-  const int64_t W = static_cast<int64_t>(T) * C::kHG;
-  const int64_t q = units_per_cta(W, gridDim.x, p.min_units);
-  const int64_t u0 = static_cast<int64_t>(blockIdx.x) * q;
-  const int64_t u1 = min(u0 + q, W);
+  const Plan pl = make_plan(static_cast<int64_t>(T) * C::kHG, p.plan);
+  const int64_t u0 = pl.begin(blockIdx.x);
+  const int64_t u1 = pl.end(blockIdx.x);
 
   uint32_t tiles = 0;
   bool ok = true;
@@ -145,6 +144,8 @@ __device__ __forceinline__ void tma_producer(const DecodeParams& p, uint32_t sba
     return true;
   };
 
+  int last_b = 0, last_hg = 0;  // the range's last piece, for the split record
+  SplitInfo last_si = {1, 0, 0};
   int64_t u = u0;
   while (ok && u < u1) {
     const int hg = static_cast<int>(u / T);
@@ -188,9 +189,12 @@ __device__ __forceinline__ void tma_producer(const DecodeParams& p, uint32_t sba
       int pflags = 0;
       if (t == seq_lo && p_hi == seq_hi) pflags |= F_FINAL;
       if (static_cast<int64_t>(hg) * T + t != u0) pflags |= F_SLOT1;
-      const SeqSplit sp = seq_split(static_cast<int64_t>(hg) * T + seq_lo, static_cast<int64_t>(hg) * T + seq_hi, q);
+      const SeqSplit sp = seq_split(pl, static_cast<int64_t>(hg) * T + seq_lo, static_cast<int64_t>(hg) * T + seq_hi);
       const SplitInfo si = {static_cast<int>(sp.last_cta - sp.first_cta + 1), static_cast<int>(sp.first_cta),
                             sp.first_slot};
+      last_b = b;
+      last_hg = hg;
+      last_si = si;
 
       for (int tt = t; tt < p_hi; tt += TILE) {
         const int cnt = min(TILE, p_hi - tt);
@@ -216,6 +220,7 @@ __device__ __forceinline__ void tma_producer(const DecodeParams& p, uint32_t sba
     }
     u = static_cast<int64_t>(hg) * T + t_stop;
   }
+  if (ok && u0 < u1 && lane == 0) write_split_rec(p.split_rec, blockIdx.x, p.epoch, last_b, last_hg, last_si);
 
   if (ok) {
     // end-of-work marker
@@ -265,6 +270,8 @@ __device__ __forceinline__ void tma_consumer(const DecodeParams& p, uint32_t sba
   const uint32_t k_lane = C::kKOff + ((lane & 7) + ((lane >> 3) & 1) * 8) * C::kRowPitch + w * 256 + (lane >> 4) * 16;
   const uint32_t v_lane = C::kVOff + ((lane & 7) + (lane >> 4) * 8) * C::kRowPitch + w * 256 + ((lane >> 3) & 1) * 16;
 
+  OwedMerge pend[2];  // split pieces whose arrival is counted after the loop
+  int n_pend = 0;
   for (uint32_t tiles = 0;; ++tiles) {
     const int stage = tiles % STAGES;
     const uint32_t par = (tiles / STAGES) & 1u;
@@ -275,7 +282,7 @@ __device__ __forceinline__ void tma_consumer(const DecodeParams& p, uint32_t sba
     SplitInfo si;
     int unused;
     ld_shared_v4(sb + C::kHdrOff + 16, si.S, si.first_cta, si.first_slot, unused);
-    if (flags & F_DONE) return;
+    if (flags & F_DONE) break;
     if (flags & F_QLOAD) {
 #pragma unroll
       for (int j = 0; j < 4; ++j)
@@ -296,10 +303,19 @@ __device__ __forceinline__ void tma_consumer(const DecodeParams& p, uint32_t sba
       const int h0 = (hg * NG + w) * kGroup;
       if (finish_piece<NG>(st, (flags & F_FINAL) != 0, hb, h0, slot_id(blockIdx.x, (flags & F_SLOT1) ? 1 : 0), w,
                            si, p, lane)) {
-        __threadfence();
-        merge_split_warp<NG>(p.part_o, p.part_lse, si, w, hb, h0, static_cast<__nv_bfloat16*>(p.out), p.lse, lane);
+        pend[n_pend < 2 ? n_pend : 1] = {si, hb, h0};
+        n_pend = min(n_pend + 1, 2);
       }
     }
+  }
+  if (n_pend == 0) return;
+  const unsigned owe = arrive_pieces<NG>(pend, n_pend, w, p, lane);
+#pragma unroll 1
+  for (int i = 0; i < 2; ++i) {
+    if (!((owe >> i) & 1u)) continue;
+    __threadfence();
+    merge_split_warp<NG>(p.part_o, p.part_lse, pend[i].si, w, pend[i].b, pend[i].h0,
+                         static_cast<__nv_bfloat16*>(p.out), p.lse, lane);
   }
 }
 

@@ -1,10 +1,12 @@
 // Internal interface between the C ABI (gqa_api.cu) and the kernels
-// (gqa_decode.cu). Not part of the public header.
+// (gqa_decode_lsu.cu, gqa_decode_tma.cu, gqa_merge.cu). Not part of the public header.
 #pragma once
 
 #include <cuda_runtime.h>
 
 #include <cstdint>
+
+#include "gqa_plan.h"
 
 namespace gqa {
 
@@ -23,22 +25,25 @@ struct DecodeParams {
   const int* kv_indices;
   void* out;
   float* lse;
-  float* part_o;    // [2 * num_ctas][NG][128 dims][8 heads] fp32
-  float* part_lse;  // [2 * num_ctas][NG][8 heads] fp32
+  float* part_o;    // [2 * (P1 + P2)][NG][128 dims][8 heads] fp32
+  float* part_lse;  // [2 * (P1 + P2)][NG][8 heads] fp32
   const int* skip_if_set;  // optional: return without work if *skip_if_set != 0
   int* err;                // device error word (bit flags below)
-  unsigned long long* tickets;  // [num_ctas][NG] arrival tickets of split sequences
+  unsigned long long* tickets;  // [P1 + P2][NG] arrival tickets of split sequences
   unsigned long long epoch;     // this call's ticket epoch (never 0, < 2^40)
+  int4* split_rec;              // [P1 + P2] per-CTA split records for the merge kernel
+  PlanConfig plan;              // the grid is plan.tier1_ctas + plan.tier2_ctas CTAs
   int batch;
-  int min_units;
   float scale_log2;        // sm_scale * log2(e)
   int num_pages_check;     // > 0: page ids are range-checked against it
   int fuse_max_splits;     // split sequences of at most this many pieces are merged by the decode kernel
 };
 
-// Default: sequences cut into at most this many pieces are merged inside the
-// decode kernel; longer splits go to the merge kernel.
-constexpr int kDefaultFuseMaxSplits = 16;
+// Default: every split sequence goes to the merge kernel, whose CTAs share the
+// work of one sequence; merging inside the decode kernel (the warp that brings
+// a sequence's last piece combines its partials) is a tuning option for
+// sequences cut into at most fuse_max_splits pieces.
+constexpr int kDefaultFuseMaxSplits = 1;
 
 // Merge CTAs per boundary between consecutive decode CTAs.
 constexpr int kMergeCtasPerBoundary = 1;
@@ -50,12 +55,20 @@ struct MergeParams {
   void* out;
   float* lse;
   const int* skip_if_set;
+  const int4* split_rec;          // the decode CTAs' split records
+  unsigned long long epoch;       // the call's epoch (tags the records)
+  PlanConfig plan;  // the decode kernel's plan
   int batch;
-  int num_decode_ctas;
-  int min_units;
   int use_pdl;
   int fuse_max_splits;  // sequences of at most this many pieces were merged by the decode kernel
 };
+
+// Decode with the split partials in a fixed caller scratch (gqa_api.cu): a plan
+// whose partials do not fit uses fewer tier-2 CTAs, down to none. Returns a
+// GQA_* code (GQA_ERR_WORKSPACE if even the tier-1 partials do not fit).
+int decode_in_scratch(const void* q, const void* k_cache, const void* v_cache, const int* kv_indptr,
+                      const int* kv_indices, float sm_scale, void* out, float* lse, int batch, cudaStream_t stream,
+                      void* scratch, size_t scratch_bytes);
 
 // Compile-time variant of the decode kernel.
 enum : int { kGatherLsu = 0, kGatherTma = 1 };

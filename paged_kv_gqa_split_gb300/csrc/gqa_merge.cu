@@ -22,19 +22,17 @@ __device__ int g_device_error;
 // -------------------------------------------------------------------- merge
 // One CTA per boundary between decode CTAs j and j + 1; it merges the sequence
 // cut there only if that sequence has more pieces than the decode kernel
-// merges itself (fuse_max_splits).
-// They hold no shared memory and few registers, so they sit beside the decode
-// CTAs (programmatic dependent launch) and run their prologue - locating the
-// sequence cut at their boundary - while the decode grid is still running.
-// After the decode grid completes, one round of loads remains: each split's
-// partial LSE and O are folded in with a running maximum, so the weights need
-// no second pass.
+// merges itself (fuse_max_splits). Decode CTA j leaves a 16-byte record of how
+// the sequence holding its last unit is cut, so after the decode grid
+// completes a merge CTA needs one load to find its work, then one round of
+// loads of the partials: each split's LSE and O are folded in with a running
+// maximum, so the weights need no second pass. With 6 KB of shared memory, one
+// merge CTA fits beside three decode CTAs on an SM (programmatic dependent
+// launch) and starts before the decode grid has drained.
 constexpr int kMergeThreads = 128;
 constexpr int kMergeWarps = kMergeThreads / 32;
-// Split counts up to this use the CTA-per-item path (warps share the splits);
-// above it, lanes share the splits of one (head, dim) item.
-constexpr int kMergeMediumSplits = 64;
-// Split counts up to this: one warp per (head, 32-dim chunk) item, all splits.
+// Split counts up to this: one warp per (head, 32-dim chunk) item, all splits;
+// above it, the block path spreads each sequence over its boundary CTAs.
 constexpr int kMergeSmallSplits = 16;
 
 template <int NG>
@@ -80,46 +78,54 @@ template <int NG>
 __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const MergeParams p) {
   constexpr int kHG = kKvHeads / NG;
   constexpr int kH8 = NG * kGroup;  // query heads per head group
-  // cross-warp combine buffer of the medium-split path: one lane's state at a time
-  __shared__ float xw[32][3 * kGroup];
+  // row-group states of the block path: [group * cols + col] -> (m[4], den[4], acc[4]); 6 KB,
+  // small enough for one merge CTA to sit beside three decode CTAs on an SM
+  __shared__ float xw[128][12];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (p.skip_if_set != nullptr && *p.skip_if_set != 0) return;
   const int B = p.batch;
+  const int j = blockIdx.x;  // boundary between decode CTAs j and j + 1
+  const bool boundary = j + 1 < p.plan.tier1_ctas + p.plan.tier2_ctas;
+  // Loads that do not depend on the decode grid go out before the wait, so
+  // their round trip overlaps it; nothing waits on them until after it.
+  const int T = __ldg(p.kv_indptr + B);
+  const bool check_empty = j < B;
+  const int e_lo = check_empty ? __ldg(p.kv_indptr + j) : 0;
+  const int e_hi = check_empty ? __ldg(p.kv_indptr + j + 1) : 0;
+
+  // Everything below reads what the decode grid wrote.
+  pdl_wait();
+  // The sequence holding decode CTA j's last unit, as that CTA recorded it
+  // (read before checking that CTA j had work, to save a round trip).
+  const int4 rec = boundary ? __ldcg(p.split_rec + j) : make_int4(0, 0, 0, 0);
 
   // Empty sequences: O = 0, LSE = -inf (no decode CTA touches them).
-  for (int b = blockIdx.x; b < B; b += gridDim.x) {
-    if (__ldg(p.kv_indptr + b) == __ldg(p.kv_indptr + b + 1)) {
+  for (int b = j; b < B; b += gridDim.x) {
+    if (b == j ? e_lo == e_hi : __ldg(p.kv_indptr + b) == __ldg(p.kv_indptr + b + 1)) {
       uint4* ob = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(b) * kQoHeads * kHeadDim);
       for (int i = tid; i < kQoHeads * kHeadDim * 2 / 16; i += kMergeThreads) ob[i] = make_uint4(0, 0, 0, 0);
       if (tid < kQoHeads) p.lse[static_cast<int64_t>(b) * kQoHeads + tid] = -INFINITY;
     }
   }
 
-  const int T = __ldg(p.kv_indptr + B);
-  const int64_t W = static_cast<int64_t>(T) * kHG;
-  const int64_t q = units_per_cta(W, p.num_decode_ctas, p.min_units);
-  const int j = blockIdx.x;  // boundary between decode CTAs j and j + 1
-  const int64_t u = static_cast<int64_t>(j + 1) * q;
-  if (u >= W) return;
-  const int hg = static_cast<int>(u / T);
-  const int t = static_cast<int>(u - static_cast<int64_t>(hg) * T);
-  const int b = warp_find_seq(p.kv_indptr, B, t, lane);  // every warp searches (L1-resident)
-  if (b < 0) return;
-  const int seq_lo = __ldg(p.kv_indptr + b);
-  if (t == seq_lo) return;  // the boundary falls between two sequences: nothing is split here
-  const int seq_hi = __ldg(p.kv_indptr + b + 1);
-  const int64_t base_u = static_cast<int64_t>(hg) * T;
-  const SeqSplit sp = seq_split(base_u + seq_lo, base_u + seq_hi, q);
-  const int S = static_cast<int>(sp.last_cta - sp.first_cta + 1);
+  const Plan pl = make_plan(static_cast<int64_t>(T) * kHG, p.plan);
+  if (!boundary || pl.begin(j + 1) >= pl.W) return;  // CTA j + 1 has no work: neither has this boundary
+  if (static_cast<unsigned>(rec.x) != static_cast<unsigned>(p.epoch)) return;  // CTA j stopped on an error
+  const int b = rec.y;
+  const int S = rec.w >> 3;
+  const int hg = (rec.w >> 1) & 3;
+  SeqSplit sp;
+  sp.first_cta = rec.z;
+  sp.first_slot = rec.w & 1;
+  sp.last_cta = sp.first_cta + S - 1;
+  if (b < 0 || b >= B || hg >= kHG || S < 1 || sp.first_cta > j) return;
+  if (sp.last_cta <= j) return;         // the sequence ends at this boundary: nothing is split here
   if (S <= p.fuse_max_splits) return;  // the decode kernel merged it
   const int rank = j - static_cast<int>(sp.first_cta);  // which of this sequence's S - 1 boundaries
   const int nranks = S - 1;
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(b) * kQoHeads + hg * kH8) * kHeadDim;
   float* lo = p.lse + static_cast<int64_t>(b) * kQoHeads + hg * kH8;
-
-  // Everything below reads the decode kernel's partials.
-  pdl_wait();
 
   if (S <= kMergeSmallSplits) {
     // (reached when the decode kernel's own merge is turned down by tuning)
@@ -142,83 +148,117 @@ __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const MergePar
         for (int h = 0; h < 8; ++h) lo[g * kGroup + h] = ma.m[h] + log2f(ma.den[h]);
       }
     }
-  } else if (S <= kMergeMediumSplits) {
-    // CTA item = (KV head g, 32-dim chunk): lane = one dim of all 8 heads; the
-    // four warps take every fourth split, then fold their states together
-    for (int it = rank; it < NG * 4; it += nranks) {
-      const int g = it >> 2;
-      const int d = (it & 3) * 32 + lane;
-      MergeAcc ma;
-      ma.init();
-#pragma unroll 4
-      for (int s = warp; s < S; s += kMergeWarps) {
-        const float4* lr = reinterpret_cast<const float4*>(partial_lse_row<NG>(p, sp, s, g));
-        const float4* orow = reinterpret_cast<const float4*>(partial_o_row<NG>(p, sp, s, g, d));
-        ma.add(lr[0], lr[1], __ldcg(orow), __ldcg(orow + 1));
-      }
-      for (int src = 1; src < kMergeWarps; ++src) {
-        __syncthreads();
-        if (warp == src) {
-#pragma unroll
-          for (int h = 0; h < 8; ++h) {
-            xw[lane][h] = ma.m[h];
-            xw[lane][8 + h] = ma.den[h];
-            xw[lane][16 + h] = ma.acc[h];
-          }
-        }
-        __syncthreads();
-        if (warp == 0) {
-#pragma unroll
-          for (int h = 0; h < 8; ++h) {
-            const float m2 = xw[lane][h];
-            const float mn = fmaxf(ma.m[h], m2);
-            const float s1 = ex2(ma.m[h] - mn), s2 = ex2(m2 - mn);  // a warp that saw no split has m = -inf
-            ma.den[h] = ma.den[h] * s1 + xw[lane][8 + h] * s2;
-            ma.acc[h] = ma.acc[h] * s1 + xw[lane][16 + h] * s2;
-            ma.m[h] = mn;
-          }
-        }
-      }
-      if (warp == 0) {
-#pragma unroll
-        for (int h = 0; h < 8; ++h) ob[(g * kGroup + h) * kHeadDim + d] = __float2bfloat16_rn(ma.acc[h] / ma.den[h]);
-        if ((it & 3) == 0 && lane == 0) {
-#pragma unroll
-          for (int h = 0; h < 8; ++h) lo[g * kGroup + h] = ma.m[h] + log2f(ma.den[h]);
-        }
-      }
-    }
   } else {
-    // warp item = (KV head g, dim d): lanes stride over the splits, then one warp
-    // reduction; items are dealt boundary-fastest over all of this sequence's CTAs
-    const int first_item = warp * nranks + rank;
-    const int item_step = kMergeWarps * nranks;
-    for (int it = first_item; it < NG * kHeadDim; it += item_step) {
-      const int g = it / kHeadDim;
-      const int d = it - g * kHeadDim;
-      MergeAcc ma;
-      ma.init();
-#pragma unroll 4
-      for (int s = lane; s < S; s += 32) {
-        const float4* lr = reinterpret_cast<const float4*>(partial_lse_row<NG>(p, sp, s, g));
-        const float4* orow = reinterpret_cast<const float4*>(partial_o_row<NG>(p, sp, s, g, d));
-        ma.add(lr[0], lr[1], __ldcg(orow), __ldcg(orow + 1));
+    // Block item = (KV head g, dims [d0, d0 + dc)) over all S splits. Threads
+    // form rows x cols: a column is one dim and 4 of the 8 heads (16 bytes of
+    // a partial O row), a row walks every rows-th split. dc is the smallest
+    // power of two whose items fit the sequence's S - 1 boundary CTAs, so a
+    // CTA holds about one split's worth of partials (16 KB at NG = 4) and each
+    // thread issues its loads in one batch of up to 8 splits.
+    const int need = (NG * kHeadDim + nranks - 1) / nranks;
+    int dc = 1;
+    while (dc < need && dc < 32) dc <<= 1;
+    const int cols = 2 * dc;
+    const int rows = kMergeThreads / cols;
+    const int col = tid % cols, row = tid / cols;
+    const int span = cols < 32 ? 32 : cols;        // lanes (or threads) that one row group spans
+    const int group = tid / span;                  // row group left after the in-warp combine
+    const int ngroups = kMergeThreads / span;
+    const bool leader = (tid % span) < cols;
+    const int hq = col & 1;                        // heads 4 hq .. 4 hq + 3
+    // a row's LSE rows are loaded by its columns 0 and 1 and shuffled to the rest
+    const int wcols = cols < 32 ? cols : 32;       // columns of a row within one warp
+    const bool lse_loader = (lane & (wcols - 1)) < 2;
+    const int lse_src = (lane & ~(wcols - 1)) | hq;
+    const int items = NG * (kHeadDim / dc);
+    for (int it = rank; it < items; it += nranks) {
+      const int g = it / (kHeadDim / dc);
+      const int d = (it % (kHeadDim / dc)) * dc + (col >> 1);
+      float m[4], den[4], acc[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        m[i] = -INFINITY;
+        den[i] = 0.f;
+        acc[i] = 0.f;
       }
+      for (int s0 = 0; s0 < S; s0 += 8 * rows) {  // same trip count in every lane (the shuffles need it)
+        float4 lv[8], ov[8];
 #pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        float mx = ma.m[h];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float sc = ex2(ma.m[h] - mx);  // lanes that saw no split contribute 0
-        float dn = ma.den[h] * sc, ac = ma.acc[h] * sc;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          dn += __shfl_xor_sync(0xffffffffu, dn, o);
-          ac += __shfl_xor_sync(0xffffffffu, ac, o);
+        for (int k = 0; k < 8; ++k) {  // the whole batch is in flight before the first fold
+          const int s = s0 + k * rows + row;
+          lv[k] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (s < S) {
+            if (lse_loader) lv[k] = __ldcg(reinterpret_cast<const float4*>(partial_lse_row<NG>(p, sp, s, g)) + hq);
+            ov[k] = __ldcg(reinterpret_cast<const float4*>(partial_o_row<NG>(p, sp, s, g, d)) + hq);
+          }
         }
-        if (lane == h) {
-          ob[(g * kGroup + h) * kHeadDim + d] = __float2bfloat16_rn(ac / dn);
-          if (d == 0) lo[g * kGroup + h] = mx + log2f(dn);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          lv[k].x = __shfl_sync(0xffffffffu, lv[k].x, lse_src);
+          lv[k].y = __shfl_sync(0xffffffffu, lv[k].y, lse_src);
+          lv[k].z = __shfl_sync(0xffffffffu, lv[k].z, lse_src);
+          lv[k].w = __shfl_sync(0xffffffffu, lv[k].w, lse_src);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float l4[4] = {lv[k].x, lv[k].y, lv[k].z, lv[k].w};
+          const float o4[4] = {ov[k].x, ov[k].y, ov[k].z, ov[k].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float mn = fmaxf(m[i], l4[i]);
+            if (mn == -INFINITY) continue;  // nothing added yet and a padding split
+            const float sc = ex2(m[i] - mn), wt = ex2(l4[i] - mn);
+            den[i] = den[i] * sc + wt;
+            acc[i] = acc[i] * sc + wt * o4[i];
+            m[i] = mn;
+          }
+        }
+      }
+      // fold the rows that share a warp (lanes col, col + cols, ...)
+      for (int o = cols; o < 32; o <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, m[i], o);
+          const float d2 = __shfl_xor_sync(0xffffffffu, den[i], o);
+          const float a2 = __shfl_xor_sync(0xffffffffu, acc[i], o);
+          const float mn = fmaxf(m[i], m2);
+          if (mn == -INFINITY) continue;
+          const float s1 = ex2(m[i] - mn), s2 = ex2(m2 - mn);
+          den[i] = den[i] * s1 + d2 * s2;
+          acc[i] = acc[i] * s1 + a2 * s2;
+          m[i] = mn;
+        }
+      }
+      // then the row groups, through shared memory
+      __syncthreads();  // the previous item's readers are done with xw
+      if (leader) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          xw[group * cols + col][i] = m[i];
+          xw[group * cols + col][4 + i] = den[i];
+          xw[group * cols + col][8 + i] = acc[i];
+        }
+      }
+      __syncthreads();
+      if (tid < cols) {
+        for (int gi = 1; gi < ngroups; ++gi) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float m2 = xw[gi * cols + col][i];
+            const float mn = fmaxf(m[i], m2);
+            if (mn == -INFINITY) continue;
+            const float s1 = ex2(m[i] - mn), s2 = ex2(m2 - mn);
+            den[i] = den[i] * s1 + xw[gi * cols + col][4 + i] * s2;
+            acc[i] = acc[i] * s1 + xw[gi * cols + col][8 + i] * s2;
+            m[i] = mn;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int h = g * kGroup + hq * 4 + i;
+          ob[h * kHeadDim + d] = __float2bfloat16_rn(acc[i] / den[i]);
+          if (d == 0) lo[h] = m[i] + log2f(den[i]);
         }
       }
     }
@@ -248,7 +288,8 @@ __global__ void gqa_validate_kernel(const int* __restrict__ indptr, const int* _
 // ------------------------------------------------------------------- launch
 template <int NG>
 static cudaError_t launch_merge_impl(const MergeParams& p, cudaStream_t stream) {
-  const int boundaries = p.num_decode_ctas > 1 ? p.num_decode_ctas - 1 : 1;
+  const int ctas = p.plan.tier1_ctas + p.plan.tier2_ctas;
+  const int boundaries = ctas > 1 ? ctas - 1 : 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(boundaries * kMergeCtasPerBoundary);
   cfg.blockDim = dim3(kMergeThreads);

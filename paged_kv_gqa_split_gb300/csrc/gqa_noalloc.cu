@@ -17,12 +17,14 @@
 #include <cstdint>
 #include <mutex>
 
+#include "gqa_kernels.h"
 #include "gqa_paged_decode.h"
 
 namespace {
 
 // Scratch for the fp32 split partials (two slots per decode CTA). Its size is
-// GQA_NOALLOC_SCRATCH_BYTES; configurations that would need more are refused.
+// GQA_NOALLOC_SCRATCH_BYTES; a plan that would need more runs with fewer
+// tier-2 CTAs.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GQA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
@@ -56,13 +58,10 @@ extern "C" int gqa_paged_decode_noalloc(const void* q, const void* k_cache, cons
                                         void* out, float* lse, int batch, struct CUstream_st* stream) {
   if (batch == 0) return GQA_OK;
   if (batch < 0) return GQA_ERR_INVALID_ARGUMENT;
-  // Scratch needed by the current device and tuning; refuse instead of overrunning it.
-  const size_t need = gqa_paged_decode_ws_size(batch, 0);
-  if (need == 0) return GQA_ERR_LAUNCH;
-  if (need > static_cast<size_t>(GQA_NOALLOC_SCRATCH_BYTES)) return GQA_ERR_WORKSPACE;
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc != GQA_OK) return rc;
-  return gqa_paged_decode_ws(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream, scratch,
-                             static_cast<size_t>(GQA_NOALLOC_SCRATCH_BYTES));
+  // the plan is shrunk to the scratch (fewer tier-2 CTAs) rather than overrunning it
+  return gqa::decode_in_scratch(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream,
+                                scratch, static_cast<size_t>(GQA_NOALLOC_SCRATCH_BYTES));
 }

@@ -103,7 +103,8 @@ def test_edge_cases_default(name):
     check(w, out, lse)
 
 
-# (num_ctas, min_units_per_cta, heads_per_cta, tile, stages, gather): gather 0 = cp.async, 1 = TMA bulk
+# (num_ctas, min_units_per_cta, heads_per_cta, tile, stages, gather[, fused_merge_max_splits, tier2_ctas,
+#  tier2_permille, tier2_min_units]): gather 0 = cp.async, 1 = TMA bulk; tier2_ctas -1 = one tier
 VARIANTS = {
     "lsu_ng4_s3": (0, 0, 4, 16, 3, 0),
     "lsu_ng4_s4": (0, 0, 4, 16, 4, 0),
@@ -123,6 +124,13 @@ VARIANTS = {
     "tma_ng4_t32": (0, 0, 4, 32, 3, 1),
     "tma_ng1_t16": (0, 0, 1, 16, 4, 1),
     "tma_small_units": (0, 16, 4, 32, 3, 1),
+    # tier 2 takes units only once the tier-1 CTAs are full, hence few tier-1 CTAs here
+    "lsu_one_tier": (0, 0, 4, 16, 2, 0, 0, -1),
+    "lsu_tier2_half_fine": (40, 8, 4, 16, 2, 0, 0, 0, 500, 16),
+    "lsu_ng1_tier2": (40, 8, 1, 16, 2, 0, 0, 0, 300, 8),
+    "lsu_few_ctas_tier2": (7, 0, 4, 16, 2, 0, 0, 13, 400, 4),
+    "lsu_tier2_unfused": (40, 8, 4, 16, 2, 0, -1, 0, 600, 8),
+    "tma_tier2": (40, 8, 4, 16, 5, 1, 0, 0, 300, 16),
 }
 
 
@@ -137,13 +145,13 @@ def test_kernel_variants(tuning, variant, case):
 
 @pytest.mark.parametrize("ng,stages", [(4, 3), (4, 2), (1, 2)])
 @pytest.mark.parametrize("fuse", [0, -1, 64, 2, 5])
-@pytest.mark.parametrize("num_ctas,min_units", [(152, 16), (40, 16), (300, 1), (3, 1), (90, 1)])
+@pytest.mark.parametrize("num_ctas,min_units", [(152, 16), (40, 16), (300, 1), (3, 1), (90, 1), (1200, 1)])
 def test_split_and_merge_paths(tuning, num_ctas, min_units, fuse, ng, stages):
     """One long and several short sequences cut into 2 to ~300 pieces, with the merge
     done in the decode kernel (up to `fuse` pieces; 0 = default 16, -1 = never; the
     warp stages 4 partials per round trip, so 5 and 16 take several batches) or by
-    the merge kernel (warp path up to 16 pieces, CTA path up to 64, lanes-over-splits
-    path above)."""
+    the merge kernel (warp path up to 16 pieces; above that the block path, whose
+    block width runs from 32 dims at 17 pieces down to 1 dim past 256 pieces)."""
     tuning(num_ctas, min_units, ng, 16, stages, 0, fuse)
     w = wl.make_workload([5000, 3, 17, 0, 900, 1, 64], seed=21, pool_factor=1.1)
     out, lse = gpu_run(w)
@@ -152,7 +160,8 @@ def test_split_and_merge_paths(tuning, num_ctas, min_units, fuse, ng, stages):
 
 @pytest.mark.parametrize("variant", [(200, 8, 4, 16, 3, 0), (600, 8, 1, 16, 3, 0), (120, 8, 2, 16, 5, 0),
                                      (90, 8, 4, 32, 3, 1), (300, 8, 4, 16, 5, 1), (200, 8, 4, 16, 3, 0, -1),
-                                     (600, 8, 1, 16, 3, 0, 64), (300, 8, 4, 16, 5, 1, -1)])
+                                     (600, 8, 1, 16, 3, 0, 64), (300, 8, 4, 16, 5, 1, -1),
+                                     (100, 8, 4, 16, 2, 0, 0, 700, 500, 4), (100, 8, 4, 16, 2, 0, -1, 700, 500, 4)])
 def test_token_count_exact_with_uniform_scores(tuning, variant):
     """q = 0 makes every score 0: lse must be log2(n) to fp32 precision, which a
     dropped or doubled token would break (1.44/n >> 2e-5 for n <= 9000), and O
