@@ -220,3 +220,112 @@ def make_pattern_workload() -> Workload:
     k = pattern((10, PAGE_SIZE, NUM_KV_HEADS, HEAD_DIM), 3, 2)
     v = pattern((10, PAGE_SIZE, NUM_KV_HEADS, HEAD_DIM), 11, 4)
     return Workload("pattern", q, k, v, indptr, indices, DEFAULT_SM_SCALE, lens)
+
+
+# ------------------------------------------------------------------ sparse
+@dataclass
+class SparseWorkload:
+    """Inputs of a selected-token (sparse) paged decode, all on the CPU.
+
+    Shapes follow the sparse split-K GQA path of the sigit.si vLLM "qsa.py" page
+    (``qsa_sparse_paged_attention``): q [rows, 32, 128] bf16; k_cache, v_cache
+    [num_blocks, page_size, 4, 128] bf16; logical_indices [rows, topk] int32
+    (logical token positions of the row's request, -1 = no selection);
+    block_table [num_requests, width] int32 (-1 = no page); token_to_req [rows]
+    int32.
+    """
+
+    name: str
+    q: torch.Tensor
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    logical_indices: torch.Tensor
+    block_table: torch.Tensor
+    token_to_req: torch.Tensor
+    sm_scale: float
+    lens: List[int] = field(default_factory=list)
+
+    @property
+    def rows(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def topk(self) -> int:
+        return int(self.logical_indices.shape[1])
+
+    @property
+    def page_size(self) -> int:
+        return int(self.k_cache.shape[1])
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.k_cache.shape[0])
+
+    def to(self, device, non_blocking: bool = False) -> "SparseWorkload":
+        t = lambda x: x.to(device, non_blocking=non_blocking)  # noqa: E731
+        return SparseWorkload(self.name, t(self.q), t(self.k_cache), t(self.v_cache), t(self.logical_indices),
+                              t(self.block_table), t(self.token_to_req), self.sm_scale, list(self.lens))
+
+
+def make_sparse_workload(
+    lens: Sequence[int],
+    topk: int,
+    page_size: int,
+    seed: int,
+    *,
+    pool_factor: float = 1.25,
+    q_std: float = 1.0,
+    name: str = "sparse",
+    sm_scale: float = DEFAULT_SM_SCALE,
+) -> SparseWorkload:
+    """One query row per request, request r holding lens[r] cached tokens.
+
+    Draw order (one ``torch.Generator`` seeded with ``seed``): the physical
+    block permutation, then each row's selection, then q, k, v. Request r
+    owns ceil(lens[r] / page_size) blocks, taken in order from a seeded
+    random permutation of ``ceil(pool_factor * total blocks)`` blocks; the
+    rest of its block-table row is -1. Row r selects min(topk, lens[r])
+    distinct positions below lens[r] (a seeded random subset, in increasing
+    order, as a top-k selection would give) and pads with -1.
+    """
+    g = torch.Generator().manual_seed(seed)
+    lens = [int(x) for x in lens]
+    rows = len(lens)
+    if rows == 0 or topk <= 0 or page_size <= 0:
+        raise ValueError("need rows, a positive topk and a positive page size")
+    nblk = [(n + page_size - 1) // page_size for n in lens]
+    width = max(1, max(nblk))
+    total_blocks = sum(nblk)
+    num_blocks = max(1, int(math.ceil(pool_factor * total_blocks)))
+    perm = torch.randperm(num_blocks, generator=g)
+    table = torch.full((rows, width), -1, dtype=torch.int32)
+    off = 0
+    for r, n in enumerate(nblk):
+        table[r, :n] = perm[off:off + n].to(torch.int32)
+        off += n
+    idx = torch.full((rows, topk), -1, dtype=torch.int32)
+    for r, n in enumerate(lens):
+        k = min(topk, n)
+        if k > 0:
+            sel = torch.randperm(n, generator=g)[:k].sort().values
+            idx[r, :k] = sel.to(torch.int32)
+    q = _randn_bf16((rows, NUM_QO_HEADS, HEAD_DIM), g, q_std)
+    kc = _randn_bf16((num_blocks, page_size, NUM_KV_HEADS, HEAD_DIM), g)
+    vc = _randn_bf16((num_blocks, page_size, NUM_KV_HEADS, HEAD_DIM), g)
+    return SparseWorkload(name, q, kc, vc, idx, table.contiguous(), torch.arange(rows, dtype=torch.int32),
+                          float(sm_scale), lens)
+
+
+# Selected-token decode workload timed by bench.py: the pages fix no sizes for
+# this path, so it takes decode-sized rows of the same head shape: 128
+# requests with 2k-8k cached tokens in blocks of 64, 2048 selected positions
+# per row (512 MB of K/V rows read per call).
+SPARSE_CONFIG = dict(rows=128, topk=2048, page_size=64, len_lo=2048, len_hi=8192, seed=5, pool_factor=1.25)
+
+
+def make_sparse_config() -> SparseWorkload:
+    c = SPARSE_CONFIG
+    g = torch.Generator().manual_seed(c["seed"])
+    lens = torch.randint(c["len_lo"], c["len_hi"] + 1, (c["rows"],), generator=g).tolist()
+    return make_sparse_workload(lens, c["topk"], c["page_size"], c["seed"] + 1000, pool_factor=c["pool_factor"],
+                                name="sparse")
