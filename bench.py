@@ -306,20 +306,52 @@ def bench_append(device, steps, warmup, step_tokens, peak):
     return res
 
 
+# ---------------------------------------------------- selected-token decode
+def bench_sparse(device, steps, warmup, peak):
+    """Selected-token decode of the sparse workload (128 rows x 2048 selected
+    positions, blocks of 64): µs per call and GB/s of the K/V rows of the used
+    columns (2048 B each) plus 16,512 B of q, O and LSE per row. Same timing
+    method as the decode line."""
+    w = wl.make_sparse_config()
+    # every non-negative position of this generator is below its request's
+    # length and inside its mapped blocks, so it is a used column
+    used = int((w.logical_indices >= 0).sum())
+    g = w.to(device)
+    out = torch.empty_like(g.q)
+    lse = torch.empty((w.rows, 32), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    flush = L2Flush(device)
+
+    def call():
+        _lib.sparse_run(g.q, g.k_cache, g.v_cache, g.logical_indices, g.block_table, g.token_to_req, w.sm_scale,
+                        out=out, lse=lse, stream=stream)
+    for _ in range(warmup):
+        call()
+    ms = statistics.median(time_steps(call, steps, stream, flush))
+    b = 2048 * used + 16512 * w.rows
+    res = {"rows": w.rows, "topk": w.topk, "page_size": w.page_size, "used_columns": used,
+           "us_per_batch": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9, "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
+           "counted_bytes": b, "launches_per_call": 3}
+    del g, out, lse, flush
+    return res
+
+
 # -------------------------------------------------------------- CPU oracle
 def oracle_sample(w, budget_s: float):
     """Run the float64 oracle over the workload's sequences in order until about
-    budget_s seconds have passed (at least one non-empty sequence)."""
+    budget_s seconds have passed (at least one non-empty sequence). Returns the
+    sequences done, the seconds taken and the oracle's (O, lse) rows for them."""
     from oracle import gqa_paged_decode_oracle
-    done, t0 = [], time.perf_counter()
+    done, outs, t0 = [], [], time.perf_counter()
     order = [b for b in range(w.batch) if w.lens[b] > 0] or [0]
     for b in order:
-        gqa_paged_decode_oracle(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices, w.sm_scale, seqs=[b])
+        o, l = gqa_paged_decode_oracle(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices, w.sm_scale, seqs=[b])
         done.append(b)
+        outs.append((o[b], l[b]))
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return [w.lens[b] for b in done], dt
+    return done, dt, outs
 
 
 def blas_threads():
@@ -332,13 +364,32 @@ def blas_threads():
         return 1
 
 
-def cpu_baseline(w, budget_s: float = 10.0):
-    lens, dt = oracle_sample(w, budget_s)
+def cpu_baseline(w, out=None, lse=None, budget_s: float = 10.0):
+    """The oracle timed on the host on a bounded sample of the workload. With
+    the GPU's (out, lse) of the timed run, the same sampled sequences also give
+    the run's parity figures."""
+    import numpy as np
+    seqs, dt, outs = oracle_sample(w, budget_s)
+    lens = [w.lens[b] for b in seqs]
     gbs = counted_bytes(lens) / dt / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+    base = {"value": gbs, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
             "sample": f"{len(lens)} of {w.batch} sequences ({sum(lens)} tokens) of the {w.name} workload, "
                       f"float64 NumPy oracle, {dt:.2f} s",
             "host_cores_available": len(os.sched_getaffinity(0))}
+    parity = None
+    if out is not None:
+        o = out.float().cpu().double().numpy()[seqs]
+        l = lse.cpu().double().numpy()[seqs]
+        o_ref = np.stack([x[0] for x in outs])
+        l_ref = np.stack([x[1] for x in outs])
+        fin = np.isfinite(l_ref)
+        o_err = float(np.abs(o - o_ref).max())
+        l_err = float(np.abs(l[fin] - l_ref[fin]).max()) if fin.any() else 0.0
+        ok = bool(np.all(np.abs(o - o_ref) <= 2e-2 + 2e-2 * np.abs(o_ref)) and l_err <= 1e-3 and
+                  np.array_equal(np.isneginf(l), np.isneginf(l_ref)))
+        parity = {"sequences": len(seqs), "tokens": sum(lens), "max_abs_dO": o_err, "max_abs_dlse": l_err,
+                  "within_tolerance": ok}
+    return base, parity
 
 
 # ------------------------------------------------------------- variant sweep
@@ -434,10 +485,8 @@ def main():
     value = world * cb / (step_ms_max * 1e-3) / 1e9
     achieved = cb / (dec_ms * 1e-3) / 1e9
 
-    # parity spot check on this very run (sampled sequences against the oracle)
-    parity = None
-    if rank == 0 and not args.no_cpu_baseline:
-        parity = spot_parity(w, r["out"], r["lse"])
+    # the GPU result of the timed run, for the parity check of the CPU-baseline leg
+    run_out, run_lse = r["out"].cpu(), r["lse"].cpu()
     del r
 
     e2e = None
@@ -463,13 +512,14 @@ def main():
             if ww is not w:
                 del ww
 
-    append = None
+    append = sparse = None
     if not args.no_workloads:
         append = bench_append(device, args.steps, warmup, w.batch, peak)
+        sparse = bench_sparse(device, args.steps, warmup, peak)
 
-    cpu = None
+    cpu, parity = None, None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w)
+        cpu, parity = cpu_baseline(w, run_out, run_lse)
 
     if rank != 0:
         if world > 1:
@@ -508,28 +558,12 @@ def main():
         "parity": parity,
         "workloads": table,
         "kv_append": append,
+        "sparse_decode": sparse,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
-
-
-def spot_parity(w, out, lse, n=4):
-    """Max errors of a few sequences of this run against the float64 oracle."""
-    import numpy as np
-    from oracle import gqa_paged_decode_oracle
-    lens = np.array(w.lens)
-    seqs = sorted(set(np.argsort(lens)[-2:].tolist()) | {0, w.batch // 2})[:n]
-    o_ref, l_ref = gqa_paged_decode_oracle(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices, w.sm_scale,
-                                           seqs=seqs)
-    o = out.float().cpu().double().numpy()[seqs]
-    l = lse.cpu().double().numpy()[seqs]
-    fin = np.isfinite(l_ref[seqs])
-    o_err = float(np.abs(o - o_ref[seqs]).max())
-    l_err = float(np.abs(l[fin] - l_ref[seqs][fin]).max()) if fin.any() else 0.0
-    ok = bool(np.all(np.abs(o - o_ref[seqs]) <= 2e-2 + 2e-2 * np.abs(o_ref[seqs])) and l_err <= 1e-3)
-    return {"sequences": seqs, "max_abs_dO": o_err, "max_abs_dlse": l_err, "within_tolerance": ok}
 
 
 def main_reference(args, world, rank, warmup):
@@ -541,7 +575,8 @@ def main_reference(args, world, rank, warmup):
         oracle_sample(w, budget)
     rates, secs, lens_done = [], [], []
     for _ in range(args.steps):
-        lens, dt = oracle_sample(w, budget)
+        seqs, dt, _ = oracle_sample(w, budget)
+        lens = [w.lens[b] for b in seqs]
         rates.append(counted_bytes(lens) / dt / 1e9)
         secs.append(dt)
         lens_done = lens

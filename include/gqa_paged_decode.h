@@ -177,6 +177,47 @@ int64_t gqa_paged_decode_plan(const int32_t* kv_indptr, int batch, int num_ctas,
                               int64_t* pieces, int64_t capacity);
 
 /*
+ * Selected-token (sparse) paged GQA decode: the sparse split-K GQA path of
+ * the sigit.si vLLM "qsa.py" page (qsa_sparse_paged_attention and its
+ * _qsa_sparse_paged_gqa_splitk_kernel), for 32 query heads over 4 KV heads
+ * of dimension 128.
+ *
+ * Query row r (of `rows`) belongs to request req = token_to_req[r] and
+ * selects `topk` logical token positions t = logical_indices[r * topk + c] of
+ * that request. Column c is used when 0 <= req < num_requests, t >= 0,
+ * t / page_size < page_table_width, and the physical page
+ * p = block_table[req * page_table_width + t / page_size] satisfies
+ * 0 <= p < num_cache_blocks; its key and value rows for KV head g are then
+ * k_cache[p][t % page_size][g][:] and v_cache[...]. Other columns (for
+ * example -1 padding) are left out. Per query head h (KV head h / 8):
+ * out[r][h] = softmax over the used columns of sm_scale * q[r][h] . k, times
+ * v, in bf16 (a column listed twice counts twice), and, when lse is not NULL,
+ * lse[r][h] = log2 sum exp(s) in fp32. A row with no used column gives
+ * out = 0 and lse = -inf.
+ *
+ * Layouts (all device memory owned by the caller, contiguous): q, out
+ * [rows][32][128] bf16, 16-byte aligned; k_cache, v_cache
+ * [num_cache_blocks][page_size][4][128] bf16, 16-byte aligned;
+ * logical_indices [rows][topk] int32; block_table
+ * [num_requests][page_table_width] int32; token_to_req [rows] int32; lse
+ * [rows][32] fp32 (8-byte aligned) or NULL. The page fixes sm_scale at
+ * 1/sqrt(128); here it is an argument.
+ *
+ * Asynchronous on `stream`. Needs topk, page_size, num_cache_blocks,
+ * num_requests, page_table_width > 0, num_cache_blocks * page_size and
+ * rows * topk below 2^31; rows == 0 returns 0 without launching. Runs the
+ * 4-KV-heads-per-CTA, 2-stage decode variant whatever the tuning's kernel
+ * choice (the tuning's CTA counts and tiers apply). Uses the library-owned
+ * workspace, which also holds rows * topk resolved slots (4 bytes each).
+ * Returns GQA_OK, GQA_ERR_INVALID_ARGUMENT, GQA_ERR_WORKSPACE,
+ * GQA_ERR_LAUNCH or GQA_ERR_UNSUPPORTED_DEVICE.
+ */
+int gqa_sparse_paged_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* logical_indices,
+                            const int32_t* block_table, const int32_t* token_to_req, float sm_scale, void* out,
+                            float* lse, int rows, int topk, int page_size, int num_cache_blocks, int num_requests,
+                            int page_table_width, struct CUstream_st* stream);
+
+/*
  * Synchronise the current device, then read and clear the sticky device error
  * word: bit 1 / 2 = a pipeline wait gave up after ~2 s (the kernel returned
  * early), bit 4 = bad page id, bit 8 = bad kv_indptr. 0 means no error.

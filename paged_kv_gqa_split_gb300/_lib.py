@@ -44,6 +44,7 @@ _SIGNATURES = {
     "gqa_paged_decode_plan": (ctypes.c_int64, [_vp] + [ctypes.c_int] * 7 + [_vp, ctypes.c_int64]),
     "gqa_paged_kv_append": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int, _vp]),
     "gqa_paged_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_int, _vp]),
+    "gqa_sparse_paged_decode": (ctypes.c_int, [_vp] * 6 + [ctypes.c_float, _vp, _vp] + [ctypes.c_int] * 6 + [_vp]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -272,3 +273,69 @@ def run_checked(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale=None, out=N
     if rc != GQA_OK:
         raise GqaError(rc, "gqa_paged_decode_checked")
     return out, lse, dev_err
+
+
+def gqa_sparse_paged_decode(q, k_cache, v_cache, logical_indices, block_table, token_to_req, sm_scale, out, lse,
+                            rows, topk, page_size, num_cache_blocks, num_requests, page_table_width, stream) -> int:
+    return load().gqa_sparse_paged_decode(q, k_cache, v_cache, logical_indices, block_table, token_to_req, sm_scale,
+                                          out, lse, rows, topk, page_size, num_cache_blocks, num_requests,
+                                          page_table_width, stream)
+
+
+def sparse_run(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, logical_indices: torch.Tensor,
+               block_table: torch.Tensor, token_to_req: torch.Tensor, sm_scale: Optional[float] = None,
+               out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, with_lse: bool = True,
+               stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Selected-token paged GQA decode on the GPU (the shape checks of the qsa.py
+    page's ``qsa_sparse_paged_attention``, for 32 query heads over 4 KV heads of
+    dimension 128). Returns (out [rows, 32, 128] bf16, lse [rows, 32] fp32 or None)."""
+    tensors = {"q": q, "k_cache": k_cache, "v_cache": v_cache, "logical_indices": logical_indices,
+               "block_table": block_table, "token_to_req": token_to_req}
+    for name, t in tensors.items():
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if not t.is_cuda:
+            raise ValueError(f"{name} is on {t.device}: the CUDA library has no CPU path; move inputs to the GPU")
+        if t.device != q.device:
+            raise ValueError(f"all inputs must be on {q.device}; {name} is on {t.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("expected q [rows, 32, 128] and k_cache / v_cache [blocks, page_size, 4, 128]")
+    if logical_indices.dim() != 2 or logical_indices.shape[0] != q.shape[0]:
+        raise ValueError("logical_indices must have one row per query")
+    if token_to_req.shape != (q.shape[0],) or block_table.dim() != 2:
+        raise ValueError("token_to_req must be [rows] and block_table [requests, width]")
+    if not all(k_cache.shape[:3]) or not all(block_table.shape) or logical_indices.shape[1] <= 0:
+        raise ValueError("the cache, the block table and the selection width must be nonempty")
+    if tuple(q.shape[1:]) != (NUM_QO_HEADS, HEAD_DIM) or tuple(k_cache.shape[2:]) != (NUM_KV_HEADS, HEAD_DIM):
+        raise ValueError("expected 32 query heads over 4 KV heads of dimension 128")
+    for name in ("q", "k_cache", "v_cache"):
+        if tensors[name].dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16")
+    for name in ("logical_indices", "block_table", "token_to_req"):
+        if tensors[name].dtype != torch.int32:
+            raise ValueError(f"{name} must be int32")
+    rows, topk = int(logical_indices.shape[0]), int(logical_indices.shape[1])
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    if out is None:
+        out = torch.empty_like(q)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() or out.device != q.device:
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q on q's device")
+    if lse is None and with_lse:
+        lse = torch.empty((rows, NUM_QO_HEADS), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.shape != (rows, NUM_QO_HEADS) or lse.dtype != torch.float32 or
+                            not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 tensor [rows, 32]")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        rc = gqa_sparse_paged_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), logical_indices.data_ptr(),
+                                     block_table.data_ptr(), token_to_req.data_ptr(), float(sm_scale),
+                                     out.data_ptr(), lse.data_ptr() if lse is not None else None, rows, topk,
+                                     int(k_cache.shape[1]), int(k_cache.shape[0]), int(block_table.shape[0]),
+                                     int(block_table.shape[1]), stream.cuda_stream)
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_sparse_paged_decode")
+    return out, lse

@@ -6,6 +6,7 @@
 // asynchronous on the caller's stream.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -141,15 +142,52 @@ int check_args(const void* q, const void* k, const void* v, const int32_t* indpt
   return GQA_OK;
 }
 
+// Selected-token batch: `rows` query rows of `topk` columns each, resolved
+// through a block table (the decode then runs in sparse mode).
+struct SparseJob {
+  const int32_t* logical_indices;
+  const int32_t* block_table;
+  const int32_t* token_to_req;
+  int topk, page_size, page_table_width, num_requests, num_cache_blocks;
+};
+
+// Grows the library-owned workspace of the current device to `need` bytes
+// (caller holds g_mu). Returns a GQA_* code.
+int library_workspace(DeviceState* st, size_t need, void** ws) {
+  if (st->ws_bytes < need) {
+    if (st->ws != nullptr) {
+      // calls already queued may still read the old buffer
+      if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_LAUNCH;
+      cudaFree(st->ws);
+      st->ws = nullptr;
+      st->ws_bytes = 0;
+    }
+    if (cudaMalloc(&st->ws, need) != cudaSuccess) {
+      cudaGetLastError();
+      st->ws = nullptr;
+      return GQA_ERR_WORKSPACE;
+    }
+    st->ws_bytes = need;
+  }
+  *ws = st->ws;
+  return GQA_OK;
+}
+
 // fit_ws: a caller workspace too small for the tuned plan makes the plan use
-// fewer tier-2 CTAs (down to none) instead of failing.
+// fewer tier-2 CTAs (down to none) instead of failing. sj: selected-token mode
+// (indptr and indices unused; the library-owned workspace also holds the
+// resolved slots).
 int run(const void* q, const void* k, const void* v, const int32_t* indptr, const int32_t* indices, float sm_scale,
         void* out, float* lse, int batch, cudaStream_t stream, void* user_ws, size_t user_ws_bytes, bool checked,
-        int num_pages, int* dev_err, bool fit_ws = false) {
-  int rc = check_args(q, k, v, indptr, indices, sm_scale, out, lse, batch);
-  if (rc != GQA_OK) return rc;
+        int num_pages, int* dev_err, bool fit_ws = false, const SparseJob* sj = nullptr) {
+  if (sj == nullptr) {
+    const int rc0 = check_args(q, k, v, indptr, indices, sm_scale, out, lse, batch);
+    if (rc0 != GQA_OK) return rc0;
+  }
+  int rc = GQA_OK;
   if (batch == 0) return GQA_OK;
   if (checked && (num_pages <= 0 || dev_err == nullptr || !aligned(dev_err, 4))) return GQA_ERR_INVALID_ARGUMENT;
+  const int64_t sparse_total = sj != nullptr ? static_cast<int64_t>(batch) * sj->topk : 0;
 
   int dev = 0;
   DeviceState* st = nullptr;
@@ -162,6 +200,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
     rc = current_device(&dev, &st);
     if (rc != GQA_OK) return rc;
     tune = g_tune;
+    if (sj != nullptr) tune.kernel = KernelChoice{gqa::kGatherLsu, 4, 16, 2};  // the one sparse variant
     ev0 = g_ev_start;
     ev1 = g_ev_stop;
     cfg = plan_config(*st, tune);
@@ -174,27 +213,14 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
         cfg.tier2_ctas = cfg.tier2_ctas > drop ? cfg.tier2_ctas - drop : 0;
       }
     }
-    const size_t need = workspace_bytes(cfg.tier1_ctas + cfg.tier2_ctas, ng);
+    const size_t need = workspace_bytes(cfg.tier1_ctas + cfg.tier2_ctas, ng) +
+                        round256(static_cast<size_t>(sparse_total) * sizeof(int32_t));
     if (user_ws != nullptr) {
       if (user_ws_bytes < need || !aligned(user_ws, 256)) return GQA_ERR_WORKSPACE;
       ws = user_ws;
     } else {
-      if (st->ws_bytes < need) {
-        if (st->ws != nullptr) {
-          // calls already queued may still read the old buffer
-          if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_LAUNCH;
-          cudaFree(st->ws);
-          st->ws = nullptr;
-          st->ws_bytes = 0;
-        }
-        if (cudaMalloc(&st->ws, need) != cudaSuccess) {
-          cudaGetLastError();
-          st->ws = nullptr;
-          return GQA_ERR_WORKSPACE;
-        }
-        st->ws_bytes = need;
-      }
-      ws = st->ws;
+      rc = library_workspace(st, need, &ws);
+      if (rc != GQA_OK) return rc;
     }
   }
 
@@ -208,6 +234,16 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   int4* split_rec = reinterpret_cast<int4*>(static_cast<char*>(ws) + tickets_off + round256(tickets_bytes(ctas, ng)));
   const unsigned long long epoch = (g_epoch.fetch_add(1) % ((1ull << 40) - 1)) + 1;
 
+  if (sj != nullptr) {  // resolve every selected column to its slot first
+    int32_t* slots = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + workspace_bytes(ctas, ng));
+    if (gqa::launch_sparse_resolve(sj->logical_indices, sj->block_table, sj->token_to_req, slots, batch, sj->topk,
+                                   sj->page_size, sj->page_table_width, sj->num_requests, sj->num_cache_blocks,
+                                   st->sm_count, stream) != cudaSuccess)
+      return GQA_ERR_LAUNCH;
+    indices = slots;
+    indptr = nullptr;
+  }
+
   if (checked) {
     if (cudaMemsetAsync(dev_err, 0, sizeof(int), stream) != cudaSuccess) return GQA_ERR_LAUNCH;
     if (gqa::launch_validate(indptr, indices, batch, num_pages, dev_err, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
@@ -216,7 +252,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   int* err_word = nullptr;
   if (gqa::device_error_word(&err_word) != cudaSuccess) return GQA_ERR_LAUNCH;
 
-  gqa::DecodeParams dp;
+  gqa::DecodeParams dp{};
   dp.q = q;
   dp.k_cache = k;
   dp.v_cache = v;
@@ -233,16 +269,20 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   dp.split_rec = split_rec;
   dp.fuse_max_splits = tune.fuse_max_splits;
   dp.batch = batch;
+  dp.sparse_topk = sj != nullptr ? sj->topk : 0;
+  dp.sparse_total = static_cast<int>(sparse_total);
   dp.plan = cfg;
   dp.scale_log2 = sm_scale * kLog2e;
   dp.num_pages_check = checked ? num_pages : 0;
 
   const bool profile = ev0 != nullptr && ev1 != nullptr;
   if (profile && cudaEventRecord(ev0, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
-  if (gqa::launch_decode(tune.kernel, dp, ctas, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
+  const cudaError_t le = sj != nullptr ? gqa::launch_decode_lsu_sparse(dp, ctas, stream)
+                                       : gqa::launch_decode(tune.kernel, dp, ctas, stream);
+  if (le != cudaSuccess) return GQA_ERR_LAUNCH;
   if (profile && cudaEventRecord(ev1, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
 
-  gqa::MergeParams mp;
+  gqa::MergeParams mp{};
   mp.kv_indptr = indptr;
   mp.part_o = part_o;
   mp.part_lse = part_lse;
@@ -250,6 +290,8 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   mp.lse = lse;
   mp.skip_if_set = checked ? dev_err : nullptr;
   mp.batch = batch;
+  mp.sparse_topk = dp.sparse_topk;
+  mp.sparse_total = dp.sparse_total;
   mp.plan = cfg;
   mp.split_rec = split_rec;
   mp.epoch = epoch;
@@ -470,6 +512,31 @@ int64_t gqa_paged_decode_plan(const int32_t* kv_indptr, int batch, int num_ctas,
     }
   }
   return n;
+}
+
+int gqa_sparse_paged_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* logical_indices,
+                            const int32_t* block_table, const int32_t* token_to_req, float sm_scale, void* out,
+                            float* lse, int rows, int topk, int page_size, int num_cache_blocks, int num_requests,
+                            int page_table_width, struct CUstream_st* stream) {
+  if (rows < 0) return GQA_ERR_INVALID_ARGUMENT;
+  if (rows == 0) return GQA_OK;
+  if (topk <= 0 || page_size <= 0 || num_cache_blocks <= 0 || num_requests <= 0 || page_table_width <= 0)
+    return GQA_ERR_INVALID_ARGUMENT;
+  if (static_cast<int64_t>(num_cache_blocks) * page_size > INT32_MAX) return GQA_ERR_INVALID_ARGUMENT;
+  if (static_cast<int64_t>(rows) * topk > INT32_MAX) return GQA_ERR_INVALID_ARGUMENT;
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || out == nullptr || logical_indices == nullptr ||
+      block_table == nullptr || token_to_req == nullptr)
+    return GQA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(sm_scale)) return GQA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    return GQA_ERR_INVALID_ARGUMENT;
+  if ((lse != nullptr && !aligned(lse, 8)) || !aligned(logical_indices, 4) || !aligned(block_table, 4) ||
+      !aligned(token_to_req, 4))
+    return GQA_ERR_INVALID_ARGUMENT;
+  const SparseJob sj{logical_indices, block_table, token_to_req, topk, page_size, page_table_width, num_requests,
+                     num_cache_blocks};
+  return run(q, k_cache, v_cache, nullptr, nullptr, sm_scale, out, lse, rows, stream, nullptr, 0, false, 0, nullptr,
+             false, &sj);
 }
 
 int gqa_paged_decode_device_error(int* flags) {

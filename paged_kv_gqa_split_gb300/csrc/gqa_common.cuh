@@ -89,8 +89,9 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[16], const __nv_bflo
 
 // One 16-token sub-tile. k_addr / v_addr: this lane's ldmatrix row address for
 // dims 0..15 of the sub-tile's K and V rows (row pitch `pitch`, dims contiguous).
-// Tokens at index >= valid are masked out (their rows must hold finite values).
-__device__ __forceinline__ void attend_subtile(HeadState& st, uint32_t k_addr, uint32_t v_addr, int valid,
+// Tokens whose bit in `valid` is clear are masked out (their rows must hold
+// finite values); a sub-tile may have none valid.
+__device__ __forceinline__ void attend_subtile(HeadState& st, uint32_t k_addr, uint32_t v_addr, unsigned valid,
                                                float scale_log2, int lane) {
   const int r = lane >> 2;
   float s[4] = {0.f, 0.f, 0.f, 0.f};
@@ -100,10 +101,11 @@ __device__ __forceinline__ void attend_subtile(HeadState& st, uint32_t k_addr, u
     ldsm_x4(k_addr + kk * 32, a0, a1, a2, a3);
     mma_bf16_16816(s, a0, a1, a2, a3, st.qf[2 * kk], st.qf[2 * kk + 1]);
   }
-  s[0] = r < valid ? s[0] * scale_log2 : -INFINITY;
-  s[1] = r < valid ? s[1] * scale_log2 : -INFINITY;
-  s[2] = r + 8 < valid ? s[2] * scale_log2 : -INFINITY;
-  s[3] = r + 8 < valid ? s[3] * scale_log2 : -INFINITY;
+  const bool v_lo = (valid >> r) & 1u, v_hi = (valid >> (r + 8)) & 1u;
+  s[0] = v_lo ? s[0] * scale_log2 : -INFINITY;
+  s[1] = v_lo ? s[1] * scale_log2 : -INFINITY;
+  s[2] = v_hi ? s[2] * scale_log2 : -INFINITY;
+  s[3] = v_hi ? s[3] * scale_log2 : -INFINITY;
   float mx0 = fmaxf(s[0], s[2]);
   float mx1 = fmaxf(s[1], s[3]);
 #pragma unroll
@@ -113,12 +115,16 @@ __device__ __forceinline__ void attend_subtile(HeadState& st, uint32_t k_addr, u
   }
   const float mn0 = fmaxf(st.m0, mx0);
   const float mn1 = fmaxf(st.m1, mx1);
-  const float a0 = ex2(st.m0 - mn0);
-  const float a1 = ex2(st.m1 - mn1);
+  // while no valid token has been seen the max is -inf: shift by 0 instead,
+  // so that the factors are 2^-inf = 0 rather than 2^(-inf - -inf) = NaN
+  const float sh0 = mn0 == -INFINITY ? 0.f : mn0;
+  const float sh1 = mn1 == -INFINITY ? 0.f : mn1;
+  const float a0 = ex2(st.m0 - sh0);
+  const float a1 = ex2(st.m1 - sh1);
   st.m0 = mn0;
   st.m1 = mn1;
-  const float p0 = ex2(s[0] - mn0), p1 = ex2(s[1] - mn1);  // token r
-  const float p2 = ex2(s[2] - mn0), p3 = ex2(s[3] - mn1);  // token r + 8
+  const float p0 = ex2(s[0] - sh0), p1 = ex2(s[1] - sh1);  // token r
+  const float p2 = ex2(s[2] - sh0), p3 = ex2(s[3] - sh1);  // token r + 8
   // the running sum keeps fp32 probabilities; only the P.V operand is bf16
   st.l0 = st.l0 * a0 + (p0 + p2);
   st.l1 = st.l1 * a1 + (p1 + p3);
@@ -196,8 +202,9 @@ __device__ __forceinline__ void merge_split_warp(const float* part_o, const floa
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
       const float mn = fmaxf(m[h], l8[h]);
-      sc[h] = ex2(m[h] - mn);  // 0 while nothing has been added (m = -inf)
-      wt[h] = ex2(l8[h] - mn);
+      const float sh = mn == -INFINITY ? 0.f : mn;  // all -inf so far: no NaN from -inf - -inf
+      sc[h] = ex2(m[h] - sh);  // 0 while nothing has been added (m = -inf)
+      wt[h] = ex2(l8[h] - sh);
       den[h] = den[h] * sc[h] + wt[h];
       m[h] = mn;
     }
@@ -211,11 +218,11 @@ __device__ __forceinline__ void merge_split_warp(const float* part_o, const floa
   __nv_bfloat16* ob = out + (b * kQoHeads + h0) * kHeadDim;
 #pragma unroll
   for (int h = 0; h < 8; ++h) {
-    const float inv = 1.f / den[h];
+    const float inv = den[h] > 0.f ? 1.f / den[h] : 0.f;  // no valid token in any piece: O = 0
 #pragma unroll
     for (int j = 0; j < 4; ++j) ob[h * kHeadDim + lane + 32 * j] = __float2bfloat16_rn(acc[j][h] * inv);
   }
-  if (lane < 8) {
+  if (lane < 8 && lse != nullptr) {
     float mm = m[0], dd = den[0];
 #pragma unroll
     for (int h = 1; h < 8; ++h) {
@@ -270,8 +277,9 @@ __device__ __forceinline__ void merge_split_warp_staged(const float* part_o, con
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
         const float mn = fmaxf(m[h], l8[h]);
-        sc[h] = ex2(m[h] - mn);  // 0 while nothing has been added (m = -inf)
-        wt[h] = ex2(l8[h] - mn);
+        const float sh = mn == -INFINITY ? 0.f : mn;  // all -inf so far: no NaN from -inf - -inf
+        sc[h] = ex2(m[h] - sh);  // 0 while nothing has been added (m = -inf)
+        wt[h] = ex2(l8[h] - sh);
         den[h] = den[h] * sc[h] + wt[h];
         m[h] = mn;
       }
@@ -289,11 +297,11 @@ __device__ __forceinline__ void merge_split_warp_staged(const float* part_o, con
   __nv_bfloat16* ob = out + (b * kQoHeads + h0) * kHeadDim;
 #pragma unroll
   for (int h = 0; h < 8; ++h) {
-    const float inv = 1.f / den[h];
+    const float inv = den[h] > 0.f ? 1.f / den[h] : 0.f;  // no valid token in any piece: O = 0
 #pragma unroll
     for (int j = 0; j < 4; ++j) ob[h * kHeadDim + lane + 32 * j] = __float2bfloat16_rn(acc[j][h] * inv);
   }
-  if (lane < 8) {
+  if (lane < 8 && lse != nullptr) {
     float mm = m[0], dd = den[0];
 #pragma unroll
     for (int h = 1; h < 8; ++h) {
@@ -323,10 +331,11 @@ __device__ __forceinline__ bool finish_piece(const HeadState& st, bool final_pie
     lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
     lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
   }
-  const float i0 = 1.f / lt0;
-  const float i1 = 1.f / lt1;
-  const float lse0 = st.m0 + log2f(lt0);
-  const float lse1 = st.m1 + log2f(lt1);
+  // a piece whose tokens were all masked out has l = 0: O = 0, LSE = -inf
+  const float i0 = lt0 > 0.f ? 1.f / lt0 : 0.f;
+  const float i1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
+  const float lse0 = lt0 > 0.f ? st.m0 + log2f(lt0) : -INFINITY;
+  const float lse1 = lt1 > 0.f ? st.m1 + log2f(lt1) : -INFINITY;
   if (final_piece) {
     __nv_bfloat16* ob = out + (b * kQoHeads + h0) * kHeadDim;
 #pragma unroll
@@ -337,7 +346,7 @@ __device__ __forceinline__ bool finish_piece(const HeadState& st, bool final_pie
       *reinterpret_cast<uint32_t*>(ob + r * kHeadDim + mt * 16 + 2 * c) = x;
       *reinterpret_cast<uint32_t*>(ob + r * kHeadDim + mt * 16 + 8 + 2 * c) = y;
     }
-    if (r == 0) *reinterpret_cast<float2*>(p.lse + b * kQoHeads + h0 + 2 * c) = make_float2(lse0, lse1);
+    if (r == 0 && p.lse != nullptr) *reinterpret_cast<float2*>(p.lse + b * kQoHeads + h0 + 2 * c) = make_float2(lse0, lse1);
     return false;
   }
   float* po = p.part_o + (sid * NG + w) * (kHeadDim * kGroup);

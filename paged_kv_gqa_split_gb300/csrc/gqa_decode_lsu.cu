@@ -75,7 +75,10 @@ struct Tile {
   SplitInfo si;
 };
 
-template <int NG, int D>
+// SP: selected-token (sparse) mode. Every row of the batch is one "sequence" of
+// exactly p.sparse_topk columns; kv_indices holds their resolved slots, and a
+// slot of -1 (an invalid column) is masked out of the softmax.
+template <int NG, int D, bool SP>
 __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const DecodeParams p) {
   using C = LsuCfg<NG, D>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -94,7 +97,7 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
   const uint8_t* __restrict__ vc = static_cast<const uint8_t*>(p.v_cache);
   const __nv_bfloat16* __restrict__ qg = static_cast<const __nv_bfloat16*>(p.q);
   const int B = p.batch;
-  const int T = __ldg(p.kv_indptr + B);
+  const int T = SP ? p.sparse_total : __ldg(p.kv_indptr + B);
   SmemPlan* splan = reinterpret_cast<SmemPlan*>(wsm + C::kPlanOff);
   int64_t u0, u1;
   {
@@ -122,22 +125,29 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
     while (walk_ok) {
       if (seg_open && tt < t_stop) {
         if (tt >= p_hi) {  // a new piece starts at tt: find its sequence
-          unsigned m;
-          for (;;) {
-            m = __ballot_sync(0xffffffffu, win <= tt);
-            if (m != 0xffffffffu) break;
-            wb += 31;
-            win = load_indptr_window(p.kv_indptr, B, wb, lane);
+          int seq_lo, seq_hi;
+          if (SP) {  // fixed-width rows
+            pb = tt / p.sparse_topk;
+            seq_lo = pb * p.sparse_topk;
+            seq_hi = seq_lo + p.sparse_topk;
+          } else {
+            unsigned m;
+            for (;;) {
+              m = __ballot_sync(0xffffffffu, win <= tt);
+              if (m != 0xffffffffu) break;
+              wb += 31;
+              win = load_indptr_window(p.kv_indptr, B, wb, lane);
+            }
+            if (m == 0) {  // kv_indptr[wb] > tt: a decreasing table
+              if (lane == 0) atomicOr(p.err, kErrBadIndptr);
+              walk_ok = false;
+              break;
+            }
+            const int k = 31 - __clz(m);
+            pb = wb + k;
+            seq_lo = __shfl_sync(0xffffffffu, win, k);
+            seq_hi = __shfl_sync(0xffffffffu, win, k + 1);
           }
-          if (m == 0) {  // kv_indptr[wb] > tt: a decreasing table
-            if (lane == 0) atomicOr(p.err, kErrBadIndptr);
-            walk_ok = false;
-            break;
-          }
-          const int k = 31 - __clz(m);
-          pb = wb + k;
-          const int seq_lo = __shfl_sync(0xffffffffu, win, k);
-          const int seq_hi = __shfl_sync(0xffffffffu, win, k + 1);
           p_hi = min(seq_hi, t_stop);
           p_flags = F_QLOAD | ((tt == seq_lo && p_hi == seq_hi) ? F_FINAL : 0) |
                     ((static_cast<int64_t>(hg) * T + tt != u0) ? F_SLOT1 : 0);
@@ -171,8 +181,10 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
 #pragma unroll
       for (int c = 0; c < C::kIdsRing / 32; ++c) request_ids(ib + 32 * c + lane);
       cp_async_commit();
-      wb = warp_find_seq(p.kv_indptr, B, tt, lane);
-      if (wb >= 0) win = load_indptr_window(p.kv_indptr, B, wb, lane);
+      if (!SP) {
+        wb = warp_find_seq(p.kv_indptr, B, tt, lane);
+        if (wb >= 0) win = load_indptr_window(p.kv_indptr, B, wb, lane);
+      }
       cp_async_wait<0>();
       __syncwarp();
       if (wb < 0) {
@@ -202,11 +214,21 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
       int flags = tl.flags;
       const int64_t hoff = static_cast<int64_t>(tl.hg * NG + w) * (kHeadDim * 2);
       const int pc = lane & 15;  // 16-byte column of the 256-byte head row
+      // tokens that enter the softmax: the first cnt, less (sparse mode) masked columns
+      unsigned mask = tl.cnt >= 16 ? 0xffffu : ((1u << tl.cnt) - 1u);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int tok = 2 * i + (lane >> 4);
         bool valid = tok < tl.cnt;
         int pg = valid ? ids[(tl.tt + tok) & (C::kIdsRing - 1)] : 0;
+        if (SP) {
+          if (pg < 0) {
+            valid = false;
+            pg = 0;
+          }
+          const unsigned bal = __ballot_sync(0xffffffffu, valid);  // lanes 0-15: token 2i, 16-31: 2i + 1
+          mask = (mask & ~(3u << (2 * i))) | ((bal & 1u) << (2 * i)) | (((bal >> 16) & 1u) << (2 * i + 1));
+        }
         if (valid && p.num_pages_check > 0 && static_cast<unsigned>(pg) >= static_cast<unsigned>(p.num_pages_check)) {
           atomicOr(p.err, kErrBadPage);
           valid = false;
@@ -229,7 +251,7 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
       }
       if (lane == 0) {
         st_shared_v4(sb + C::kHdrOff, tl.b, tl.cnt, flags, tl.hg);
-        st_shared_v4(sb + C::kHdrOff + 16, tl.si.S, tl.si.first_cta, tl.si.first_slot, 0);
+        st_shared_v4(sb + C::kHdrOff + 16, tl.si.S, tl.si.first_cta, tl.si.first_slot, static_cast<int>(mask));
       }
     } else if (more) {
       more = false;
@@ -260,8 +282,8 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
     int hb, cnt, flags, thg;
     ld_shared_v4(sb + C::kHdrOff, hb, cnt, flags, thg);
     SplitInfo si;
-    int unused;
-    ld_shared_v4(sb + C::kHdrOff + 16, si.S, si.first_cta, si.first_slot, unused);
+    int tok_mask;
+    ld_shared_v4(sb + C::kHdrOff + 16, si.S, si.first_cta, si.first_slot, tok_mask);
     if (flags & F_DONE) break;
     const int h0 = (thg * NG + w) * kGroup;
     if (flags & F_QLOAD) {
@@ -274,7 +296,7 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
       }
       st.reset();
     }
-    attend_subtile(st, sb + k_lane, sb + v_lane, cnt, p.scale_log2, lane);
+    attend_subtile(st, sb + k_lane, sb + v_lane, static_cast<unsigned>(tok_mask), p.scale_log2, lane);
     if (flags & F_END) {
       if (finish_piece<NG>(st, (flags & F_FINAL) != 0, hb, h0, slot_id(blockIdx.x, (flags & F_SLOT1) ? 1 : 0), w,
                            si, p, lane)) {
@@ -302,19 +324,19 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
   }
 }
 
-template <int NG, int D>
+template <int NG, int D, bool SP>
 static cudaError_t launch_lsu(const DecodeParams& p, int num_ctas, cudaStream_t stream) {
   using C = LsuCfg<NG, D>;
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gqa_decode_lsu_kernel<NG, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(gqa_decode_lsu_kernel<NG, D, SP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  gqa_decode_lsu_kernel<NG, D><<<num_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
+  gqa_decode_lsu_kernel<NG, D, SP><<<num_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -330,10 +352,15 @@ int lsu_smem_bytes(int ng, int stages) {
 
 cudaError_t launch_decode_lsu(int ng, int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream) {
 #define X(NG, D) \
-  if (ng == NG && stages == D) return launch_lsu<NG, D>(p, num_ctas, stream);
+  if (ng == NG && stages == D) return launch_lsu<NG, D, false>(p, num_ctas, stream);
   GQA_LSU_VARIANTS(X)
 #undef X
   return cudaErrorInvalidValue;
+}
+
+// Selected-token mode: one variant, 4 KV heads per CTA and a 2-deep ring.
+cudaError_t launch_decode_lsu_sparse(const DecodeParams& p, int num_ctas, cudaStream_t stream) {
+  return launch_lsu<4, 2, true>(p, num_ctas, stream);
 }
 
 }  // namespace gqa

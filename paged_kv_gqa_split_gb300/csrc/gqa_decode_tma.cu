@@ -292,8 +292,9 @@ __device__ __forceinline__ void tma_consumer(const DecodeParams& p, uint32_t sba
 #pragma unroll
     for (int sub = 0; sub < TILE / 16; ++sub) {
       if (sub * 16 < cnt) {
+        const int c = cnt - sub * 16;
         attend_subtile(st, sb + k_lane + sub * 16 * C::kRowPitch, sb + v_lane + sub * 16 * C::kRowPitch,
-                       cnt - sub * 16, p.scale_log2, lane);
+                       c >= 16 ? 0xffffu : ((1u << c) - 1u), p.scale_log2, lane);
       }
     }
     // the stage's shared memory is no longer read by this warp

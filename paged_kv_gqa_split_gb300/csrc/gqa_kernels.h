@@ -33,7 +33,10 @@ struct DecodeParams {
   unsigned long long epoch;     // this call's ticket epoch (never 0, < 2^40)
   int4* split_rec;              // [P1 + P2] per-CTA split records for the merge kernel
   PlanConfig plan;              // the grid is plan.tier1_ctas + plan.tier2_ctas CTAs
-  int batch;
+  int batch;                    // sequences (sparse mode: query rows)
+  int sparse_topk;              // 0: paged mode (kv_indptr / kv_indices); > 0: every row has this many
+                                // columns and kv_indices holds their resolved slots (-1: masked out)
+  int sparse_total;             // sparse mode: rows * sparse_topk (kv_indptr is not read)
   float scale_log2;        // sm_scale * log2(e)
   int num_pages_check;     // > 0: page ids are range-checked against it
   int fuse_max_splits;     // split sequences of at most this many pieces are merged by the decode kernel
@@ -59,6 +62,8 @@ struct MergeParams {
   unsigned long long epoch;       // the call's epoch (tags the records)
   PlanConfig plan;  // the decode kernel's plan
   int batch;
+  int sparse_topk;   // as in DecodeParams
+  int sparse_total;
   int use_pdl;
   int fuse_max_splits;  // sequences of at most this many pieces were merged by the decode kernel
 };
@@ -82,6 +87,12 @@ struct KernelChoice {
 
 int lsu_smem_bytes(int ng, int stages);
 cudaError_t launch_decode_lsu(int ng, int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream);
+// The selected-token variant (p.sparse_topk > 0): 4 KV heads per CTA, 2 stages.
+cudaError_t launch_decode_lsu_sparse(const DecodeParams& p, int num_ctas, cudaStream_t stream);
+// Resolve the selected columns of a sparse batch to slots (-1: invalid column).
+cudaError_t launch_sparse_resolve(const int* logical_indices, const int* block_table, const int* token_to_req,
+                                  int* slots, int rows, int topk, int page_size, int page_table_width,
+                                  int num_requests, int num_cache_blocks, int sm_count, cudaStream_t stream);
 int tma_smem_bytes(int ng, int tile, int stages);
 cudaError_t launch_decode_tma(int ng, int tile, int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream);
 

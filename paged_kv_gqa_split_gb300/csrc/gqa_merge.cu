@@ -65,8 +65,9 @@ struct MergeAcc {
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
       const float mn = fmaxf(m[h], l8[h]);
-      const float sc = ex2(m[h] - mn);  // 0 while nothing has been added (m = -inf)
-      const float wt = ex2(l8[h] - mn);
+      const float sh = mn == -INFINITY ? 0.f : mn;  // all -inf so far (pieces with no valid token)
+      const float sc = ex2(m[h] - sh);  // 0 while nothing has been added (m = -inf)
+      const float wt = ex2(l8[h] - sh);
       den[h] = den[h] * sc + wt;
       acc[h] = acc[h] * sc + wt * o8[h];
       m[h] = mn;
@@ -89,8 +90,10 @@ __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const MergePar
   const bool boundary = j + 1 < p.plan.tier1_ctas + p.plan.tier2_ctas;
   // Loads that do not depend on the decode grid go out before the wait, so
   // their round trip overlaps it; nothing waits on them until after it.
-  const int T = __ldg(p.kv_indptr + B);
-  const bool check_empty = j < B;
+  // sparse rows (sparse_topk > 0) are never empty and have no kv_indptr
+  const bool sparse = p.sparse_topk > 0;
+  const int T = sparse ? p.sparse_total : __ldg(p.kv_indptr + B);
+  const bool check_empty = !sparse && j < B;
   const int e_lo = check_empty ? __ldg(p.kv_indptr + j) : 0;
   const int e_hi = check_empty ? __ldg(p.kv_indptr + j + 1) : 0;
 
@@ -101,11 +104,11 @@ __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const MergePar
   const int4 rec = boundary ? __ldcg(p.split_rec + j) : make_int4(0, 0, 0, 0);
 
   // Empty sequences: O = 0, LSE = -inf (no decode CTA touches them).
-  for (int b = j; b < B; b += gridDim.x) {
+  for (int b = j; !sparse && b < B; b += gridDim.x) {
     if (b == j ? e_lo == e_hi : __ldg(p.kv_indptr + b) == __ldg(p.kv_indptr + b + 1)) {
       uint4* ob = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(b) * kQoHeads * kHeadDim);
       for (int i = tid; i < kQoHeads * kHeadDim * 2 / 16; i += kMergeThreads) ob[i] = make_uint4(0, 0, 0, 0);
-      if (tid < kQoHeads) p.lse[static_cast<int64_t>(b) * kQoHeads + tid] = -INFINITY;
+      if (tid < kQoHeads && p.lse != nullptr) p.lse[static_cast<int64_t>(b) * kQoHeads + tid] = -INFINITY;
     }
   }
 
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const MergePar
   const int rank = j - static_cast<int>(sp.first_cta);  // which of this sequence's S - 1 boundaries
   const int nranks = S - 1;
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(b) * kQoHeads + hg * kH8) * kHeadDim;
-  float* lo = p.lse + static_cast<int64_t>(b) * kQoHeads + hg * kH8;
+  float* lo = p.lse != nullptr ? p.lse + static_cast<int64_t>(b) * kQoHeads + hg * kH8 : nullptr;
 
   if (S <= kMergeSmallSplits) {
     // (reached when the decode kernel's own merge is turned down by tuning)
@@ -142,10 +145,13 @@ __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const MergePar
         ma.add(lr[0], lr[1], __ldcg(orow), __ldcg(orow + 1));
       }
 #pragma unroll
-      for (int h = 0; h < 8; ++h) ob[(g * kGroup + h) * kHeadDim + d] = __float2bfloat16_rn(ma.acc[h] / ma.den[h]);
-      if ((it & 3) == 0 && lane == 0) {
+      for (int h = 0; h < 8; ++h) {
+        const float o = ma.den[h] > 0.f ? ma.acc[h] / ma.den[h] : 0.f;  // no valid token anywhere: O = 0
+        ob[(g * kGroup + h) * kHeadDim + d] = __float2bfloat16_rn(o);
+      }
+      if ((it & 3) == 0 && lane == 0 && lo != nullptr) {
 #pragma unroll
-        for (int h = 0; h < 8; ++h) lo[g * kGroup + h] = ma.m[h] + log2f(ma.den[h]);
+        for (int h = 0; h < 8; ++h) lo[g * kGroup + h] = ma.den[h] > 0.f ? ma.m[h] + log2f(ma.den[h]) : -INFINITY;
       }
     }
   } else {
@@ -257,8 +263,8 @@ __global__ void __launch_bounds__(kMergeThreads) gqa_merge_kernel(const MergePar
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int h = g * kGroup + hq * 4 + i;
-          ob[h * kHeadDim + d] = __float2bfloat16_rn(acc[i] / den[i]);
-          if (d == 0) lo[h] = m[i] + log2f(den[i]);
+          ob[h * kHeadDim + d] = __float2bfloat16_rn(den[i] > 0.f ? acc[i] / den[i] : 0.f);
+          if (d == 0 && lo != nullptr) lo[h] = den[i] > 0.f ? m[i] + log2f(den[i]) : -INFINITY;
         }
       }
     }

@@ -21,7 +21,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gqa_paged_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(gqa_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_problem_entry_point():
@@ -123,3 +123,34 @@ def test_append_argument_checks(lib):
     assert _lib.gqa_paged_kv_append(a, a, a, a, a, 3, 0, None) == _lib.GQA_ERR_INVALID_ARGUMENT
     assert _lib.gqa_paged_kv_append(a, None, a, a, a, 3, 4, None) == _lib.GQA_ERR_INVALID_ARGUMENT
     assert _lib.gqa_paged_kv_append(a + 8, a, a, a, a, 3, 4, None) == _lib.GQA_ERR_INVALID_ARGUMENT
+
+
+def _sparse_args(**kw):
+    a = 1 << 20  # 16-byte aligned dummy device address; no call below reaches the device
+    args = dict(q=a, k_cache=a, v_cache=a, logical_indices=a, block_table=a, token_to_req=a, sm_scale=0.1, out=a,
+                lse=a, rows=2, topk=8, page_size=16, num_cache_blocks=10, num_requests=2, page_table_width=4,
+                stream=None)
+    args.update(kw)
+    return list(args.values())
+
+
+def test_sparse_rows_zero_is_a_noop(lib):
+    assert _lib.gqa_sparse_paged_decode(*_sparse_args(rows=0, q=None, k_cache=None)) == 0
+
+
+@pytest.mark.parametrize("bad", [dict(rows=-1), dict(topk=0), dict(page_size=0), dict(num_cache_blocks=0),
+                                 dict(num_requests=0), dict(page_table_width=0), dict(q=None), dict(out=None),
+                                 dict(block_table=None), dict(token_to_req=None), dict(logical_indices=None),
+                                 dict(sm_scale=float("nan")), dict(q=(1 << 20) + 8), dict(lse=(1 << 20) + 4),
+                                 dict(logical_indices=(1 << 20) + 2), dict(num_cache_blocks=1 << 26, page_size=64),
+                                 dict(rows=1 << 20, topk=1 << 12)])
+def test_sparse_bad_arguments_rejected(lib, bad):
+    assert _lib.gqa_sparse_paged_decode(*_sparse_args(**bad)) == _lib.GQA_ERR_INVALID_ARGUMENT
+
+
+def test_sparse_cpu_tensors_raise():
+    import torch
+    from paged_kv_gqa_split_gb300 import workloads as wl
+    w = wl.make_sparse_workload([5, 9], 4, 4, seed=1)
+    with pytest.raises(ValueError, match="no CPU path"):
+        _lib.sparse_run(w.q, w.k_cache, w.v_cache, w.logical_indices, w.block_table, w.token_to_req)
