@@ -329,3 +329,43 @@ def make_sparse_config() -> SparseWorkload:
     lens = torch.randint(c["len_lo"], c["len_hi"] + 1, (c["rows"],), generator=g).tolist()
     return make_sparse_workload(lens, c["topk"], c["page_size"], c["seed"] + 1000, pool_factor=c["pool_factor"],
                                 name="sparse")
+
+
+# --------------------------------------------------------------------- fp8
+FP8_ROW_BYTES = NUM_KV_HEADS * HEAD_DIM + 4 * NUM_KV_HEADS  # 512 e4m3 values + 4 fp32 scales per token
+
+
+def quantize_fp8_rows(x: torch.Tensor) -> torch.Tensor:
+    """[P, 1, 4, 128] bf16 -> [P, 528] uint8 FP8 cache rows.
+
+    Each (token, KV head) row of 128 values gets the scale amax / 448 (1 for an
+    all-zero row) and is stored as e4m3 codes of x / scale (torch's
+    round-to-nearest cast), followed by the 4 heads' float32 scales. This is
+    input encoding only: the decode reads the rows as given.
+    """
+    xf = x.reshape(-1, NUM_KV_HEADS, HEAD_DIM).to(torch.float32)
+    amax = xf.abs().amax(dim=2)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    codes = (xf / scale[:, :, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    rows = torch.empty((xf.shape[0], FP8_ROW_BYTES), dtype=torch.uint8)
+    rows[:, :NUM_KV_HEADS * HEAD_DIM] = codes.reshape(-1, NUM_KV_HEADS * HEAD_DIM)
+    rows[:, NUM_KV_HEADS * HEAD_DIM:] = scale.contiguous().view(torch.uint8).reshape(-1, 4 * NUM_KV_HEADS)
+    return rows
+
+
+def make_fp8_workload(lens: Sequence[int], seed: int, *, pool_factor: float = 1.0, q_std: float = 1.0,
+                      name: str = "custom_fp8") -> Workload:
+    """The bf16 workload of the same lengths and seed, with K and V quantized to
+    [P, 528]-byte FP8 rows (quantize_fp8_rows). q, kv_indptr and kv_indices are
+    unchanged."""
+    w = make_workload(lens, seed, pool_factor=pool_factor, q_std=q_std, name=name)
+    return Workload(name, w.q, quantize_fp8_rows(w.k_cache), quantize_fp8_rows(w.v_cache), w.kv_indptr,
+                    w.kv_indices, w.sm_scale, list(w.lens))
+
+
+def make_fp8_config(name: str) -> Workload:
+    """A named workload (same lengths, seed and pool as the bf16 one) over an FP8 cache."""
+    cfg = CONFIGS[name]
+    g = torch.Generator().manual_seed(cfg.seed)
+    lens = cfg.lens_fn(g)
+    return make_fp8_workload(lens, cfg.seed, pool_factor=cfg.pool_factor, q_std=cfg.q_std, name=name + "_fp8")
