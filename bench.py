@@ -336,6 +336,37 @@ def bench_sparse(device, steps, warmup, peak):
     return res
 
 
+# ------------------------------------------------------------ FP8 KV cache
+def bench_fp8(w, g, device, steps, warmup, peak):
+    """Decode of workload w over an FP8 copy of its cache (528-byte rows: 4 KV
+    heads x 128 e4m3 codes + 4 fp32 scales, quantized on the device from the
+    bf16 cache already in HBM, outside the timed region). Counted bytes: 1056 B
+    per token (K and V rows) + 16,512 B of q, O and LSE per sequence. Times the
+    default ring depth and the other two compiled ones."""
+    k8 = wl.quantize_fp8_rows(g.k_cache)
+    v8 = wl.quantize_fp8_rows(g.v_cache)
+    out = torch.empty_like(g.q)
+    lse = torch.empty((w.batch, 32), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    flush = L2Flush(device)
+    b = 1056 * w.total_tokens + 16512 * w.batch
+    res = {"workload": w.name, "counted_bytes": b, "bytes_vs_bf16": b / counted_bytes(w.lens)}
+    for stages in (2, 3, 4):
+        _lib.gqa_paged_decode_set_tuning(0, 0, 4, 16, stages, 0)
+
+        def call():
+            _lib.run_fp8(g.q, k8, v8, g.kv_indptr, g.kv_indices, w.sm_scale, out=out, lse=lse, stream=stream)
+        for _ in range(warmup):
+            call()
+        ms = statistics.median(time_steps(call, steps, stream, flush))
+        res[f"stages_{stages}"] = {"us_per_batch": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9,
+                                   "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
+    _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0)
+    res.update(res["stages_2"])  # the default depth
+    del k8, v8, out, lse, flush
+    return res
+
+
 # -------------------------------------------------------------- CPU oracle
 def oracle_sample(w, budget_s: float):
     """Run the float64 oracle over the workload's sequences in order until about
@@ -512,10 +543,11 @@ def main():
             if ww is not w:
                 del ww
 
-    append = sparse = None
+    append = sparse = fp8 = None
     if not args.no_workloads:
         append = bench_append(device, args.steps, warmup, w.batch, peak)
         sparse = bench_sparse(device, args.steps, warmup, peak)
+        fp8 = bench_fp8(w, w.to(device), device, args.steps, warmup, peak)
 
     cpu, parity = None, None
     if rank == 0 and not args.no_cpu_baseline:
@@ -559,6 +591,7 @@ def main():
         "workloads": table,
         "kv_append": append,
         "sparse_decode": sparse,
+        "fp8_decode": fp8,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

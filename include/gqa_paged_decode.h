@@ -177,6 +177,27 @@ int64_t gqa_paged_decode_plan(const int32_t* kv_indptr, int batch, int num_ctas,
                               int64_t* pieces, int64_t capacity);
 
 /*
+ * gqa_paged_decode over an FP8 KV cache. The cache format follows the FP8
+ * cache of the flash_mla_with_kvcache page (docs.flagos.io, FlagGems):
+ * float8_e4m3 values followed by one float32 scale per 128 values, a value
+ * being e4m3 * scale. For this shape one token row of k_cache (and of
+ * v_cache) is 528 bytes: the e4m3 codes of KV heads 0..3 (128 each,
+ * head-major, bytes 0..511), then the 4 heads' little-endian float32 scales
+ * (bytes 512..527). k_cache, v_cache: [num_pages][528] bytes, 16-byte
+ * aligned; every other argument, the result (bf16 O, fp32 base-2 LSE) and
+ * the error behaviour are those of gqa_paged_decode.
+ *
+ * The kernel converts e4m3 to f16 exactly, takes each token's K scale on its
+ * score and its V scale on its probability, and computes Q.K and P.V with f16
+ * tensor-core operands (Q rescaled by a power of two per KV head so that it
+ * cannot overflow f16). It uses 4 KV heads per CTA; a tuning with 4 heads per
+ * CTA and 2-4 stages sets its ring depth (default 2).
+ */
+int gqa_paged_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_indptr,
+                         const int32_t* kv_indices, float sm_scale, void* out, float* lse, int batch,
+                         struct CUstream_st* stream);
+
+/*
  * Selected-token (sparse) paged GQA decode: the sparse split-K GQA path of
  * the sigit.si vLLM "qsa.py" page (qsa_sparse_paged_attention and its
  * _qsa_sparse_paged_gqa_splitk_kernel), for 32 query heads over 4 KV heads

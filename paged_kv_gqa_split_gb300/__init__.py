@@ -5,9 +5,10 @@ calls the CUDA library through its C ABI (include/gqa_paged_decode.h). The
 library is built in-tree by ``paged_kv_gqa_split_gb300.build.build()``; it is
 loaded on first use, and every call fails loudly if it is missing.
 ``sparse_run(q, k_cache, v_cache, logical_indices, block_table, token_to_req)``
-is the selected-token variant over a block table of any page size, and
+is the selected-token variant over a block table of any page size,
+``run_fp8`` reads an FP8 (e4m3, per-128 fp32 scale) cache, and
 ``kv_append`` stores new tokens' K/V rows into the page pool.
 """
-from ._lib import GqaError, kv_append, run, run_checked, sparse_run  # noqa: F401
+from ._lib import GqaError, kv_append, run, run_checked, run_fp8, sparse_run  # noqa: F401
 
-__all__ = ["GqaError", "kv_append", "run", "run_checked", "sparse_run"]
+__all__ = ["GqaError", "kv_append", "run", "run_checked", "run_fp8", "sparse_run"]

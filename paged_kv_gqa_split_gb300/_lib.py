@@ -45,6 +45,7 @@ _SIGNATURES = {
     "gqa_paged_kv_append": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int, _vp]),
     "gqa_paged_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_int, _vp]),
     "gqa_sparse_paged_decode": (ctypes.c_int, [_vp] * 6 + [ctypes.c_float, _vp, _vp] + [ctypes.c_int] * 6 + [_vp]),
+    "gqa_paged_decode_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_int, _vp]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -338,4 +339,61 @@ def sparse_run(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, lo
                                      int(block_table.shape[1]), stream.cuda_stream)
     if rc != GQA_OK:
         raise GqaError(rc, "gqa_sparse_paged_decode")
+    return out, lse
+
+
+FP8_ROW_BYTES = NUM_KV_HEADS * HEAD_DIM + 4 * NUM_KV_HEADS  # 512 e4m3 codes + 4 fp32 scales per token
+
+
+def gqa_paged_decode_fp8(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream) -> int:
+    return load().gqa_paged_decode_fp8(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream)
+
+
+def run_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, kv_indptr: torch.Tensor,
+            kv_indices: torch.Tensor, sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Paged GQA decode over FP8 caches of [P, 528] uint8 rows (4 KV heads x 128
+    e4m3 codes, then the 4 heads' float32 scales). Returns (out [B, 32, 128]
+    bf16, lse [B, 32] fp32, base 2)."""
+    tensors = {"q": q, "k_cache": k_cache, "v_cache": v_cache, "kv_indptr": kv_indptr, "kv_indices": kv_indices}
+    for name, t in tensors.items():
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if not t.is_cuda:
+            raise ValueError(f"{name} is on {t.device}: the CUDA library has no CPU path; move inputs to the GPU")
+        if t.device != q.device:
+            raise ValueError(f"all inputs must be on {q.device}; {name} is on {t.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dim() != 3 or tuple(q.shape[1:]) != (NUM_QO_HEADS, HEAD_DIM) or q.dtype != torch.bfloat16:
+        raise ValueError("expected q [B, 32, 128] bf16")
+    for name in ("k_cache", "v_cache"):
+        t = tensors[name]
+        if t.dtype != torch.uint8 or t.dim() < 2 or t.shape[-1] != FP8_ROW_BYTES:
+            raise ValueError(f"{name} must be uint8 rows of {FP8_ROW_BYTES} bytes ([P, {FP8_ROW_BYTES}])")
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must have the same shape")
+    for name in ("kv_indptr", "kv_indices"):
+        if tensors[name].dtype != torch.int32:
+            raise ValueError(f"{name} must be int32")
+    if kv_indptr.dim() != 1 or kv_indptr.shape[0] < 1:
+        raise ValueError("kv_indptr must be [B + 1]")
+    batch = int(q.shape[0])
+    if kv_indptr.shape[0] != batch + 1:
+        raise ValueError(f"kv_indptr has {kv_indptr.shape[0]} entries; expected batch + 1 = {batch + 1}")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((batch, NUM_QO_HEADS), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        rc = gqa_paged_decode_fp8(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), kv_indptr.data_ptr(),
+                                  kv_indices.data_ptr(), float(sm_scale), out.data_ptr(), lse.data_ptr(), batch,
+                                  stream.cuda_stream)
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_paged_decode_fp8")
     return out, lse

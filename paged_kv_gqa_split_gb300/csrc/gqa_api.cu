@@ -179,7 +179,7 @@ int library_workspace(DeviceState* st, size_t need, void** ws) {
 // resolved slots).
 int run(const void* q, const void* k, const void* v, const int32_t* indptr, const int32_t* indices, float sm_scale,
         void* out, float* lse, int batch, cudaStream_t stream, void* user_ws, size_t user_ws_bytes, bool checked,
-        int num_pages, int* dev_err, bool fit_ws = false, const SparseJob* sj = nullptr) {
+        int num_pages, int* dev_err, bool fit_ws = false, const SparseJob* sj = nullptr, bool fp8 = false) {
   if (sj == nullptr) {
     const int rc0 = check_args(q, k, v, indptr, indices, sm_scale, out, lse, batch);
     if (rc0 != GQA_OK) return rc0;
@@ -201,6 +201,11 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
     if (rc != GQA_OK) return rc;
     tune = g_tune;
     if (sj != nullptr) tune.kernel = KernelChoice{gqa::kGatherLsu, 4, 16, 2};  // the one sparse variant
+    if (fp8) {  // FP8 caches: the FP8 variant; a cp.async tuning with 4 heads per CTA picks its depth
+      const KernelChoice& k = tune.kernel;
+      const bool pick = k.gather == gqa::kGatherLsu && k.heads_per_cta == 4 && k.stages >= 2 && k.stages <= 4;
+      tune.kernel = KernelChoice{gqa::kGatherLsuF8, 4, 16, pick ? k.stages : 2};
+    }
     ev0 = g_ev_start;
     ev1 = g_ev_stop;
     cfg = plan_config(*st, tune);
@@ -537,6 +542,13 @@ int gqa_sparse_paged_decode(const void* q, const void* k_cache, const void* v_ca
                      num_cache_blocks};
   return run(q, k_cache, v_cache, nullptr, nullptr, sm_scale, out, lse, rows, stream, nullptr, 0, false, 0, nullptr,
              false, &sj);
+}
+
+int gqa_paged_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_indptr,
+                         const int32_t* kv_indices, float sm_scale, void* out, float* lse, int batch,
+                         struct CUstream_st* stream) {
+  return run(q, k_cache, v_cache, kv_indptr, kv_indices, sm_scale, out, lse, batch, stream, nullptr, 0, false, 0,
+             nullptr, false, nullptr, true);
 }
 
 int gqa_paged_decode_device_error(int* flags) {

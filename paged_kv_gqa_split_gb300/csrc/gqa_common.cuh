@@ -67,23 +67,41 @@ struct HeadState {
   float acc[8][4];   // O^T accumulators
   float m0, m1;      // running max (base-2 logits) of heads 2c, 2c + 1
   float l0, l1;      // running sum of 2^(s - m) over this lane's tokens
+  float qsc;         // FP8 path: 1 / the power of two Q was scaled by for f16
+  float cv;          // FP8 path: running power of two >= every V scale of the piece (0: none yet)
 
   __device__ __forceinline__ void reset() {
     m0 = m1 = -INFINITY;
     l0 = l1 = 0.f;
+    cv = 0.f;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
   }
 };
 
 // Q^T B-fragments straight from global memory: query rows q[b, h0 .. h0+7, :].
+// PERM (the FP8-cache path): k-block t = 4 kb + j takes, in lane (r, c), the
+// dims 64 kb + 16 c + 4 j .. + 3 instead of 16 t + 2 c, +1 and 16 t + 8 + 2 c,
+// +1: the same permutation of the contraction dims as the e4m3 K fragments,
+// which a lane reads as 16 consecutive bytes of a K row (attend_subtile_f8).
+template <bool PERM = false>
 __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[16], const __nv_bfloat16* q, int64_t b, int h0, int lane) {
   const int r = lane >> 2, c = lane & 3;
-  const uint32_t* row = reinterpret_cast<const uint32_t*>(q + (b * kQoHeads + h0 + r) * kHeadDim) + c;
+  if constexpr (PERM) {
+    const __nv_bfloat16* row = q + (b * kQoHeads + h0 + r) * kHeadDim;
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    qf[2 * kk] = __ldg(row + 8 * kk);
-    qf[2 * kk + 1] = __ldg(row + 8 * kk + 4);
+    for (int t = 0; t < 8; ++t) {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(row + 64 * (t >> 2) + 16 * c + 4 * (t & 3)));
+      qf[2 * t] = v.x;
+      qf[2 * t + 1] = v.y;
+    }
+  } else {
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(q + (b * kQoHeads + h0 + r) * kHeadDim) + c;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      qf[2 * kk] = __ldg(row + 8 * kk);
+      qf[2 * kk + 1] = __ldg(row + 8 * kk + 4);
+    }
   }
 }
 
@@ -144,6 +162,121 @@ __device__ __forceinline__ void attend_subtile(HeadState& st, uint32_t k_addr, u
     ldsm_x4_trans(v_addr + mt * 32, v0, v1, v2, v3);
     mma_bf16_16816(st.acc[mt], v0, v1, v2, v3, b0, b1);
   }
+}
+
+// FP8-cache form of attend_subtile, straight from the staged e4m3 rows (no
+// conversion pass through shared memory; e4m3 -> f16 is exact):
+// - K (rows = tokens at a 192-byte pitch): lane (r, c) reads 16 bytes of rows
+//   r and r + 8 per 64-dim block with one 128-bit load each and converts them
+//   into the A fragments of 4 k-blocks; the contraction dims are thereby
+//   permuted within each 64-dim block, and Q's fragments follow the same
+//   permutation (load_q_frags<true>).
+// - V (rows = tokens at a 144-byte pitch): ldmatrix.trans gives each lane the
+//   bytes of tokens 2c, 2c + 1 for dims 2g, 2g + 1; a byte permute pairs the
+//   tokens of one dim before the conversion, so A-fragment row g of m-tile mt
+//   holds dim 16 mt + 2 g and row g + 8 holds dim 16 mt + 2 g + 1
+//   (finish_piece<.., true> writes O accordingly).
+// sk_lo / sk_hi and sv_lo / sv_hi are the scales of this lane's tokens r and
+// r + 8 for this KV head. A score takes its token's K scale (and Q's
+// power-of-two f16 scale, through st.qsc). A probability enters P.V times its
+// token's V scale over st.cv, a running power of two no smaller than any V
+// scale seen in the piece, so the f16 P operand stays in [0, 1]; acc then
+// holds O * l / cv, and l sums the plain probabilities.
+__device__ __forceinline__ void attend_subtile_f8(HeadState& st, uint32_t k_addr, uint32_t v_addr, unsigned valid,
+                                                  float scale_log2, float sk_lo, float sk_hi, float sv_lo,
+                                                  float sv_hi, int lane, int k_pitch) {
+  const int r = lane >> 2;
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb) {
+    uint32_t x[4], y[4];
+    ld_shared_u4(k_addr + kb * 64, x[0], x[1], x[2], x[3]);                // row r
+    ld_shared_u4(k_addr + 8 * k_pitch + kb * 64, y[0], y[1], y[2], y[3]);  // row r + 8
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int t = 4 * kb + j;
+      mma_f16_16816(s, cvt_e4m3x2_f16x2(x[j]), cvt_e4m3x2_f16x2(y[j]), cvt_e4m3x2_f16x2(x[j] >> 16),
+                    cvt_e4m3x2_f16x2(y[j] >> 16), st.qf[2 * t], st.qf[2 * t + 1]);
+    }
+  }
+  const bool v_lo = (valid >> r) & 1u, v_hi = (valid >> (r + 8)) & 1u;
+  const float c_lo = scale_log2 * st.qsc * sk_lo, c_hi = scale_log2 * st.qsc * sk_hi;
+  s[0] = v_lo ? s[0] * c_lo : -INFINITY;
+  s[1] = v_lo ? s[1] * c_lo : -INFINITY;
+  s[2] = v_hi ? s[2] * c_hi : -INFINITY;
+  s[3] = v_hi ? s[3] * c_hi : -INFINITY;
+  float mx0 = fmaxf(s[0], s[2]);
+  float mx1 = fmaxf(s[1], s[3]);
+  float vm = fmaxf(v_lo ? fabsf(sv_lo) : 0.f, v_hi ? fabsf(sv_hi) : 0.f);
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+  }
+  const float mn0 = fmaxf(st.m0, mx0);
+  const float mn1 = fmaxf(st.m1, mx1);
+  const float sh0 = mn0 == -INFINITY ? 0.f : mn0;
+  const float sh1 = mn1 == -INFINITY ? 0.f : mn1;
+  const float a0 = ex2(st.m0 - sh0);
+  const float a1 = ex2(st.m1 - sh1);
+  st.m0 = mn0;
+  st.m1 = mn1;
+  const float cv_new = fmaxf(st.cv, vm > 0.f ? pow2_ceil(vm) : 0.f);
+  const float cr = cv_new > 0.f ? st.cv / cv_new : 1.f;  // exact: both are powers of two (or st.cv = 0)
+  const float iv = cv_new > 0.f ? 1.f / cv_new : 0.f;
+  st.cv = cv_new;
+  const float p0 = ex2(s[0] - sh0), p1 = ex2(s[1] - sh1);  // token r
+  const float p2 = ex2(s[2] - sh0), p3 = ex2(s[3] - sh1);  // token r + 8
+  st.l0 = st.l0 * a0 + (p0 + p2);
+  st.l1 = st.l1 * a1 + (p1 + p3);
+  const float b_a0 = a0 * cr, b_a1 = a1 * cr;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    st.acc[mt][0] *= b_a0;
+    st.acc[mt][1] *= b_a1;
+    st.acc[mt][2] *= b_a0;
+    st.acc[mt][3] *= b_a1;
+  }
+  const float w_lo = sv_lo * iv, w_hi = sv_hi * iv;
+  const uint32_t b0 = movmatrix_trans(pack_f16(p0 * w_lo, p1 * w_lo));
+  const uint32_t b1 = movmatrix_trans(pack_f16(p2 * w_hi, p3 * w_hi));
+#pragma unroll
+  for (int mp = 0; mp < 4; ++mp) {  // m-tiles 2 mp and 2 mp + 1
+    uint32_t t0, t1, t2, t3;        // tokens 0-7 / 8-15 of m-tile 2 mp, then of 2 mp + 1
+    ldsm_x4_trans(v_addr + mp * 32, t0, t1, t2, t3);
+    mma_f16_16816(st.acc[2 * mp], cvt_e4m3x2_f16x2(__byte_perm(t0, 0, 0x0020)),
+                  cvt_e4m3x2_f16x2(__byte_perm(t0, 0, 0x0031)), cvt_e4m3x2_f16x2(__byte_perm(t1, 0, 0x0020)),
+                  cvt_e4m3x2_f16x2(__byte_perm(t1, 0, 0x0031)), b0, b1);
+    mma_f16_16816(st.acc[2 * mp + 1], cvt_e4m3x2_f16x2(__byte_perm(t2, 0, 0x0020)),
+                  cvt_e4m3x2_f16x2(__byte_perm(t2, 0, 0x0031)), cvt_e4m3x2_f16x2(__byte_perm(t3, 0, 0x0020)),
+                  cvt_e4m3x2_f16x2(__byte_perm(t3, 0, 0x0031)), b0, b1);
+  }
+}
+
+// FP8-cache path: turn bf16 Q fragments into f16 ones scaled by a power of two
+// chosen so that the group's largest |q| lands in [2^13, 2^14) (no f16
+// overflow; exact for every component down to 2^-27 of that maximum).
+// Returns the inverse of the scale, folded into the score scale.
+__device__ __forceinline__ float q_frags_to_f16(uint32_t (&qf)[16]) {
+  float mx = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&qf[i]);
+    mx = fmaxf(mx, fmaxf(fabsf(__low2float(v)), fabsf(__high2float(v))));
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  int e = static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu);  // biased exponent of the maximum
+  int se = mx > 0.f ? 127 + 13 - (e - 127) : 127;                   // 2^(13 - (e - 127)), or 1
+  se = se < 1 ? 1 : (se > 253 ? 253 : se);  // keeps 1 / qs a normal float
+  const float qs = __uint_as_float(static_cast<uint32_t>(se) << 23);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&qf[i]);
+    qf[i] = pack_f16(__low2float(v) * qs, __high2float(v) * qs);
+  }
+  return __uint_as_float(static_cast<uint32_t>(254 - se) << 23);  // 1 / qs, exact
 }
 
 // Where a piece's sequence was cut: S pieces held by decode CTAs first_cta ..
@@ -320,9 +453,12 @@ __device__ __forceinline__ void merge_split_warp_staged(const float* part_o, con
 // true for a partial of a sequence cut into at most fuse_max_splits pieces:
 // the warp must count its arrival (arrive_pieces) after its main loop, and
 // merges the sequence if its arrival was the last.
-template <int NG>
+// DP (the FP8-cache path): accumulator row g of m-tile mt holds dim
+// 16 mt + 2 g and row g + 8 dim 16 mt + 2 g + 1 (see attend_subtile_f8).
+template <int NG, bool DP = false>
 __device__ __forceinline__ bool finish_piece(const HeadState& st, bool final_piece, int64_t b, int h0, int64_t sid,
-                                             int w, const SplitInfo& si, const DecodeParams& p, int lane) {
+                                             int w, const SplitInfo& si, const DecodeParams& p, int lane,
+                                             float oscale = 1.f) {
   const int r = lane >> 2, c = lane & 3;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
   float lt0 = st.l0, lt1 = st.l1;
@@ -332,8 +468,9 @@ __device__ __forceinline__ bool finish_piece(const HeadState& st, bool final_pie
     lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
   }
   // a piece whose tokens were all masked out has l = 0: O = 0, LSE = -inf
-  const float i0 = lt0 > 0.f ? 1.f / lt0 : 0.f;
-  const float i1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
+  // oscale: the FP8 path's acc holds O * l / cv, so its oscale is cv
+  const float i0 = lt0 > 0.f ? oscale / lt0 : 0.f;
+  const float i1 = lt1 > 0.f ? oscale / lt1 : 0.f;
   const float lse0 = lt0 > 0.f ? st.m0 + log2f(lt0) : -INFINITY;
   const float lse1 = lt1 > 0.f ? st.m1 + log2f(lt1) : -INFINITY;
   if (final_piece) {
@@ -343,8 +480,13 @@ __device__ __forceinline__ bool finish_piece(const HeadState& st, bool final_pie
       // rows = dims, cols = heads  ->  transpose to rows = heads, cols = dims
       const uint32_t x = movmatrix_trans(pack_bf16(st.acc[mt][0] * i0, st.acc[mt][1] * i1));
       const uint32_t y = movmatrix_trans(pack_bf16(st.acc[mt][2] * i0, st.acc[mt][3] * i1));
-      *reinterpret_cast<uint32_t*>(ob + r * kHeadDim + mt * 16 + 2 * c) = x;
-      *reinterpret_cast<uint32_t*>(ob + r * kHeadDim + mt * 16 + 8 + 2 * c) = y;
+      if constexpr (DP) {  // x: dims 4c, 4c + 2; y: dims 4c + 1, 4c + 3 (of m-tile mt)
+        *reinterpret_cast<uint2*>(ob + r * kHeadDim + mt * 16 + 4 * c) =
+            make_uint2(__byte_perm(x, y, 0x5410), __byte_perm(x, y, 0x7632));
+      } else {
+        *reinterpret_cast<uint32_t*>(ob + r * kHeadDim + mt * 16 + 2 * c) = x;
+        *reinterpret_cast<uint32_t*>(ob + r * kHeadDim + mt * 16 + 8 + 2 * c) = y;
+      }
     }
     if (r == 0 && p.lse != nullptr) *reinterpret_cast<float2*>(p.lse + b * kQoHeads + h0 + 2 * c) = make_float2(lse0, lse1);
     return false;
@@ -352,9 +494,10 @@ __device__ __forceinline__ bool finish_piece(const HeadState& st, bool final_pie
   float* po = p.part_o + (sid * NG + w) * (kHeadDim * kGroup);
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
-    *reinterpret_cast<float2*>(po + (mt * 16 + r) * kGroup + 2 * c) = make_float2(st.acc[mt][0] * i0, st.acc[mt][1] * i1);
-    *reinterpret_cast<float2*>(po + (mt * 16 + 8 + r) * kGroup + 2 * c) =
-        make_float2(st.acc[mt][2] * i0, st.acc[mt][3] * i1);
+    const int d_lo = DP ? mt * 16 + 2 * r : mt * 16 + r;          // dim of accumulator row r
+    const int d_hi = DP ? mt * 16 + 2 * r + 1 : mt * 16 + 8 + r;  // dim of accumulator row r + 8
+    *reinterpret_cast<float2*>(po + d_lo * kGroup + 2 * c) = make_float2(st.acc[mt][0] * i0, st.acc[mt][1] * i1);
+    *reinterpret_cast<float2*>(po + d_hi * kGroup + 2 * c) = make_float2(st.acc[mt][2] * i0, st.acc[mt][3] * i1);
   }
   if (r == 0) *reinterpret_cast<float2*>(p.part_lse + (sid * NG + w) * kGroup + 2 * c) = make_float2(lse0, lse1);
   return si.S <= p.fuse_max_splits;  // else the merge kernel combines this sequence

@@ -33,14 +33,27 @@
 
 namespace gqa {
 
-template <int NG, int D>
+// Per-warp shared memory. bf16 cache (F8 = false): each stage holds the K and
+// V head rows of one tile at a 272-byte pitch, ready for ldmatrix. FP8 cache
+// (F8 = true): each stage holds the tile's 128-byte e4m3 head rows of K (at a
+// 192-byte pitch: the 128-bit row reads of attend_subtile_f8 then hit 8
+// distinct bank groups) and of V (at a 144-byte pitch, for ldmatrix), plus
+// their per-token scales.
+template <int NG, int D, bool F8 = false>
 struct LsuCfg {
   static constexpr int kHG = kKvHeads / NG;           // head groups on the unit line
   static constexpr int kTile = 16;                    // tokens per stage (one mma sub-tile)
   static constexpr int kRowPitch = kHeadDim * 2 + 16; // 256 B head row + 16 B: ldmatrix rows hit all banks
+  static constexpr int kRowBytes8 = kHeadDim;         // e4m3 head row
+  // global row of one token (all 4 KV heads): 1 KB of bf16, or 512 B of e4m3 + 4 fp32 scales
+  static constexpr int kGlobalRowBytes = F8 ? kKvHeads * kHeadDim + 4 * kKvHeads : kPageBytes;
+  static constexpr int kK8Pitch = 192;                // F8 K row pitch
+  static constexpr int kV8Pitch = 144;                // F8 V row pitch
   static constexpr int kKOff = 0;
-  static constexpr int kVOff = kTile * kRowPitch;
-  static constexpr int kHdrOff = 2 * kTile * kRowPitch;
+  static constexpr int kVOff = F8 ? kTile * kK8Pitch : kTile * kRowPitch;
+  static constexpr int kSkOff = kVOff + kTile * kV8Pitch;  // F8: K scales of the tile's tokens
+  static constexpr int kSvOff = kSkOff + kTile * 4;         // F8: V scales
+  static constexpr int kHdrOff = F8 ? kSvOff + kTile * 4 : 2 * kTile * kRowPitch;
   static constexpr int kStageBytes = kHdrOff + 32;    // tile header: 8 ints
   static constexpr int kIdsRing = 256;                // page ids held per warp (tokens)
   static constexpr int kIdsOff = D * kStageBytes;
@@ -78,9 +91,11 @@ struct Tile {
 // SP: selected-token (sparse) mode. Every row of the batch is one "sequence" of
 // exactly p.sparse_topk columns; kv_indices holds their resolved slots, and a
 // slot of -1 (an invalid column) is masked out of the softmax.
-template <int NG, int D, bool SP>
-__global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const DecodeParams p) {
-  using C = LsuCfg<NG, D>;
+// F8: the K/V caches are FP8 rows (kGlobalRowBytes per token): e4m3 values of
+// the 4 KV heads, then their fp32 scales.
+template <int NG, int D, bool SP, bool F8 = false>
+__global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kernel(const DecodeParams p) {
+  using C = LsuCfg<NG, D, F8>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int w = threadIdx.x >> 5;  // KV head within the head group
   const int lane = threadIdx.x & 31;
@@ -212,12 +227,45 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
         ib += 32;
       }
       int flags = tl.flags;
-      const int64_t hoff = static_cast<int64_t>(tl.hg * NG + w) * (kHeadDim * 2);
+      const int64_t hoff = static_cast<int64_t>(tl.hg * NG + w) * (F8 ? kHeadDim : kHeadDim * 2);
       const int pc = lane & 15;  // 16-byte column of the 256-byte head row
       // tokens that enter the softmax: the first cnt, less (sparse mode) masked columns
       unsigned mask = tl.cnt >= 16 ? 0xffffu : ((1u << tl.cnt) - 1u);
+      if constexpr (F8) {
+        // 16 tokens x 8 16-byte chunks of the 128-byte e4m3 head row, for K and V
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 4; ++i) {
+          const int tok = 4 * i + (lane >> 3), ch = lane & 7;
+          bool valid = tok < tl.cnt;
+          int pg = valid ? ids[(tl.tt + tok) & (C::kIdsRing - 1)] : 0;
+          if (valid && p.num_pages_check > 0 &&
+              static_cast<unsigned>(pg) >= static_cast<unsigned>(p.num_pages_check)) {
+            atomicOr(p.err, kErrBadPage);
+            valid = false;
+            pg = 0;
+          }
+          const int64_t off = static_cast<int64_t>(pg) * C::kGlobalRowBytes + hoff + ch * 16;
+          const uint32_t nbytes = valid ? 16u : 0u;
+          cp_async_16(sb + C::kKOff + tok * C::kK8Pitch + ch * 16, kc + off, nbytes);
+          cp_async_16(sb + C::kVOff + tok * C::kV8Pitch + ch * 16, vc + off, nbytes);
+        }
+        {  // the per-token scales of this KV head: lanes 0-15 K, 16-31 V
+          const int tok = lane & 15;
+          bool valid = tok < tl.cnt;
+          int pg = valid ? ids[(tl.tt + tok) & (C::kIdsRing - 1)] : 0;
+          if (valid && p.num_pages_check > 0 &&
+              static_cast<unsigned>(pg) >= static_cast<unsigned>(p.num_pages_check)) {
+            valid = false;
+            pg = 0;
+          }
+          const int64_t off = static_cast<int64_t>(pg) * C::kGlobalRowBytes + kKvHeads * kHeadDim +
+                              (tl.hg * NG + w) * 4;
+          cp_async_4(sb + (lane < 16 ? C::kSkOff : C::kSvOff) + tok * 4, (lane < 16 ? kc : vc) + off,
+                     valid ? 4u : 0u);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < (F8 ? 0 : 8); ++i) {
         const int tok = 2 * i + (lane >> 4);
         bool valid = tok < tl.cnt;
         int pg = valid ? ids[(tl.tt + tok) & (C::kIdsRing - 1)] : 0;
@@ -242,7 +290,7 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
       if (flags & F_QLOAD) {
         const int h0 = (tl.hg * NG + w) * kGroup;
         if (!qn_busy) {
-          load_q_frags(qn, qg, tl.b, h0, lane);
+          load_q_frags<F8>(qn, qg, tl.b, h0, lane);
           qn_busy = true;
           flags |= F_QREG;
         } else if (lane < 16) {
@@ -266,8 +314,13 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
   st.reset();
 #pragma unroll
   for (int i = 0; i < 16; ++i) st.qf[i] = 0;
-  const uint32_t k_lane = C::kKOff + ((lane & 7) + ((lane >> 3) & 1) * 8) * C::kRowPitch + (lane >> 4) * 16;
-  const uint32_t v_lane = C::kVOff + ((lane & 7) + (lane >> 4) * 8) * C::kRowPitch + ((lane >> 3) & 1) * 16;
+  // per-lane ldmatrix row addresses within a stage. F8: K row (lane >> 2) at
+  // column (lane & 3) * 16 for the 128-bit reads; V matrix (lane >> 3) is
+  // tokens 0-7 / 8-15 of dims block 0 / 1 for ldmatrix.trans.
+  const uint32_t k_lane = F8 ? C::kKOff + (lane >> 2) * C::kK8Pitch + (lane & 3) * 16
+                             : C::kKOff + ((lane & 7) + ((lane >> 3) & 1) * 8) * C::kRowPitch + (lane >> 4) * 16;
+  const uint32_t v_lane = F8 ? C::kVOff + (((lane >> 3) & 1) * 8 + (lane & 7)) * C::kV8Pitch + (lane >> 4) * 16
+                             : C::kVOff + ((lane & 7) + (lane >> 4) * 8) * C::kRowPitch + ((lane >> 3) & 1) * 16;
 
   OwedMerge pend[2];  // split pieces whose arrival is counted after the loop
   int n_pend = 0;
@@ -292,14 +345,23 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
         for (int i = 0; i < 16; ++i) st.qf[i] = qn[i];
         qn_busy = false;
       } else {
-        load_q_frags(st.qf, qg, hb, h0, lane);
+        load_q_frags<F8>(st.qf, qg, hb, h0, lane);
       }
       st.reset();
+      if constexpr (F8) st.qsc = q_frags_to_f16(st.qf);
     }
-    attend_subtile(st, sb + k_lane, sb + v_lane, static_cast<unsigned>(tok_mask), p.scale_log2, lane);
+    if constexpr (F8) {
+      const int r = lane >> 2;
+      const float sk_lo = ld_shared_f32(sb + C::kSkOff + r * 4), sk_hi = ld_shared_f32(sb + C::kSkOff + (r + 8) * 4);
+      const float sv_lo = ld_shared_f32(sb + C::kSvOff + r * 4), sv_hi = ld_shared_f32(sb + C::kSvOff + (r + 8) * 4);
+      attend_subtile_f8(st, sb + k_lane, sb + v_lane, static_cast<unsigned>(tok_mask), p.scale_log2, sk_lo, sk_hi,
+                        sv_lo, sv_hi, lane, C::kK8Pitch);
+    } else {
+      attend_subtile(st, sb + k_lane, sb + v_lane, static_cast<unsigned>(tok_mask), p.scale_log2, lane);
+    }
     if (flags & F_END) {
-      if (finish_piece<NG>(st, (flags & F_FINAL) != 0, hb, h0, slot_id(blockIdx.x, (flags & F_SLOT1) ? 1 : 0), w,
-                           si, p, lane)) {
+      if (finish_piece<NG, F8>(st, (flags & F_FINAL) != 0, hb, h0, slot_id(blockIdx.x, (flags & F_SLOT1) ? 1 : 0),
+                               w, si, p, lane, F8 ? st.cv : 1.f)) {
         pend[n_pend < 2 ? n_pend : 1] = {si, hb, h0};
         n_pend = min(n_pend + 1, 2);
       }
@@ -324,19 +386,19 @@ __global__ void __launch_bounds__(NG * 32, 16 / NG) gqa_decode_lsu_kernel(const 
   }
 }
 
-template <int NG, int D, bool SP>
+template <int NG, int D, bool SP, bool F8 = false>
 static cudaError_t launch_lsu(const DecodeParams& p, int num_ctas, cudaStream_t stream) {
-  using C = LsuCfg<NG, D>;
+  using C = LsuCfg<NG, D, F8>;
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gqa_decode_lsu_kernel<NG, D, SP>,
+    cudaError_t e = cudaFuncSetAttribute(gqa_decode_lsu_kernel<NG, D, SP, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  gqa_decode_lsu_kernel<NG, D, SP><<<num_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
+  gqa_decode_lsu_kernel<NG, D, SP, F8><<<num_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -361,6 +423,25 @@ cudaError_t launch_decode_lsu(int ng, int stages, const DecodeParams& p, int num
 // Selected-token mode: one variant, 4 KV heads per CTA and a 2-deep ring.
 cudaError_t launch_decode_lsu_sparse(const DecodeParams& p, int num_ctas, cudaStream_t stream) {
   return launch_lsu<4, 2, true>(p, num_ctas, stream);
+}
+
+// FP8-cache variants: 4 KV heads per CTA, 2, 3 or 4 stages.
+#define GQA_LSU_F8_VARIANTS(X) X(4, 2) X(4, 3) X(4, 4)
+
+int lsu_f8_smem_bytes(int stages) {
+#define X(NG, D) \
+  if (stages == D) return LsuCfg<NG, D, true>::kSmemBytes;
+  GQA_LSU_F8_VARIANTS(X)
+#undef X
+  return -1;
+}
+
+cudaError_t launch_decode_lsu_f8(int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream) {
+#define X(NG, D) \
+  if (stages == D) return launch_lsu<NG, D, false, true>(p, num_ctas, stream);
+  GQA_LSU_F8_VARIANTS(X)
+#undef X
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace gqa

@@ -76,7 +76,7 @@ int decode_in_scratch(const void* q, const void* k_cache, const void* v_cache, c
                       void* scratch, size_t scratch_bytes);
 
 // Compile-time variant of the decode kernel.
-enum : int { kGatherLsu = 0, kGatherTma = 1 };
+enum : int { kGatherLsu = 0, kGatherTma = 1, kGatherLsuF8 = 2 };  // kGatherLsuF8: FP8 caches only
 
 struct KernelChoice {
   int gather;         // kGatherLsu: self-loading warps with cp.async; kGatherTma: producer warp + bulk copies
@@ -86,6 +86,8 @@ struct KernelChoice {
 };
 
 int lsu_smem_bytes(int ng, int stages);
+int lsu_f8_smem_bytes(int stages);
+cudaError_t launch_decode_lsu_f8(int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream);
 cudaError_t launch_decode_lsu(int ng, int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream);
 // The selected-token variant (p.sparse_topk > 0): 4 KV heads per CTA, 2 stages.
 cudaError_t launch_decode_lsu_sparse(const DecodeParams& p, int num_ctas, cudaStream_t stream);
@@ -100,18 +102,22 @@ cudaError_t launch_decode_tma(int ng, int tile, int stages, const DecodeParams& 
 inline int decode_smem_bytes(const KernelChoice& k) {
   if (k.gather == kGatherLsu) return k.tile == 16 ? lsu_smem_bytes(k.heads_per_cta, k.stages) : -1;
   if (k.gather == kGatherTma) return tma_smem_bytes(k.heads_per_cta, k.tile, k.stages);
+  if (k.gather == kGatherLsuF8) return k.heads_per_cta == 4 && k.tile == 16 ? lsu_f8_smem_bytes(k.stages) : -1;
   return -1;
 }
 
 // Warps a variant runs per CTA and the most CTAs per SM worth launching.
 inline int decode_max_ctas_per_sm(const KernelChoice& k) {
-  // LSU: up to 16 gathering warps per SM; TMA: up to 4 consumer warps per SM.
+  // LSU: up to 16 gathering warps per SM; TMA: up to 4 consumer warps per SM; FP8: 3 CTAs (its
+  // launch bounds leave 170 registers per thread).
+  if (k.gather == kGatherLsuF8) return 3;
   return k.gather == kGatherLsu ? 16 / k.heads_per_cta : 4 / k.heads_per_cta;
 }
 
 inline cudaError_t launch_decode(const KernelChoice& k, const DecodeParams& p, int num_ctas, cudaStream_t stream) {
   if (k.gather == kGatherLsu) return launch_decode_lsu(k.heads_per_cta, k.stages, p, num_ctas, stream);
   if (k.gather == kGatherTma) return launch_decode_tma(k.heads_per_cta, k.tile, k.stages, p, num_ctas, stream);
+  if (k.gather == kGatherLsuF8) return launch_decode_lsu_f8(k.stages, p, num_ctas, stream);
   return cudaErrorInvalidValue;
 }
 

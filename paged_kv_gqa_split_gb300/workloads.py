@@ -347,7 +347,7 @@ def quantize_fp8_rows(x: torch.Tensor) -> torch.Tensor:
     amax = xf.abs().amax(dim=2)
     scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
     codes = (xf / scale[:, :, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
-    rows = torch.empty((xf.shape[0], FP8_ROW_BYTES), dtype=torch.uint8)
+    rows = torch.empty((xf.shape[0], FP8_ROW_BYTES), dtype=torch.uint8, device=x.device)
     rows[:, :NUM_KV_HEADS * HEAD_DIM] = codes.reshape(-1, NUM_KV_HEADS * HEAD_DIM)
     rows[:, NUM_KV_HEADS * HEAD_DIM:] = scale.contiguous().view(torch.uint8).reshape(-1, 4 * NUM_KV_HEADS)
     return rows

@@ -154,3 +154,21 @@ def test_sparse_cpu_tensors_raise():
     w = wl.make_sparse_workload([5, 9], 4, 4, seed=1)
     with pytest.raises(ValueError, match="no CPU path"):
         _lib.sparse_run(w.q, w.k_cache, w.v_cache, w.logical_indices, w.block_table, w.token_to_req)
+
+
+def test_fp8_argument_checks(lib):
+    a = 1 << 20
+    assert _lib.gqa_paged_decode_fp8(None, None, None, None, None, 0.1, None, None, 0, None) == 0
+    assert _lib.gqa_paged_decode_fp8(a, a, a, a, a, 0.1, a, a, -1, None) == _lib.GQA_ERR_INVALID_ARGUMENT
+    assert _lib.gqa_paged_decode_fp8(a, a, a, None, a, 0.1, a, a, 2, None) == _lib.GQA_ERR_INVALID_ARGUMENT
+    assert _lib.gqa_paged_decode_fp8(a, a + 8, a, a, a, 0.1, a, a, 2, None) == _lib.GQA_ERR_INVALID_ARGUMENT
+    assert _lib.gqa_paged_decode_fp8(a, a, a, a, a, float("nan"), a, a, 2, None) == _lib.GQA_ERR_INVALID_ARGUMENT
+
+
+def test_fp8_wrapper_checks():
+    import torch
+    from paged_kv_gqa_split_gb300 import workloads as wl
+    w = wl.make_fp8_workload([3, 4], seed=1)
+    with pytest.raises(ValueError, match="no CPU path"):
+        _lib.run_fp8(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices)
+    assert w.k_cache.shape[1] == _lib.FP8_ROW_BYTES and w.k_cache.dtype == torch.uint8

@@ -1,0 +1,105 @@
+"""Paged GQA decode over an FP8 (e4m3, per-128 fp32 scale) cache, on the GPU,
+against the float64 oracle over the same FP8 rows (oracle/fp8.py).
+
+The tolerances are the dense path's: |dO| <= 2e-2 + 2e-2 |O_ref|, |dlse| <= 1e-3.
+The oracle dequantizes the very bytes the kernel reads, so the comparison
+measures the kernel's arithmetic, not the quantization of the inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.fp8 as f8
+from paged_kv_gqa_split_gb300 import _lib
+from paged_kv_gqa_split_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+O_ATOL, O_RTOL, LSE_ATOL = 2e-2, 2e-2, 1e-3
+
+
+@pytest.fixture(autouse=True)
+def _defaults(cuda_device):
+    _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0)
+    yield
+    _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0)
+
+
+def gpu_fp8(w):
+    g = w.to("cuda")
+    out, lse = _lib.run_fp8(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, w.sm_scale)
+    torch.cuda.synchronize()
+    return out.float().cpu().double().numpy(), lse.cpu().double().numpy()
+
+
+def check(w, out, lse, seqs=None):
+    o_ref, l_ref = f8.gqa_paged_decode_fp8_oracle(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices, w.sm_scale,
+                                                  seqs)
+    sel = list(range(w.batch)) if seqs is None else list(seqs)
+    o, orf, l, lrf = out[sel], o_ref[sel], lse[sel], l_ref[sel]
+    bad = np.abs(o - orf) > O_ATOL + O_RTOL * np.abs(orf)
+    assert not bad.any(), f"{bad.sum()} O elements out of tolerance, max |dO| {np.abs(o - orf).max():.3g}"
+    assert np.array_equal(np.isneginf(l), np.isneginf(lrf))
+    fin = np.isfinite(lrf)
+    assert np.all(np.abs(l[fin] - lrf[fin]) <= LSE_ATOL), np.abs(l[fin] - lrf[fin]).max()
+    assert np.all(o[~fin.any(axis=1)] == 0)
+
+
+@pytest.mark.parametrize("lens", [[1], [0], [0, 0, 3], [15, 16, 17], [255, 256, 257, 0, 129],
+                                  [3, 1000, 0, 77, 2049, 1, 16, 600], list(range(1, 41))])
+def test_fp8_edge_and_ragged(lens):
+    w = wl.make_fp8_workload(lens, seed=len(lens) + 300, pool_factor=1.5)
+    out, lse = gpu_fp8(w)
+    check(w, out, lse)
+
+
+@pytest.mark.parametrize("tuning", [(0, 0, 4, 16, 2, 0), (0, 0, 4, 16, 3, 0), (0, 0, 4, 16, 4, 0),
+                                    (40, 8, 4, 16, 2, 0, 0, 0, 500, 16), (7, 1, 4, 16, 3, 0, 0, 13, 400, 4),
+                                    (300, 1, 4, 16, 2, 0, 4), (60, 8, 4, 16, 4, 0, -1, -1)])
+def test_fp8_variants_and_splits(tuning):
+    assert _lib.gqa_paged_decode_set_tuning(*tuning) == 0
+    w = wl.make_fp8_workload([5000, 3, 17, 0, 900, 1, 64], seed=301, pool_factor=1.1)
+    out, lse = gpu_fp8(w)
+    check(w, out, lse)
+
+
+def test_fp8_large_queries():
+    """|q| near 1e4: the f16 form of Q needs its power-of-two rescale."""
+    w = wl.make_fp8_workload([700, 64, 3], seed=302, q_std=1.0)
+    w.q.mul_(8192.0)                                   # exact in bf16 (a power of two)
+    w.sm_scale = w.sm_scale / 8192.0 / 4.0             # keep the logits in a sane range
+    out, lse = gpu_fp8(w)
+    check(w, out, lse)
+
+
+def _scale_rows(cache, up, down):
+    sc = cache[:, 512:].clone().view(torch.float32)          # [P, 4]
+    sc[0::7] *= up
+    sc[3::11] *= down
+    cache[:, 512:] = sc.view(torch.uint8)
+
+
+def test_fp8_extreme_and_zero_scales():
+    """K scales 2^4 up and down on some tokens (sharp softmax), V scales 2^5 up
+    and down on others (the P operand's running normaliser), all-zero rows
+    elsewhere. Much larger spreads leave the test's absolute tolerances, not
+    the kernel: logits near 10^6 have an fp32 ulp far above 1e-3 in the LSE,
+    and V scales 2^20 apart within one sequence push the small-scale tokens'
+    probabilities into f16's subnormal range, an error that grows with the
+    largest V value as it does for any 16-bit P operand."""
+    w = wl.make_fp8_workload([900, 300, 40], seed=303)
+    _scale_rows(w.k_cache, 2.0 ** 4, 2.0 ** -4)
+    _scale_rows(w.v_cache, 2.0 ** 5, 2.0 ** -5)
+    w.v_cache[5::13, :512] = 0                                   # zero codes: value 0 whatever the scale
+    w.k_cache[9::17, :] = 0                                      # zero codes and zero scales
+    out, lse = gpu_fp8(w)
+    check(w, out, lse)
+
+
+@pytest.mark.parametrize("name", ["mid", "skewed"])
+def test_fp8_named_workloads_sampled(name):
+    w = wl.make_fp8_config(name)
+    out, lse = gpu_fp8(w)
+    lens = np.array(w.lens)
+    seqs = sorted({0, w.batch // 2, int(np.argmax(lens)), w.batch - 1})
+    check(w, out, lse, seqs)
