@@ -481,6 +481,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="time every decode variant instead of the contract line")
+    ap.add_argument("--only", choices=["fp8", "sparse"], default=None,
+                    help="time only the FP8-cache decode of --workload, or only the selected-token decode, and "
+                         "print its result (for profiling a small case)")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
 
@@ -503,6 +506,16 @@ def main():
 
     if args.sweep:
         sweep(device, args.steps, warmup, ["tiny", "mid", "long", "large", "skewed"])
+        return
+    if args.only is not None:
+        peak, _ = hbm_peak()
+        if args.only == "fp8":
+            w = wl.make_config(args.workload)
+            res = bench_fp8(w, w.to(device), device, args.steps, warmup, peak)
+        else:
+            res = bench_sparse(device, args.steps, warmup, peak)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "result": res}), flush=True)
         return
 
     peak, peak_kind = hbm_peak()
