@@ -369,3 +369,84 @@ def make_fp8_config(name: str) -> Workload:
     g = torch.Generator().manual_seed(cfg.seed)
     lens = cfg.lens_fn(g)
     return make_fp8_workload(lens, cfg.seed, pool_factor=cfg.pool_factor, q_std=cfg.q_std, name=name + "_fp8")
+
+
+# --------------------------------------------------------------------- mla
+MLA_D_QK = 576
+MLA_D_V = 512
+
+
+@dataclass
+class MlaWorkload:
+    """Inputs of a dense MLA paged decode (one latent KV head), all on the CPU.
+
+    Shapes follow the flash_mla_with_kvcache page: q [B, s_q, h_q, 576] bf16;
+    kv_cache [num_blocks, page_size, 1, 576] bf16 (the first 512 values of a
+    row are also its value vector); block_table [B, width] int32;
+    cache_seqlens [B] int32.
+    """
+
+    name: str
+    q: torch.Tensor
+    kv_cache: torch.Tensor
+    block_table: torch.Tensor
+    cache_seqlens: torch.Tensor
+    softmax_scale: float
+    lens: List[int] = field(default_factory=list)
+
+    @property
+    def batch(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def page_size(self) -> int:
+        return int(self.kv_cache.shape[1])
+
+    @property
+    def total_tokens(self) -> int:
+        return int(sum(self.lens))
+
+    def to(self, device, non_blocking: bool = False) -> "MlaWorkload":
+        t = lambda x: x.to(device, non_blocking=non_blocking)  # noqa: E731
+        return MlaWorkload(self.name, t(self.q), t(self.kv_cache), t(self.block_table), t(self.cache_seqlens),
+                           self.softmax_scale, list(self.lens))
+
+
+def make_mla_workload(lens: Sequence[int], h_q: int, s_q: int, page_size: int, seed: int, *,
+                      pool_factor: float = 1.25, q_std: float = 1.0, name: str = "mla") -> MlaWorkload:
+    """Sequence b holds lens[b] cached tokens in ceil(lens[b] / page_size)
+    blocks, taken in order from a seeded random permutation of
+    ceil(pool_factor * blocks in use) blocks (the rest of its block-table row
+    is -1). Draw order: the block permutation, then q, then the cache."""
+    g = torch.Generator().manual_seed(seed)
+    lens = [int(x) for x in lens]
+    bsz = len(lens)
+    nblk = [(n + page_size - 1) // page_size for n in lens]
+    width = max(1, max(nblk) if nblk else 1)
+    num_blocks = max(1, int(math.ceil(pool_factor * sum(nblk))))
+    perm = torch.randperm(num_blocks, generator=g)
+    table = torch.full((bsz, width), -1, dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(nblk):
+        table[b, :n] = perm[off:off + n].to(torch.int32)
+        off += n
+    q = _randn_bf16((bsz, s_q, h_q, MLA_D_QK), g, q_std)
+    kv = _randn_bf16((num_blocks, page_size, 1, MLA_D_QK), g)
+    return MlaWorkload(name, q, kv, table.contiguous(), torch.tensor(lens, dtype=torch.int32),
+                       MLA_D_QK ** -0.5, lens)
+
+
+# Dense MLA decode workload timed by bench.py: the pages fix the latent shape
+# (576 / 512, one KV head) and show blocks of 64; the batch takes decode-sized
+# sequences with 16 query heads per sequence (a DeepSeek-style model split 8
+# ways by heads): 128 sequences of U[1024, 8192] cached tokens (about 680 MB of
+# latent rows per call).
+MLA_CONFIG = dict(batch=128, h_q=16, s_q=1, page_size=64, len_lo=1024, len_hi=8192, seed=6, pool_factor=1.25)
+
+
+def make_mla_config() -> MlaWorkload:
+    c = MLA_CONFIG
+    g = torch.Generator().manual_seed(c["seed"])
+    lens = torch.randint(c["len_lo"], c["len_hi"] + 1, (c["batch"],), generator=g).tolist()
+    return make_mla_workload(lens, c["h_q"], c["s_q"], c["page_size"], c["seed"] + 1000,
+                             pool_factor=c["pool_factor"], name="mla")
