@@ -367,6 +367,38 @@ def bench_fp8(w, g, device, steps, warmup, peak):
     return res
 
 
+# ------------------------------------------------------------ MLA decode
+def bench_mla(device, steps, warmup, peak):
+    """Dense MLA decode of the MLA workload (128 sequences of U[1024, 8192]
+    cached tokens, 16 query heads, blocks of 64): µs per call and GB/s of the
+    counted bytes, 1152 B of latent row per cached token plus q (1152 B),
+    O (1024 B) and LSE (4 B) per query row. FLOPs: 2 * (576 + 512) per
+    (token, query row)."""
+    w = wl.make_mla_config()
+    g = w.to(device)
+    rows = int(w.q.shape[1] * w.q.shape[2])
+    out = torch.empty((w.batch, w.q.shape[1], w.q.shape[2], 512), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((w.batch, w.q.shape[2], w.q.shape[1]), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    flush = L2Flush(device)
+
+    def call():
+        _lib.mla_run(g.q, g.kv_cache, g.block_table, g.cache_seqlens, w.softmax_scale, out=out, lse=lse,
+                     stream=stream)
+    for _ in range(warmup):
+        call()
+    ms = statistics.median(time_steps(call, steps, stream, flush))
+    t = w.total_tokens
+    b = 1152 * t + (1152 + 1024 + 4) * rows * w.batch
+    flops = 2 * (576 + 512) * t * rows
+    res = {"batch": w.batch, "h_q": int(w.q.shape[2]), "s_q": int(w.q.shape[1]), "page_size": w.page_size,
+           "total_tokens": t, "us_per_batch": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9,
+           "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak, "tflops": flops / (ms * 1e-3) / 1e12,
+           "counted_bytes": b, "launches_per_call": 4}
+    del g, out, lse, flush
+    return res
+
+
 # -------------------------------------------------------------- CPU oracle
 def oracle_sample(w, budget_s: float):
     """Run the float64 oracle over the workload's sequences in order until about
@@ -481,7 +513,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="time every decode variant instead of the contract line")
-    ap.add_argument("--only", choices=["fp8", "sparse"], default=None,
+    ap.add_argument("--only", choices=["fp8", "sparse", "mla"], default=None,
                     help="time only the FP8-cache decode of --workload, or only the selected-token decode, and "
                          "print its result (for profiling a small case)")
     args = ap.parse_args()
@@ -512,6 +544,8 @@ def main():
         if args.only == "fp8":
             w = wl.make_config(args.workload)
             res = bench_fp8(w, w.to(device), device, args.steps, warmup, peak)
+        elif args.only == "mla":
+            res = bench_mla(device, args.steps, warmup, peak)
         else:
             res = bench_sparse(device, args.steps, warmup, peak)
         if rank == 0:
@@ -556,11 +590,12 @@ def main():
             if ww is not w:
                 del ww
 
-    append = sparse = fp8 = None
+    append = sparse = fp8 = mla = None
     if not args.no_workloads:
         append = bench_append(device, args.steps, warmup, w.batch, peak)
         sparse = bench_sparse(device, args.steps, warmup, peak)
         fp8 = bench_fp8(w, w.to(device), device, args.steps, warmup, peak)
+        mla = bench_mla(device, args.steps, warmup, peak)
 
     cpu, parity = None, None
     if rank == 0 and not args.no_cpu_baseline:
@@ -605,6 +640,7 @@ def main():
         "kv_append": append,
         "sparse_decode": sparse,
         "fp8_decode": fp8,
+        "mla_decode": mla,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

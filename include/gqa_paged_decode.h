@@ -198,6 +198,40 @@ int gqa_paged_decode_fp8(const void* q, const void* k_cache, const void* v_cache
                          struct CUstream_st* stream);
 
 /*
+ * Dense MLA paged decode: the dense decode of the flash_mla_with_kvcache page
+ * (docs.flagos.io, FlagGems; flash_mla_with_kvcache without sparse indices),
+ * for one latent KV head of d_qk = 576 values per token (512 "NoPE" values,
+ * which are also V, then 64 "RoPE" values) and d_v = 512.
+ *
+ * For sequence b, query token i < s_q and head h < h_q, over the cached
+ * tokens t < cache_seqlens[b] at kv_cache[block_table[b * page_table_width
+ * + t / page_size]][t % page_size][0][:]:
+ * s_t = softmax_scale * q[b][i][h][:] . kv_t[:] (all 576 values),
+ * out[b][i][h][:] = sum_t softmax(s)_t kv_t[0:512] (bf16) and, when lse is
+ * not NULL, lse[b][h][i] = log sum_t exp(s_t) (natural log, fp32; the page's
+ * layout). Not causal within the s_q query tokens (the page's dense kernel
+ * supports causal masking only for s_q = 1, where it changes nothing). A
+ * sequence with no cached token gives out = 0 and lse = -inf; a token whose
+ * block-table entry lies outside [0, num_blocks) is left out.
+ *
+ * Layouts (caller-owned device memory, contiguous): q [batch][s_q][h_q][576]
+ * bf16 and out [batch][s_q][h_q][512] bf16, 16-byte aligned; kv_cache
+ * [num_blocks][page_size][1][576] bf16, 16-byte aligned; block_table
+ * [batch][page_table_width] int32; cache_seqlens [batch] int32; lse
+ * [batch][h_q][s_q] fp32 or NULL. s_q * h_q must be a multiple of 16; a
+ * length above page_table_width * page_size counts as that (the tokens past
+ * the table have no block); negative lengths count as 0;
+ * num_blocks * page_size and batch * page_table_width * page_size must be
+ * below 2^31. Asynchronous on `stream`; batch == 0 returns 0 without
+ * launching. Uses the library-owned workspace (CSR offsets, one slot per
+ * cached token, fp32 partials). Returns GQA_OK, GQA_ERR_INVALID_ARGUMENT,
+ * GQA_ERR_WORKSPACE, GQA_ERR_LAUNCH or GQA_ERR_UNSUPPORTED_DEVICE.
+ */
+int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_table, const int32_t* cache_seqlens,
+                   float softmax_scale, void* out, float* lse, int batch, int s_q, int h_q, int page_size,
+                   int num_blocks, int page_table_width, struct CUstream_st* stream);
+
+/*
  * Selected-token (sparse) paged GQA decode: the sparse split-K GQA path of
  * the sigit.si vLLM "qsa.py" page (qsa_sparse_paged_attention and its
  * _qsa_sparse_paged_gqa_splitk_kernel), for 32 query heads over 4 KV heads

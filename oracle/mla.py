@@ -18,7 +18,9 @@ block_table[b, t // page_size], offset t % page_size. For every query row
 
 over t < cache_seqlens[b] (the page's dense kernel is not causal within the
 rows of one call). O is [B, s_q, h_q, 512]; lse is [B, h_q, s_q], the page's
-layout. A sequence with no cached token gives O = 0 and lse = -inf.
+layout. A sequence with no cached token gives O = 0 and lse = -inf. Tokens
+the page leaves undefined (past the block table, or in a block outside the
+pool) are left out (``mla_slots``).
 """
 from __future__ import annotations
 
@@ -34,14 +36,21 @@ D_QK = 576
 D_V = 512
 
 
-def mla_slots(block_table, cache_seqlens, page_size: int) -> list:
-    """Per sequence, the flat slot (block * page_size + offset) of every cached token."""
+def mla_slots(block_table, cache_seqlens, page_size: int, num_blocks: Optional[int] = None) -> list:
+    """Per sequence, the flat slot (block * page_size + offset) of every cached
+    token. Where the page leaves the result undefined (its kernel would read
+    outside the table or the pool), this reading leaves the token out: tokens
+    past the table's width * page_size, and tokens whose block lies outside
+    [0, num_blocks)."""
     table = np.asarray(_as_np_int(block_table), dtype=np.int64)
     lens = np.asarray(_as_np_int(cache_seqlens), dtype=np.int64)
+    cap = table.shape[1] * page_size
     out = []
     for b in range(lens.shape[0]):
-        t = np.arange(int(lens[b]), dtype=np.int64)
-        out.append(table[b, t // page_size] * page_size + t % page_size)
+        t = np.arange(min(max(int(lens[b]), 0), cap), dtype=np.int64)
+        blk = table[b, t // page_size]
+        keep = blk >= 0 if num_blocks is None else (blk >= 0) & (blk < num_blocks)
+        out.append((blk * page_size + t % page_size)[keep])
     return out
 
 
@@ -57,7 +66,7 @@ def mla_decode_oracle(q, kv_cache, block_table, cache_seqlens, softmax_scale: fl
     flat = kv_cache.reshape(num_blocks * page_size, D_QK)
     out = np.full((bsz, s_q, h_q, D_V), np.nan)
     lse = np.full((bsz, h_q, s_q), np.nan)
-    slots = mla_slots(block_table, cache_seqlens, page_size)
+    slots = mla_slots(block_table, cache_seqlens, page_size, num_blocks)
     todo = range(bsz) if seqs is None else seqs
     for b in todo:
         if len(slots[b]) == 0:                                   # nothing cached: O = 0, lse = -inf

@@ -46,6 +46,7 @@ _SIGNATURES = {
     "gqa_paged_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_int, _vp]),
     "gqa_sparse_paged_decode": (ctypes.c_int, [_vp] * 6 + [ctypes.c_float, _vp, _vp] + [ctypes.c_int] * 6 + [_vp]),
     "gqa_paged_decode_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_int, _vp]),
+    "gqa_mla_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp] + [ctypes.c_int] * 6 + [_vp]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -396,4 +397,60 @@ def run_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, kv_in
                                   stream.cuda_stream)
     if rc != GQA_OK:
         raise GqaError(rc, "gqa_paged_decode_fp8")
+    return out, lse
+
+
+MLA_D_QK, MLA_D_V = 576, 512
+
+
+def gqa_mla_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale, out, lse, batch, s_q, h_q, page_size,
+                   num_blocks, page_table_width, stream) -> int:
+    return load().gqa_mla_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale, out, lse, batch, s_q, h_q,
+                                 page_size, num_blocks, page_table_width, stream)
+
+
+def mla_run(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor, cache_seqlens: torch.Tensor,
+            softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None, with_lse: bool = True,
+            stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Dense MLA paged decode on the GPU (flash_mla_with_kvcache's dense path,
+    one latent KV head of 576 values, d_v = 512). Returns (out [B, s_q, h_q, 512]
+    bf16, lse [B, h_q, s_q] fp32 natural log, or None)."""
+    tensors = {"q": q, "kv_cache": kv_cache, "block_table": block_table, "cache_seqlens": cache_seqlens}
+    for name, t in tensors.items():
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if not t.is_cuda:
+            raise ValueError(f"{name} is on {t.device}: the CUDA library has no CPU path; move inputs to the GPU")
+        if t.device != q.device:
+            raise ValueError(f"all inputs must be on {q.device}; {name} is on {t.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dim() != 4 or q.shape[-1] != MLA_D_QK or q.dtype != torch.bfloat16:
+        raise ValueError("expected q [B, s_q, h_q, 576] bf16")
+    if kv_cache.dim() != 4 or kv_cache.shape[2] != 1 or kv_cache.shape[3] != MLA_D_QK or \
+            kv_cache.dtype != torch.bfloat16:
+        raise ValueError("expected kv_cache [num_blocks, page_size, 1, 576] bf16 (one latent KV head)")
+    bsz, s_q, h_q = (int(x) for x in q.shape[:3])
+    if block_table.dim() != 2 or block_table.shape[0] != bsz or block_table.dtype != torch.int32:
+        raise ValueError("block_table must be int32 [B, width]")
+    if cache_seqlens.shape != (bsz,) or cache_seqlens.dtype != torch.int32:
+        raise ValueError("cache_seqlens must be int32 [B]")
+    if (s_q * h_q) % 16:
+        raise ValueError("s_q * h_q must be a multiple of 16")
+    if softmax_scale is None:
+        softmax_scale = MLA_D_QK ** -0.5
+    if out is None:
+        out = torch.empty((bsz, s_q, h_q, MLA_D_V), dtype=torch.bfloat16, device=q.device)
+    if lse is None and with_lse:
+        lse = torch.empty((bsz, h_q, s_q), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        rc = gqa_mla_decode(q.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(), cache_seqlens.data_ptr(),
+                            float(softmax_scale), out.data_ptr(), lse.data_ptr() if lse is not None else None, bsz,
+                            s_q, h_q, int(kv_cache.shape[1]), int(kv_cache.shape[0]), int(block_table.shape[1]),
+                            stream.cuda_stream)
+    if rc != GQA_OK:
+        raise GqaError(rc, "gqa_mla_decode")
     return out, lse

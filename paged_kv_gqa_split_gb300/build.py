@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libgqa_paged_decode.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 SOURCES = ["gqa_decode_lsu.cu", "gqa_decode_tma.cu", "gqa_merge.cu", "gqa_api.cu", "gqa_noalloc.cu", "gqa_kv_append.cu",
-           "gqa_sparse.cu"]
+           "gqa_sparse.cu", "gqa_mla.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -551,6 +551,79 @@ int gqa_paged_decode_fp8(const void* q, const void* k_cache, const void* v_cache
              nullptr, false, nullptr, true);
 }
 
+int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_table, const int32_t* cache_seqlens,
+                   float softmax_scale, void* out, float* lse, int batch, int s_q, int h_q, int page_size,
+                   int num_blocks, int page_table_width, struct CUstream_st* stream) {
+  if (batch < 0) return GQA_ERR_INVALID_ARGUMENT;
+  if (batch == 0) return GQA_OK;
+  if (s_q <= 0 || h_q <= 0 || page_size <= 0 || num_blocks <= 0 || page_table_width <= 0)
+    return GQA_ERR_INVALID_ARGUMENT;
+  const int64_t rows = static_cast<int64_t>(s_q) * h_q;
+  if (rows % 16 != 0 || rows > (1 << 20)) return GQA_ERR_INVALID_ARGUMENT;
+  if (static_cast<int64_t>(num_blocks) * page_size > INT32_MAX) return GQA_ERR_INVALID_ARGUMENT;
+  const int64_t max_tokens = static_cast<int64_t>(batch) * page_table_width * page_size;  // bound on sum(seqlens)
+  if (max_tokens > INT32_MAX || max_tokens * (rows / 16) > (int64_t{1} << 40)) return GQA_ERR_INVALID_ARGUMENT;
+  if (q == nullptr || kv_cache == nullptr || block_table == nullptr || cache_seqlens == nullptr || out == nullptr)
+    return GQA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(softmax_scale)) return GQA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
+      !aligned(cache_seqlens, 4) || (lse != nullptr && !aligned(lse, 4)))
+    return GQA_ERR_INVALID_ARGUMENT;
+
+  DeviceState* st = nullptr;
+  int dev = 0;
+  gqa::PlanConfig cfg;
+  void* ws = nullptr;
+  size_t off_indptr = 0, off_slots = 0, off_po = 0, off_pl = 0, off_rec = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int rc = current_device(&dev, &st);
+    if (rc != GQA_OK) return rc;
+    const Tuning& t = g_tune;
+    cfg.tier1_ctas = t.num_ctas > 0 ? t.num_ctas : st->sm_count * 2;  // two 4-warp MLA CTAs per SM
+    cfg.tier2_ctas = t.tier2_ctas > 0 ? t.tier2_ctas : (t.tier2_ctas == 0 ? kDefaultTier2PerTier1 * cfg.tier1_ctas : 0);
+    cfg.min_units = t.min_units > 0 ? t.min_units : kDefaultMinUnits;
+    cfg.tier2_permille = t.tier2_permille;
+    cfg.tier2_min_units = t.tier2_min_units;
+    const size_t ctas = static_cast<size_t>(cfg.tier1_ctas) + cfg.tier2_ctas;
+    off_indptr = 0;
+    off_slots = round256(static_cast<size_t>(batch + 1) * 4);
+    off_po = off_slots + round256(static_cast<size_t>(max_tokens) * 4);
+    off_pl = off_po + round256(2 * ctas * 16 * 512 * sizeof(float));
+    off_rec = off_pl + round256(2 * ctas * 16 * sizeof(float));
+    const size_t need = off_rec + round256(2 * ctas * 16);
+    rc = library_workspace(st, need, &ws);
+    if (rc != GQA_OK) return rc;
+  }
+  char* wsb = static_cast<char*>(ws);
+  int* err_word = nullptr;
+  if (gqa::device_error_word(&err_word) != cudaSuccess) return GQA_ERR_LAUNCH;
+  gqa::MlaParams mp{};
+  mp.q = q;
+  mp.kv = kv_cache;
+  mp.kv_indptr_mut = reinterpret_cast<int*>(wsb + off_indptr);
+  mp.kv_indptr = mp.kv_indptr_mut;
+  mp.slots_mut = reinterpret_cast<int*>(wsb + off_slots);
+  mp.slots = mp.slots_mut;
+  mp.out = out;
+  mp.lse = lse;
+  mp.part_o = reinterpret_cast<float*>(wsb + off_po);
+  mp.part_lse = reinterpret_cast<float*>(wsb + off_pl);
+  mp.split_rec = reinterpret_cast<int4*>(wsb + off_rec);
+  mp.err = err_word;
+  mp.plan = cfg;
+  mp.epoch = (g_epoch.fetch_add(1) % ((1ull << 40) - 1)) + 1;
+  mp.batch = batch;
+  mp.rows = static_cast<int>(rows);
+  mp.h_q = h_q;
+  mp.s_q = s_q;
+  mp.scale_log2 = softmax_scale * kLog2e;
+  return gqa::launch_mla(mp, cache_seqlens, block_table, page_table_width, page_size, num_blocks, st->sm_count,
+                         stream) == cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_LAUNCH;
+}
+
 int gqa_paged_decode_device_error(int* flags) {
   if (flags == nullptr) return GQA_ERR_INVALID_ARGUMENT;
   if (cudaDeviceSynchronize() != cudaSuccess) return GQA_ERR_LAUNCH;

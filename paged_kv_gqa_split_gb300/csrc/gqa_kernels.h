@@ -75,6 +75,33 @@ int decode_in_scratch(const void* q, const void* k_cache, const void* v_cache, c
                       const int* kv_indices, float sm_scale, void* out, float* lse, int batch, cudaStream_t stream,
                       void* scratch, size_t scratch_bytes);
 
+// Dense MLA decode (gqa_mla.cu): one latent KV head of 576 values per token,
+// 512 of them also V; `rows` = s_q * h_q query rows per sequence, a multiple
+// of 16. The prep kernels fill kv_indptr_mut / slots_mut (workspace) from
+// cache_seqlens and the block table; the decode and merge read them.
+struct MlaParams {
+  const void* q;             // [B][rows][576] bf16
+  const void* kv;            // [num_blocks * page_size][576] bf16 (the cache, slot-major)
+  const int* kv_indptr;      // [B + 1]
+  int* kv_indptr_mut;        // the same buffer, written by the scan
+  const int* slots;          // [T] slot of every cached token, -1 outside the pool
+  int* slots_mut;
+  void* out;                 // [B][rows][512] bf16
+  float* lse;                // [B][h_q][s_q] fp32 natural log, or NULL
+  float* part_o;             // [2 * CTAs][16][512] fp32
+  float* part_lse;           // [2 * CTAs][16] fp32 (base 2)
+  int4* split_rec;           // [2 * CTAs]
+  int* err;
+  PlanConfig plan;
+  unsigned long long epoch;
+  int batch, rows, h_q, s_q;
+  float scale_log2;
+};
+
+int mla_smem_bytes();
+cudaError_t launch_mla(const MlaParams& p, const int* cache_seqlens, const int* block_table, int width,
+                       int page_size, int num_blocks, int sm_count, cudaStream_t stream);
+
 // Compile-time variant of the decode kernel.
 enum : int { kGatherLsu = 0, kGatherTma = 1, kGatherLsuF8 = 2 };  // kGatherLsuF8: FP8 caches only
 

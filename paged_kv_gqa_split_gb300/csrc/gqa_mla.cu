@@ -1,0 +1,530 @@
+// Dense MLA paged decode: one latent KV head, d_qk = 576 (512 "NoPE" + 64
+// "RoPE" values per token), d_v = 512 (the NoPE part is also V), the dense
+// decode of the flash_mla_with_kvcache page (docs.flagos.io, FlagGems;
+// _dense_decode_dispatch): for every query row (query token i, head h) of
+// sequence b, s_t = scale * q . kv_t over all 576 values, O = softmax(s) .
+// kv[:, :512] (bf16) and lse = log sum exp(s) (natural log, stored
+// [B][h_q][s_q]); a sequence with no cached token gives O = 0, lse = -inf.
+//
+// GB300 mapping. Two prep kernels turn cache_seqlens and the block table into
+// the dense path's CSR form (kv_indptr, and one flat slot per cached token:
+// block * page_size + offset, -1 when the table points outside the pool), so
+// the dense path's two-tier split plan, walker, split records and tiers
+// apply unchanged; the unit is one cached token for one group of 16 query
+// rows. A decode CTA has 4 warps that share 16-token tiles of 1152-byte
+// latent rows (gathered with 16-byte cp.async into a 4-deep ring at a
+// 1168-byte pitch) and compute:
+//   S = Q K^T: each warp contracts 144 of the 576 dims (its Q fragments stay
+//     in registers), the 4 partial 16 x 16 score tiles are summed through
+//     shared memory, so every warp holds the full tile in the mma accumulator
+//     layout, which is also P's A-fragment layout;
+//   online softmax in base 2, identical in every warp;
+//   O += P V: each warp owns 128 of the 512 output dims (V fragments by
+//     ldmatrix.trans from the same latent rows).
+// Pieces of a sequence cut across CTAs leave fp32 partials [16 rows][512]
+// that gqa_mla_merge_kernel combines.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gqa_common.cuh"
+#include "gqa_kernels.h"
+
+namespace gqa {
+
+constexpr int kMlaDqk = 576;
+constexpr int kMlaDv = 512;
+constexpr int kMlaRows = 16;                       // query rows per row group (one m16 tile)
+constexpr int kMlaTile = 16;                       // tokens per stage
+constexpr int kMlaStages = 4;
+constexpr int kMlaWarps = 4;
+constexpr int kMlaThreads = kMlaWarps * 32;
+constexpr int kMlaRowBytes = kMlaDqk * 2;          // 1152
+constexpr int kMlaPitch = kMlaRowBytes + 16;       // 1168: 73 16-byte groups, so 8 rows hit 8 bank groups
+constexpr int kMlaChunks = kMlaRowBytes / 16;      // 72 16-byte copies per row
+constexpr int kMlaKSteps = kMlaDqk / kMlaWarps / 16;  // 9 k-steps of 16 dims per warp (144 dims)
+constexpr int kMlaVDims = kMlaDv / kMlaWarps;      // 128 output dims per warp
+constexpr int kMlaIdsRing = 256;
+constexpr int kMlaStageBytes = kMlaTile * kMlaPitch;                       // 18,688
+constexpr int kMlaHdrOff = kMlaStages * kMlaStageBytes;                   // tile headers: 32 B per stage
+constexpr int kMlaSpartOff = kMlaHdrOff + kMlaStages * 32;                // [warp][lane][8] fp32 partial scores
+constexpr int kMlaIdsOff = kMlaSpartOff + kMlaWarps * 32 * 8 * 4;         // per-warp slot rings
+constexpr int kMlaPlanOff = kMlaIdsOff + kMlaWarps * kMlaIdsRing * 4;     // per-warp plan copies
+constexpr int kMlaSmemBytes = kMlaPlanOff + kMlaWarps * 32;
+static_assert(kMlaSmemBytes <= 113 * 1024, "two MLA CTAs per SM");
+
+struct MlaSmemPlan {
+  int64_t W1, q1, q2;
+  int P1, unused;
+};
+
+// ------------------------------------------------------------------ prep
+// kv_indptr = exclusive prefix sum of the lengths, each clamped to [0, cap]
+// (cap = the block table's width * page_size: tokens past the table have no
+// block, and the slot buffer holds batch * cap entries); one CTA.
+__global__ void __launch_bounds__(1024) gqa_mla_scan_kernel(const int* __restrict__ seqlens, int batch, int cap,
+                                                            int* __restrict__ indptr) {
+  __shared__ int warp_sum[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (batch + 1023) / 1024;
+  const int lo = tid * per, hi = min(batch, lo + per);
+  int mine = 0;
+  for (int i = lo; i < hi; ++i) mine += min(max(__ldg(seqlens + i), 0), cap);
+  int x = mine;  // inclusive warp scan of the chunk sums
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int v = warp_sum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    warp_sum[lane] = v;
+  }
+  __syncthreads();
+  int run = x - mine + (warp > 0 ? warp_sum[warp - 1] : 0);  // exclusive prefix of this chunk
+  for (int i = lo; i < hi; ++i) {
+    indptr[i] = run;
+    run += min(max(__ldg(seqlens + i), 0), cap);
+  }
+  if (tid == 1023) indptr[batch] = warp_sum[31];
+}
+
+// slots[indptr[b] + t] = block_table[b, t / page_size] * page_size + t % page_size, or -1.
+__global__ void __launch_bounds__(256) gqa_mla_fill_kernel(const int* __restrict__ indptr,
+                                                           const int* __restrict__ block_table, int batch,
+                                                           int width, int page_size, int num_blocks,
+                                                           int* __restrict__ slots) {
+  for (int b = blockIdx.x; b < batch; b += gridDim.x) {
+    const int base = __ldg(indptr + b), n = __ldg(indptr + b + 1) - base;
+    for (int t = threadIdx.x; t < n; t += blockDim.x) {
+      const int lp = t / page_size;
+      int slot = -1;
+      if (lp < width) {
+        const int page = __ldg(block_table + static_cast<int64_t>(b) * width + lp);
+        if (page >= 0 && page < num_blocks) slot = page * page_size + (t - lp * page_size);
+      }
+      slots[base + t] = slot;
+    }
+  }
+}
+
+// --------------------------------------------------------------- decode
+__device__ __forceinline__ SeqSplit mla_seq_split(const MlaSmemPlan* sp, int64_t u_lo, int64_t u_hi) {
+  Plan pl;
+  pl.W1 = sp->W1;
+  pl.q1 = sp->q1;
+  pl.q2 = sp->q2;
+  pl.P1 = sp->P1;
+  return seq_split(pl, u_lo, u_hi);
+}
+
+__device__ __forceinline__ void mla_write_rec(int4* rec, int cta, unsigned long long epoch, int b, int hg,
+                                              const SplitInfo& si) {
+  // same record as the dense path, with up to 2^24 row groups
+  rec[cta] = make_int4(static_cast<int>(static_cast<unsigned>(epoch)), b, si.first_cta, si.S);
+  rec[gridDim.x + cta] = make_int4(hg, si.first_slot, 0, 0);
+}
+
+__global__ void __launch_bounds__(kMlaThreads, 2) gqa_mla_decode_kernel(const MlaParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const uint32_t sbase = smem_addr(smem);
+  const int* ids = reinterpret_cast<const int*>(smem + kMlaIdsOff + w * kMlaIdsRing * 4);
+  const uint32_t ids_base = sbase + kMlaIdsOff + w * kMlaIdsRing * 4;
+
+  pdl_launch_dependents();
+  const uint8_t* __restrict__ kv = static_cast<const uint8_t*>(p.kv);
+  const __nv_bfloat16* __restrict__ qg = static_cast<const __nv_bfloat16*>(p.q);
+  const int B = p.batch;
+  const int T = __ldg(p.kv_indptr + B);
+  const int HG = p.rows / kMlaRows;
+  MlaSmemPlan* splan = reinterpret_cast<MlaSmemPlan*>(smem + kMlaPlanOff + w * 32);
+  int64_t u0, u1;
+  {
+    const Plan pl = make_plan(static_cast<int64_t>(T) * HG, p.plan);
+    u0 = pl.begin(blockIdx.x);
+    u1 = pl.end(blockIdx.x);
+    if (lane == 0) *splan = MlaSmemPlan{pl.W1, pl.q1, pl.q2, pl.P1, 0};
+    __syncwarp();
+  }
+
+  // ------------------------------------------ walker (the same in every warp)
+  int64_t u_next = u0;
+  bool seg_open = false, walk_ok = true;
+  int hg = 0, tt = 0, t_stop = 0;
+  int p_hi = 0, p_flags = 0, pb = 0;
+  SplitInfo p_si = {1, 0, 0};
+  int wb = 0, win = 0, ib = 0;
+  auto request_ids = [&](int pos) {
+    cp_async_4(ids_base + (pos & (kMlaIdsRing - 1)) * 4, p.slots + min(pos, T - 1), pos < T ? 4u : 0u);
+  };
+  struct MTile {
+    int b, cnt, flags, hg, tt;
+    SplitInfo si;
+  };
+  auto next_tile = [&](MTile& tl) -> bool {
+    while (walk_ok) {
+      if (seg_open && tt < t_stop) {
+        if (tt >= p_hi) {
+          unsigned m;
+          for (;;) {
+            m = __ballot_sync(0xffffffffu, win <= tt);
+            if (m != 0xffffffffu) break;
+            wb += 31;
+            win = load_indptr_window(p.kv_indptr, B, wb, lane);
+          }
+          if (m == 0) {
+            if (lane == 0) atomicOr(p.err, kErrBadIndptr);
+            walk_ok = false;
+            break;
+          }
+          const int k = 31 - __clz(m);
+          pb = wb + k;
+          const int seq_lo = __shfl_sync(0xffffffffu, win, k);
+          const int seq_hi = __shfl_sync(0xffffffffu, win, k + 1);
+          p_hi = min(seq_hi, t_stop);
+          p_flags = F_QLOAD | ((tt == seq_lo && p_hi == seq_hi) ? F_FINAL : 0) |
+                    ((static_cast<int64_t>(hg) * T + tt != u0) ? F_SLOT1 : 0);
+          const int64_t base_u = static_cast<int64_t>(hg) * T;
+          const SeqSplit sp = mla_seq_split(splan, base_u + seq_lo, base_u + seq_hi);
+          p_si.S = static_cast<int>(sp.last_cta - sp.first_cta + 1);
+          p_si.first_cta = static_cast<int>(sp.first_cta);
+          p_si.first_slot = sp.first_slot;
+        }
+        tl.cnt = min(kMlaTile, p_hi - tt);
+        tl.flags = p_flags | ((tt + tl.cnt == p_hi) ? F_END : 0);
+        tl.b = pb;
+        tl.hg = hg;
+        tl.tt = tt;
+        tl.si = p_si;
+        p_flags &= ~F_QLOAD;
+        tt += tl.cnt;
+        return true;
+      }
+      if (u_next >= u1) return false;
+      hg = static_cast<int>(u_next / T);
+      tt = static_cast<int>(u_next - static_cast<int64_t>(hg) * T);
+      t_stop = static_cast<int>(min(static_cast<int64_t>(T), u1 - static_cast<int64_t>(hg) * T));
+      u_next = static_cast<int64_t>(hg) * T + t_stop;
+      seg_open = true;
+      p_hi = tt;
+      ib = tt & ~31;
+#pragma unroll
+      for (int cc = 0; cc < kMlaIdsRing / 32; ++cc) request_ids(ib + 32 * cc + lane);
+      cp_async_commit();
+      wb = warp_find_seq(p.kv_indptr, B, tt, lane);
+      if (wb >= 0) win = load_indptr_window(p.kv_indptr, B, wb, lane);
+      cp_async_wait<0>();
+      __syncwarp();
+      if (wb < 0) {
+        if (lane == 0) atomicOr(p.err, kErrBadIndptr);
+        walk_ok = false;
+        break;
+      }
+    }
+    return false;
+  };
+
+  // ------------------------------------------------------------- issue
+  int issued = 0;
+  bool more = true;
+  auto issue = [&]() {
+    const int stage = issued % kMlaStages;
+    const uint32_t sb = sbase + stage * kMlaStageBytes;
+    MTile tl;
+    if (more && next_tile(tl)) {
+      while (tl.tt >= ib + 32) {
+        request_ids(ib + kMlaIdsRing + lane);
+        ib += 32;
+      }
+      // 16 rows x 72 chunks: thread tid copies chunks tid, tid + 128, ...
+#pragma unroll
+      for (int k = 0; k < kMlaTile * kMlaChunks / kMlaThreads; ++k) {
+        const int i = tid + kMlaThreads * k;
+        const int row = i / kMlaChunks, ch = i - row * kMlaChunks;
+        int slot = row < tl.cnt ? ids[(tl.tt + row) & (kMlaIdsRing - 1)] : -1;
+        const bool valid = slot >= 0;
+        const uint8_t* src = kv + static_cast<int64_t>(valid ? slot : 0) * kMlaRowBytes + ch * 16;
+        cp_async_16(sb + row * kMlaPitch + ch * 16, src, valid ? 16u : 0u);
+      }
+      if (tid == 0) {
+        // rows that enter the softmax: the first cnt, less those whose slot is -1
+        unsigned mask = 0;
+        for (int r = 0; r < tl.cnt; ++r) mask |= (ids[(tl.tt + r) & (kMlaIdsRing - 1)] >= 0 ? 1u : 0u) << r;
+        const uint32_t hdr = sbase + kMlaHdrOff + stage * 32;
+        st_shared_v4(hdr, tl.b, tl.cnt, tl.flags, tl.hg);
+        st_shared_v4(hdr + 16, tl.si.S, tl.si.first_cta, tl.si.first_slot, static_cast<int>(mask));
+      }
+      if ((tl.flags & F_QLOAD) && lane < 16) {  // the piece's Q rows toward L2 for its first tile
+        const __nv_bfloat16* qr = qg + (static_cast<int64_t>(tl.b) * p.rows + tl.hg * kMlaRows) * kMlaDqk;
+        for (int x = lane + 16 * w; x < kMlaRows * kMlaRowBytes / 128; x += 64) prefetch_l2(qr + x * 64);
+      }
+    } else if (more) {
+      more = false;
+      if (tid == 0) st_shared_v4(sbase + kMlaHdrOff + stage * 32, 0, 0, F_DONE, 0);
+    }
+    cp_async_commit();
+    ++issued;
+  };
+
+  // ----------------------------------------------------------- compute
+  uint32_t qa[kMlaKSteps][4];  // Q A-fragments: rows g / g+8, dims 144 w + 16 ks + {2c, 2c+8} (+1)
+  float acc[kMlaVDims / 8][4];  // O rows g / g+8, dims 128 w + 8 nt + 2c (+1)
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < kMlaVDims / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  // per-lane ldmatrix addresses inside a stage
+  const int mk = lane >> 3;
+  const uint32_t k_lane = ((mk >> 1) * 8 + (lane & 7)) * kMlaPitch + (w * 144 + (mk & 1) * 8) * 2;
+  const uint32_t v_lane = ((mk & 1) * 8 + (lane & 7)) * kMlaPitch + (w * kMlaVDims + (mk >> 1) * 8) * 2;
+  float* spart = reinterpret_cast<float*>(smem + kMlaSpartOff);
+
+#pragma unroll 1
+  for (int i = 0; i < kMlaStages - 1; ++i) issue();
+#pragma unroll 1
+  for (int k = 0;; ++k) {
+    cp_async_wait<kMlaStages - 2>();  // this thread's copies of tile k have landed
+    __syncthreads();                  // everyone's have, and everyone is done with tile k - 1
+    issue();                          // tile k + 3 into the stage tile k - 1 used
+    const int stage = k % kMlaStages;
+    const uint32_t sb = sbase + stage * kMlaStageBytes;
+    int hb, cnt, flags, thg, unused_s, unused_f, unused_fs, mask;
+    ld_shared_v4(sbase + kMlaHdrOff + stage * 32, hb, cnt, flags, thg);
+    ld_shared_v4(sbase + kMlaHdrOff + stage * 32 + 16, unused_s, unused_f, unused_fs, mask);
+    if (flags & F_DONE) break;
+    if (flags & F_QLOAD) {
+      const __nv_bfloat16* qr = qg + (static_cast<int64_t>(hb) * p.rows + thg * kMlaRows) * kMlaDqk;
+#pragma unroll
+      for (int ks = 0; ks < kMlaKSteps; ++ks) {
+        const int d = w * 144 + ks * 16 + 2 * c;
+        qa[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qr + g * kMlaDqk + d));
+        qa[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qr + (g + 8) * kMlaDqk + d));
+        qa[ks][2] = __ldg(reinterpret_cast<const uint32_t*>(qr + g * kMlaDqk + d + 8));
+        qa[ks][3] = __ldg(reinterpret_cast<const uint32_t*>(qr + (g + 8) * kMlaDqk + d + 8));
+      }
+      m0 = m1 = -INFINITY;
+      l0 = l1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < kMlaVDims / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    }
+    // partial scores of this warp's 144 dims: tokens 0-7 (s[0..3]) and 8-15 (s[4..7])
+    float sl[4] = {0.f, 0.f, 0.f, 0.f}, sh[4] = {0.f, 0.f, 0.f, 0.f};  // tokens 0-7 / 8-15
+#pragma unroll
+    for (int ks = 0; ks < kMlaKSteps; ++ks) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(sb + k_lane + ks * 32, b0, b1, b2, b3);
+      mma_bf16_16816(sl, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+      mma_bf16_16816(sh, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+    }
+    float4* my = reinterpret_cast<float4*>(spart + (w * 32 + lane) * 8);
+    my[0] = make_float4(sl[0], sl[1], sl[2], sl[3]);
+    my[1] = make_float4(sh[0], sh[1], sh[2], sh[3]);
+    __syncthreads();
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ww = 0; ww < kMlaWarps; ++ww) {
+      const float4* o = reinterpret_cast<const float4*>(spart + (ww * 32 + lane) * 8);
+      const float4 x = o[0], y = o[1];
+      s[0] += x.x; s[1] += x.y; s[2] += x.z; s[3] += x.w;
+      s[4] += y.x; s[5] += y.y; s[6] += y.z; s[7] += y.w;
+    }
+    // scale, mask (tokens 2c, 2c + 1, 8 + 2c, 9 + 2c), online softmax in base 2 (rows g: s0,1,4,5; g+8: s2,3,6,7)
+    const unsigned um = static_cast<unsigned>(mask);
+    const int tk[4] = {2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool ok = (um >> tk[j]) & 1u;
+      const int ia = j < 2 ? j : 2 + j;      // row g entry of token tk[j]
+      const int ib2 = ia + 2;                // row g + 8 entry
+      s[ia] = ok ? s[ia] * p.scale_log2 : -INFINITY;
+      s[ib2] = ok ? s[ib2] * p.scale_log2 : -INFINITY;
+    }
+    float mx0 = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[4], s[5]));
+    float mx1 = fmaxf(fmaxf(s[2], s[3]), fmaxf(s[6], s[7]));
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float sh0 = mn0 == -INFINITY ? 0.f : mn0, sh1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float a0 = ex2(m0 - sh0), a1 = ex2(m1 - sh1);
+    m0 = mn0;
+    m1 = mn1;
+    float pr[8];
+    pr[0] = ex2(s[0] - sh0); pr[1] = ex2(s[1] - sh0); pr[4] = ex2(s[4] - sh0); pr[5] = ex2(s[5] - sh0);
+    pr[2] = ex2(s[2] - sh1); pr[3] = ex2(s[3] - sh1); pr[6] = ex2(s[6] - sh1); pr[7] = ex2(s[7] - sh1);
+    l0 = l0 * a0 + (pr[0] + pr[1] + pr[4] + pr[5]);
+    l1 = l1 * a1 + (pr[2] + pr[3] + pr[6] + pr[7]);
+    const uint32_t pa0 = pack_bf16(pr[0], pr[1]), pa1 = pack_bf16(pr[2], pr[3]);
+    const uint32_t pa2 = pack_bf16(pr[4], pr[5]), pa3 = pack_bf16(pr[6], pr[7]);
+#pragma unroll
+    for (int np = 0; np < kMlaVDims / 16; ++np) {
+      uint32_t v0, v1, v2, v3;
+      ldsm_x4_trans(sb + v_lane + np * 32, v0, v1, v2, v3);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float* a = acc[2 * np + h];
+        a[0] *= a0; a[1] *= a0; a[2] *= a1; a[3] *= a1;
+      }
+      mma_bf16_16816(acc[2 * np], pa0, pa1, pa2, pa3, v0, v1);
+      mma_bf16_16816(acc[2 * np + 1], pa0, pa1, pa2, pa3, v2, v3);
+    }
+    if (flags & F_END) {
+      SplitInfo si;
+      int dummy;
+      ld_shared_v4(sbase + kMlaHdrOff + stage * 32 + 16, si.S, si.first_cta, si.first_slot, dummy);
+      float lt0 = l0, lt1 = l1;
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
+        lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
+      }
+      const float i0 = lt0 > 0.f ? 1.f / lt0 : 0.f, i1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
+      const float lse0 = lt0 > 0.f ? m0 + log2f(lt0) : -INFINITY;  // base 2
+      const float lse1 = lt1 > 0.f ? m1 + log2f(lt1) : -INFINITY;
+      const int r0 = thg * kMlaRows + g, r1 = r0 + 8;  // query rows (i * h_q + h) of sequence hb
+      if (flags & F_FINAL) {
+        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(hb) * p.rows * kMlaDv;
+#pragma unroll
+        for (int nt = 0; nt < kMlaVDims / 8; ++nt) {
+          const int d = w * kMlaVDims + nt * 8 + 2 * c;
+          *reinterpret_cast<uint32_t*>(ob + static_cast<int64_t>(r0) * kMlaDv + d) = pack_bf16(acc[nt][0] * i0, acc[nt][1] * i0);
+          *reinterpret_cast<uint32_t*>(ob + static_cast<int64_t>(r1) * kMlaDv + d) = pack_bf16(acc[nt][2] * i1, acc[nt][3] * i1);
+        }
+        if (w == 0 && c == 0 && p.lse != nullptr) {  // natural log, [B][h_q][s_q]
+          const float ln2 = 0.6931471805599453f;
+          p.lse[static_cast<int64_t>(hb) * p.rows + (r0 % p.h_q) * p.s_q + r0 / p.h_q] = lse0 * ln2;
+          p.lse[static_cast<int64_t>(hb) * p.rows + (r1 % p.h_q) * p.s_q + r1 / p.h_q] = lse1 * ln2;
+        }
+      } else {
+        const int64_t sid = slot_id(blockIdx.x, (flags & F_SLOT1) ? 1 : 0);
+        float* po = p.part_o + sid * (kMlaRows * kMlaDv);
+#pragma unroll
+        for (int nt = 0; nt < kMlaVDims / 8; ++nt) {
+          const int d = w * kMlaVDims + nt * 8 + 2 * c;
+          *reinterpret_cast<float2*>(po + g * kMlaDv + d) = make_float2(acc[nt][0] * i0, acc[nt][1] * i0);
+          *reinterpret_cast<float2*>(po + (g + 8) * kMlaDv + d) = make_float2(acc[nt][2] * i1, acc[nt][3] * i1);
+        }
+        if (w == 0 && c == 0) {
+          p.part_lse[sid * kMlaRows + g] = lse0;
+          p.part_lse[sid * kMlaRows + g + 8] = lse1;
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+  if (tid == 0 && u0 < u1 && walk_ok) mla_write_rec(p.split_rec, blockIdx.x, p.epoch, pb, hg, p_si);
+}
+
+// ---------------------------------------------------------------- merge
+// One CTA per boundary between decode CTAs j and j + 1, as for the dense
+// path: it finds the sequence cut there from CTA j's record and, being rank
+// r of its S - 1 boundary CTAs, merges a share of the 512 output dims of the
+// 16 rows over all S pieces (running max; lanes over 4-dim columns, threads
+// over rows). It also writes the empty sequences.
+__global__ void __launch_bounds__(128) gqa_mla_merge_kernel(const MlaParams p) {
+  const int tid = threadIdx.x;
+  const int B = p.batch;
+  const int j = blockIdx.x;
+  const bool boundary = j + 1 < p.plan.tier1_ctas + p.plan.tier2_ctas;
+  const int T = __ldg(p.kv_indptr + B);
+  pdl_wait();
+  const int4 rec0 = boundary ? __ldcg(p.split_rec + j) : make_int4(0, 0, 0, 0);
+  const int4 rec1 = boundary ? __ldcg(p.split_rec + (p.plan.tier1_ctas + p.plan.tier2_ctas) + j)
+                             : make_int4(0, 0, 0, 0);
+  for (int b = j; b < B; b += gridDim.x) {  // empty sequences: O = 0, LSE = -inf
+    if (__ldg(p.kv_indptr + b) == __ldg(p.kv_indptr + b + 1)) {
+      uint4* ob = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(b) * p.rows * kMlaDv);
+      for (int i = tid; i < p.rows * kMlaDv * 2 / 16; i += 128) ob[i] = make_uint4(0, 0, 0, 0);
+      if (p.lse != nullptr)
+        for (int i = tid; i < p.rows; i += 128) p.lse[static_cast<int64_t>(b) * p.rows + i] = -INFINITY;
+    }
+  }
+  const int HG = p.rows / kMlaRows;
+  const Plan pl = make_plan(static_cast<int64_t>(T) * HG, p.plan);
+  if (!boundary || pl.begin(j + 1) >= pl.W) return;
+  if (static_cast<unsigned>(rec0.x) != static_cast<unsigned>(p.epoch)) return;
+  const int b = rec0.y, S = rec0.w, hg = rec1.x;
+  SeqSplit sp;
+  sp.first_cta = rec0.z;
+  sp.first_slot = rec1.y;
+  sp.last_cta = sp.first_cta + S - 1;
+  if (b < 0 || b >= B || hg < 0 || hg >= HG || S < 2 || sp.first_cta > j || sp.last_cta <= j) return;
+  const int rank = j - static_cast<int>(sp.first_cta), nranks = S - 1;
+  const int row = tid >> 3, col = tid & 7;  // 16 rows x 8 columns of 4 dims
+  const int per = ((kMlaDv / 32 + nranks - 1) / nranks) * 32;  // dims per rank, a multiple of 32
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) +
+                      (static_cast<int64_t>(b) * p.rows + hg * kMlaRows + row) * kMlaDv;
+  for (int d0 = rank * per; d0 < min(kMlaDv, (rank + 1) * per); d0 += 32) {
+    const int d = d0 + 4 * col;
+    float m = -INFINITY, den = 0.f, a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int s = 0; s < S; ++s) {
+      const int64_t sid = slot_id(sp.first_cta + s, s == 0 ? sp.first_slot : 0);
+      const float l = __ldcg(p.part_lse + sid * kMlaRows + row);
+      const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + (sid * kMlaRows + row) * kMlaDv + d));
+      const float mn = fmaxf(m, l);
+      if (mn == -INFINITY) continue;
+      const float sc = ex2(m - mn), wt = ex2(l - mn);
+      den = den * sc + wt;
+      a[0] = a[0] * sc + wt * o.x;
+      a[1] = a[1] * sc + wt * o.y;
+      a[2] = a[2] * sc + wt * o.z;
+      a[3] = a[3] * sc + wt * o.w;
+      m = mn;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    *reinterpret_cast<uint2*>(ob + d) = make_uint2(pack_bf16(a[0] * inv, a[1] * inv), pack_bf16(a[2] * inv, a[3] * inv));
+    if (d == 0 && p.lse != nullptr) {
+      const int r = hg * kMlaRows + row;
+      p.lse[static_cast<int64_t>(b) * p.rows + (r % p.h_q) * p.s_q + r / p.h_q] =
+          den > 0.f ? (m + log2f(den)) * 0.6931471805599453f : -INFINITY;
+    }
+  }
+}
+
+// --------------------------------------------------------------- launch
+int mla_smem_bytes() { return kMlaSmemBytes; }
+
+cudaError_t launch_mla(const MlaParams& p, const int* cache_seqlens, const int* block_table, int width,
+                       int page_size, int num_blocks, int sm_count, cudaStream_t stream) {
+  gqa_mla_scan_kernel<<<1, 1024, 0, stream>>>(cache_seqlens, p.batch, width * page_size, p.kv_indptr_mut);
+  int fill_grid = p.batch < sm_count * 4 ? p.batch : sm_count * 4;
+  if (fill_grid < 1) fill_grid = 1;
+  gqa_mla_fill_kernel<<<fill_grid, 256, 0, stream>>>(p.kv_indptr, block_table, p.batch, width, page_size,
+                                                     num_blocks, p.slots_mut);
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(gqa_mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  const int ctas = p.plan.tier1_ctas + p.plan.tier2_ctas;
+  gqa_mla_decode_kernel<<<ctas, kMlaThreads, kMlaSmemBytes, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas > 1 ? ctas - 1 : 1);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gqa_mla_merge_kernel, p);
+}
+
+}  // namespace gqa

@@ -172,3 +172,21 @@ def test_fp8_wrapper_checks():
     with pytest.raises(ValueError, match="no CPU path"):
         _lib.run_fp8(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices)
     assert w.k_cache.shape[1] == _lib.FP8_ROW_BYTES and w.k_cache.dtype == torch.uint8
+
+
+def test_mla_argument_checks(lib):
+    a = 1 << 20
+    ok = [a, a, a, a, 0.07, a, a, 2, 1, 16, 64, 10, 4, None]
+    assert _lib.gqa_mla_decode(*ok[:7], 0, *ok[8:]) == 0
+    for i, bad in ((7, -1), (8, 0), (9, 12), (10, 0), (11, 0), (12, 0), (0, None), (5, None), (2, None),
+                   (0, a + 8), (6, a + 2), (4, float("nan"))):
+        args = list(ok)
+        args[i] = bad
+        assert _lib.gqa_mla_decode(*args) == _lib.GQA_ERR_INVALID_ARGUMENT, (i, bad)
+
+
+def test_mla_cpu_tensors_raise():
+    from paged_kv_gqa_split_gb300 import workloads as wl
+    w = wl.make_mla_workload([5, 9], 16, 1, 4, seed=1)
+    with pytest.raises(ValueError, match="no CPU path"):
+        _lib.mla_run(w.q, w.kv_cache, w.block_table, w.cache_seqlens)

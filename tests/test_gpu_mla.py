@@ -1,0 +1,94 @@
+"""Dense MLA paged decode on the GPU against the float64 oracle (oracle/mla.py).
+
+The flash_mla_with_kvcache page's dense path: one latent KV head of 576 values
+(512 of them also V), blocks through a block table, natural-log LSE in the
+page's [B, h_q, s_q] layout. Tolerances are the dense path's: |dO| <= 2e-2 +
+2e-2 |O_ref|, |dlse| <= 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.mla as ml
+from paged_kv_gqa_split_gb300 import _lib
+from paged_kv_gqa_split_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+O_ATOL, O_RTOL, LSE_ATOL = 2e-2, 2e-2, 1e-3
+
+
+@pytest.fixture(autouse=True)
+def _defaults(cuda_device):
+    _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0)
+    yield
+    _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0)
+
+
+def gpu_mla(w, with_lse=True):
+    g = w.to("cuda")
+    out, lse = _lib.mla_run(g.q, g.kv_cache, g.block_table, g.cache_seqlens, w.softmax_scale, with_lse=with_lse)
+    torch.cuda.synchronize()
+    return out.float().cpu().double().numpy(), (lse.cpu().double().numpy() if lse is not None else None)
+
+
+def check(w, out, lse, seqs=None):
+    o_ref, l_ref = ml.mla_decode_oracle(w.q, w.kv_cache, w.block_table, w.cache_seqlens, w.softmax_scale, seqs)
+    sel = list(range(w.batch)) if seqs is None else list(seqs)
+    o, orf = out[sel], o_ref[sel]
+    bad = np.abs(o - orf) > O_ATOL + O_RTOL * np.abs(orf)
+    assert not bad.any(), f"{bad.sum()} O elements out of tolerance, max |dO| {np.abs(o - orf).max():.3g}"
+    if lse is not None:
+        l, lrf = lse[sel], l_ref[sel]
+        assert np.array_equal(np.isneginf(l), np.isneginf(lrf))
+        fin = np.isfinite(lrf)
+        assert np.all(np.abs(l[fin] - lrf[fin]) <= LSE_ATOL), np.abs(l[fin] - lrf[fin]).max()
+    empty = np.isneginf(l_ref[sel]).all(axis=(1, 2))
+    assert np.all(o[empty] == 0)
+
+
+@pytest.mark.parametrize("lens,h_q,s_q,ps,seed", [
+    ([1, 0, 17, 64, 65, 300], 16, 1, 64, 1),
+    ([2000, 5, 700], 32, 1, 64, 2),             # two row groups
+    ([900, 33, 0, 128], 16, 2, 16, 3),          # two query tokens per sequence
+    ([500, 77], 8, 2, 1, 4),                    # page size 1, 8 heads x 2 tokens = 16 rows
+    ([4000, 3, 1500], 16, 1, 128, 5),
+    ([6000, 6000], 64, 1, 64, 6),               # rows cut across CTAs in 4 row groups
+])
+def test_mla_matches_oracle(lens, h_q, s_q, ps, seed):
+    w = wl.make_mla_workload(lens, h_q, s_q, ps, seed)
+    out, lse = gpu_mla(w)
+    check(w, out, lse)
+
+
+def test_mla_invalid_blocks_and_long_lengths():
+    w = wl.make_mla_workload([700, 300, 129], 16, 1, 64, seed=11)
+    w.block_table[0, 3] = -1                    # a hole: tokens 192..255 of sequence 0 are left out
+    w.block_table[1, 1] = w.kv_cache.shape[0] + 7
+    w.cache_seqlens[2] = 10 ** 6                # past the table: counts as width * page_size
+    w.lens[2] = 10 ** 6
+    out, lse = gpu_mla(w)
+    check(w, out, lse)
+
+
+@pytest.mark.parametrize("tuning", [(40, 8, 0, 0, 0, 0, 0, 0, 500, 16), (7, 1, 0, 0, 0, 0, 0, 13, 400, 4),
+                                    (300, 1, 0, 0, 0, 0, 0, -1), (1, 0, 0, 0, 0, 0, 0, -1)])
+def test_mla_split_plans(tuning):
+    assert _lib.gqa_paged_decode_set_tuning(*tuning) == 0
+    w = wl.make_mla_workload([3000, 40, 1200, 0, 7], 16, 1, 64, seed=12)
+    out, lse = gpu_mla(w)
+    check(w, out, lse)
+
+
+def test_mla_without_lse():
+    w = wl.make_mla_workload([800, 90], 16, 1, 64, seed=13)
+    out, lse = gpu_mla(w, with_lse=False)
+    assert lse is None
+    check(w, out, None)
+
+
+def test_mla_config_sampled_sequences():
+    w = wl.make_mla_config()
+    out, lse = gpu_mla(w)
+    lens = np.array(w.lens)
+    check(w, out, lse, sorted({0, int(np.argmax(lens)), w.batch // 2, w.batch - 1}))

@@ -146,7 +146,7 @@ def test_pins_catch_planted_mistakes(monkeypatch, slip):
             lse2 = lse2 / math.log(2.0)           # the caller's ln 2 factor then yields log2
         return o, lse2
 
-    def bad_slots(block_table, cache_seqlens, page_size):
+    def bad_slots(block_table, cache_seqlens, page_size, num_blocks=None):
         table = np.asarray(block_table, dtype=np.int64)
         out = []
         for b, n in enumerate(np.asarray(cache_seqlens)):
