@@ -581,7 +581,8 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
     if (rc != GQA_OK) return rc;
     const Tuning& t = g_tune;
     cfg.tier1_ctas = t.num_ctas > 0 ? t.num_ctas : st->sm_count * 2;  // two 4-warp MLA CTAs per SM
-    cfg.tier2_ctas = t.tier2_ctas > 0 ? t.tier2_ctas : (t.tier2_ctas == 0 ? kDefaultTier2PerTier1 * cfg.tier1_ctas : 0);
+    // one tier unless the tuning asks for tier 2: the MLA merge walks a sequence's pieces in turn
+    cfg.tier2_ctas = t.tier2_ctas > 0 ? t.tier2_ctas : 0;
     cfg.min_units = t.min_units > 0 ? t.min_units : kDefaultMinUnits;
     cfg.tier2_permille = t.tier2_permille;
     cfg.tier2_min_units = t.tier2_min_units;

@@ -47,7 +47,8 @@ constexpr int kMlaVDims = kMlaDv / kMlaWarps;      // 128 output dims per warp
 constexpr int kMlaIdsRing = 256;
 constexpr int kMlaStageBytes = kMlaTile * kMlaPitch;                       // 18,688
 constexpr int kMlaHdrOff = kMlaStages * kMlaStageBytes;                   // tile headers: 32 B per stage
-constexpr int kMlaSpartOff = kMlaHdrOff + kMlaStages * 32;                // [warp][lane][8] fp32 partial scores
+constexpr int kMlaValidOff = kMlaHdrOff + kMlaStages * 32;                // per stage: one byte per row (slot >= 0)
+constexpr int kMlaSpartOff = kMlaValidOff + kMlaStages * kMlaTile;        // [warp][half][lane] float4 partial scores
 constexpr int kMlaIdsOff = kMlaSpartOff + kMlaWarps * 32 * 8 * 4;         // per-warp slot rings
 constexpr int kMlaPlanOff = kMlaIdsOff + kMlaWarps * kMlaIdsRing * 4;     // per-warp plan copies
 constexpr int kMlaSmemBytes = kMlaPlanOff + kMlaWarps * 32;
@@ -245,23 +246,24 @@ __global__ void __launch_bounds__(kMlaThreads, 2) gqa_mla_decode_kernel(const Ml
         request_ids(ib + kMlaIdsRing + lane);
         ib += 32;
       }
-      // 16 rows x 72 chunks: thread tid copies chunks tid, tid + 128, ...
-#pragma unroll
-      for (int k = 0; k < kMlaTile * kMlaChunks / kMlaThreads; ++k) {
-        const int i = tid + kMlaThreads * k;
-        const int row = i / kMlaChunks, ch = i - row * kMlaChunks;
-        int slot = row < tl.cnt ? ids[(tl.tt + row) & (kMlaIdsRing - 1)] : -1;
+      // 16 rows x 72 chunks: 8 threads per row, each copying chunks (tid & 7) + 8 k
+      {
+        const int row = tid >> 3;
+        const int slot = row < tl.cnt ? ids[(tl.tt + row) & (kMlaIdsRing - 1)] : -1;
         const bool valid = slot >= 0;
-        const uint8_t* src = kv + static_cast<int64_t>(valid ? slot : 0) * kMlaRowBytes + ch * 16;
-        cp_async_16(sb + row * kMlaPitch + ch * 16, src, valid ? 16u : 0u);
+        const uint8_t* src = kv + static_cast<int64_t>(valid ? slot : 0) * kMlaRowBytes + (tid & 7) * 16;
+        const uint32_t dst = sb + row * kMlaPitch + (tid & 7) * 16;
+#pragma unroll
+        for (int k = 0; k < kMlaChunks / 8; ++k) cp_async_16(dst + k * 128, src + k * 128, valid ? 16u : 0u);
+        // the row enters the softmax when it is one of the first cnt and its slot is valid
+        if ((tid & 7) == 0)
+          asm volatile("st.shared.u8 [%0], %1;" ::"r"(sbase + kMlaValidOff + stage * kMlaTile + row),
+                       "r"(valid ? 1 : 0) : "memory");
       }
       if (tid == 0) {
-        // rows that enter the softmax: the first cnt, less those whose slot is -1
-        unsigned mask = 0;
-        for (int r = 0; r < tl.cnt; ++r) mask |= (ids[(tl.tt + r) & (kMlaIdsRing - 1)] >= 0 ? 1u : 0u) << r;
         const uint32_t hdr = sbase + kMlaHdrOff + stage * 32;
         st_shared_v4(hdr, tl.b, tl.cnt, tl.flags, tl.hg);
-        st_shared_v4(hdr + 16, tl.si.S, tl.si.first_cta, tl.si.first_slot, static_cast<int>(mask));
+        st_shared_v4(hdr + 16, tl.si.S, tl.si.first_cta, tl.si.first_slot, 0);
       }
       if ((tl.flags & F_QLOAD) && lane < 16) {  // the piece's Q rows toward L2 for its first tile
         const __nv_bfloat16* qr = qg + (static_cast<int64_t>(tl.b) * p.rows + tl.hg * kMlaRows) * kMlaDqk;
@@ -296,10 +298,13 @@ __global__ void __launch_bounds__(kMlaThreads, 2) gqa_mla_decode_kernel(const Ml
     issue();                          // tile k + 3 into the stage tile k - 1 used
     const int stage = k % kMlaStages;
     const uint32_t sb = sbase + stage * kMlaStageBytes;
-    int hb, cnt, flags, thg, unused_s, unused_f, unused_fs, mask;
+    int hb, cnt, flags, thg;
     ld_shared_v4(sbase + kMlaHdrOff + stage * 32, hb, cnt, flags, thg);
-    ld_shared_v4(sbase + kMlaHdrOff + stage * 32 + 16, unused_s, unused_f, unused_fs, mask);
     if (flags & F_DONE) break;
+    // validity of this lane's tokens 2c, 2c + 1, 8 + 2c, 9 + 2c (one byte per row)
+    const uint8_t* vrow = smem + kMlaValidOff + stage * kMlaTile;
+    const unsigned mask = (vrow[2 * c] ? 1u : 0u) << (2 * c) | (vrow[2 * c + 1] ? 1u : 0u) << (2 * c + 1) |
+                          (vrow[8 + 2 * c] ? 1u : 0u) << (8 + 2 * c) | (vrow[9 + 2 * c] ? 1u : 0u) << (9 + 2 * c);
     if (flags & F_QLOAD) {
       const __nv_bfloat16* qr = qg + (static_cast<int64_t>(hb) * p.rows + thg * kMlaRows) * kMlaDqk;
 #pragma unroll
@@ -324,20 +329,20 @@ __global__ void __launch_bounds__(kMlaThreads, 2) gqa_mla_decode_kernel(const Ml
       mma_bf16_16816(sl, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
       mma_bf16_16816(sh, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
     }
-    float4* my = reinterpret_cast<float4*>(spart + (w * 32 + lane) * 8);
+    float4* my = reinterpret_cast<float4*>(spart) + w * 64 + lane;  // [warp][half][lane]: 16-byte lane stride
     my[0] = make_float4(sl[0], sl[1], sl[2], sl[3]);
-    my[1] = make_float4(sh[0], sh[1], sh[2], sh[3]);
+    my[32] = make_float4(sh[0], sh[1], sh[2], sh[3]);
     __syncthreads();
     float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ww = 0; ww < kMlaWarps; ++ww) {
-      const float4* o = reinterpret_cast<const float4*>(spart + (ww * 32 + lane) * 8);
-      const float4 x = o[0], y = o[1];
+      const float4* o = reinterpret_cast<const float4*>(spart) + ww * 64 + lane;
+      const float4 x = o[0], y = o[32];
       s[0] += x.x; s[1] += x.y; s[2] += x.z; s[3] += x.w;
       s[4] += y.x; s[5] += y.y; s[6] += y.z; s[7] += y.w;
     }
     // scale, mask (tokens 2c, 2c + 1, 8 + 2c, 9 + 2c), online softmax in base 2 (rows g: s0,1,4,5; g+8: s2,3,6,7)
-    const unsigned um = static_cast<unsigned>(mask);
+    const unsigned um = mask;
     const int tk[4] = {2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -366,15 +371,16 @@ __global__ void __launch_bounds__(kMlaThreads, 2) gqa_mla_decode_kernel(const Ml
     l1 = l1 * a1 + (pr[2] + pr[3] + pr[6] + pr[7]);
     const uint32_t pa0 = pack_bf16(pr[0], pr[1]), pa1 = pack_bf16(pr[2], pr[3]);
     const uint32_t pa2 = pack_bf16(pr[4], pr[5]), pa3 = pack_bf16(pr[6], pr[7]);
+    if (!__all_sync(0xffffffffu, a0 == 1.f && a1 == 1.f)) {  // some row's max moved: rescale O
+#pragma unroll
+      for (int nt = 0; nt < kMlaVDims / 8; ++nt) {
+        acc[nt][0] *= a0; acc[nt][1] *= a0; acc[nt][2] *= a1; acc[nt][3] *= a1;
+      }
+    }
 #pragma unroll
     for (int np = 0; np < kMlaVDims / 16; ++np) {
       uint32_t v0, v1, v2, v3;
       ldsm_x4_trans(sb + v_lane + np * 32, v0, v1, v2, v3);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float* a = acc[2 * np + h];
-        a[0] *= a0; a[1] *= a0; a[2] *= a1; a[3] *= a1;
-      }
       mma_bf16_16816(acc[2 * np], pa0, pa1, pa2, pa3, v0, v1);
       mma_bf16_16816(acc[2 * np + 1], pa0, pa1, pa2, pa3, v2, v3);
     }
