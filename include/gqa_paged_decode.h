@@ -232,6 +232,16 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
                    int num_blocks, int page_table_width, struct CUstream_st* stream);
 
 /*
+ * Tuning of gqa_mla_decode for tests and benchmarks (process-wide): the ring
+ * depth of its decode kernel, 3 (three CTAs per SM) or 4 (two CTAs per SM);
+ * 0 restores the default (3). The tier settings of
+ * gqa_paged_decode_set_tuning (tier-1 CTAs, smallest share, tier 2) apply to
+ * gqa_mla_decode as well; with num_ctas 0 it takes one CTA per resident slot.
+ * Returns GQA_ERR_INVALID_ARGUMENT for another value.
+ */
+int gqa_mla_set_tuning(int stages);
+
+/*
  * Selected-token (sparse) paged GQA decode: the sparse split-K GQA path of
  * the sigit.si vLLM "qsa.py" page (qsa_sparse_paged_attention and its
  * _qsa_sparse_paged_gqa_splitk_kernel), for 32 query heads over 4 KV heads

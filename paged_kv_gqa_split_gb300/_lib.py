@@ -47,6 +47,7 @@ _SIGNATURES = {
     "gqa_sparse_paged_decode": (ctypes.c_int, [_vp] * 6 + [ctypes.c_float, _vp, _vp] + [ctypes.c_int] * 6 + [_vp]),
     "gqa_paged_decode_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_int, _vp]),
     "gqa_mla_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp] + [ctypes.c_int] * 6 + [_vp]),
+    "gqa_mla_set_tuning": (ctypes.c_int, [ctypes.c_int]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -401,6 +402,11 @@ def run_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, kv_in
 
 
 MLA_D_QK, MLA_D_V = 576, 512
+
+
+def gqa_mla_set_tuning(stages: int) -> int:
+    """Ring depth of the MLA decode kernel: 3 or 4, 0 for the default."""
+    return load().gqa_mla_set_tuning(stages)
 
 
 def gqa_mla_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale, out, lse, batch, s_q, h_q, page_size,

@@ -53,6 +53,7 @@ struct Tuning {
   int tier2_min_units = kDefaultTier2MinUnits;
   int fuse_max_splits = gqa::kDefaultFuseMaxSplits;
   KernelChoice kernel = {gqa::kGatherLsu, 4, 16, 2};
+  int mla_stages = gqa::kMlaDefaultStages;
 };
 
 std::mutex g_mu;
@@ -421,7 +422,15 @@ int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_p
   }
   if (!valid_kernel(t.kernel)) return GQA_ERR_INVALID_ARGUMENT;
   std::lock_guard<std::mutex> lock(g_mu);
+  t.mla_stages = g_tune.mla_stages;  // set by gqa_mla_set_tuning
   g_tune = t;
+  return GQA_OK;
+}
+
+int gqa_mla_set_tuning(int stages) {
+  if (stages != 0 && stages != 3 && stages != 4) return GQA_ERR_INVALID_ARGUMENT;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_tune.mla_stages = stages == 0 ? gqa::kMlaDefaultStages : stages;
   return GQA_OK;
 }
 
@@ -575,12 +584,14 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
   gqa::PlanConfig cfg;
   void* ws = nullptr;
   size_t off_indptr = 0, off_slots = 0, off_po = 0, off_pl = 0, off_rec = 0;
+  int mla_stages = gqa::kMlaDefaultStages;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     int rc = current_device(&dev, &st);
     if (rc != GQA_OK) return rc;
     const Tuning& t = g_tune;
-    cfg.tier1_ctas = t.num_ctas > 0 ? t.num_ctas : st->sm_count * 2;  // two 4-warp MLA CTAs per SM
+    mla_stages = t.mla_stages;
+    cfg.tier1_ctas = t.num_ctas > 0 ? t.num_ctas : st->sm_count * gqa::mla_ctas_per_sm(mla_stages);  // one wave
     // one tier unless the tuning asks for tier 2: the MLA merge walks a sequence's pieces in turn
     cfg.tier2_ctas = t.tier2_ctas > 0 ? t.tier2_ctas : 0;
     cfg.min_units = t.min_units > 0 ? t.min_units : kDefaultMinUnits;
@@ -619,7 +630,7 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
   mp.h_q = h_q;
   mp.s_q = s_q;
   mp.scale_log2 = softmax_scale * kLog2e;
-  return gqa::launch_mla(mp, cache_seqlens, block_table, page_table_width, page_size, num_blocks, st->sm_count,
+  return gqa::launch_mla(mp, cache_seqlens, block_table, page_table_width, page_size, num_blocks, mla_stages,
                          stream) == cudaSuccess
              ? GQA_OK
              : GQA_ERR_LAUNCH;

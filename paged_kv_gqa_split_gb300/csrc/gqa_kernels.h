@@ -98,9 +98,12 @@ struct MlaParams {
   float scale_log2;
 };
 
-int mla_smem_bytes();
+// MLA decode shapes: stages 3 (3 CTAs per SM) or 4 (2 CTAs per SM).
+constexpr int kMlaDefaultStages = 3;
+int mla_smem_bytes(int stages);
+int mla_ctas_per_sm(int stages);
 cudaError_t launch_mla(const MlaParams& p, const int* cache_seqlens, const int* block_table, int width,
-                       int page_size, int num_blocks, int sm_count, cudaStream_t stream);
+                       int page_size, int num_blocks, int stages, cudaStream_t stream);
 
 // Compile-time variant of the decode kernel.
 enum : int { kGatherLsu = 0, kGatherTma = 1, kGatherLsuF8 = 2 };  // kGatherLsuF8: FP8 caches only

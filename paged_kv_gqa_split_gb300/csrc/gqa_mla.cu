@@ -36,7 +36,6 @@ constexpr int kMlaDqk = 576;
 constexpr int kMlaDv = 512;
 constexpr int kMlaRows = 16;                       // query rows per row group (one m16 tile)
 constexpr int kMlaTile = 16;                       // tokens per stage
-constexpr int kMlaStages = 4;
 constexpr int kMlaWarps = 4;
 constexpr int kMlaThreads = kMlaWarps * 32;
 constexpr int kMlaRowBytes = kMlaDqk * 2;          // 1152
@@ -45,14 +44,21 @@ constexpr int kMlaChunks = kMlaRowBytes / 16;      // 72 16-byte copies per row
 constexpr int kMlaKSteps = kMlaDqk / kMlaWarps / 16;  // 9 k-steps of 16 dims per warp (144 dims)
 constexpr int kMlaVDims = kMlaDv / kMlaWarps;      // 128 output dims per warp
 constexpr int kMlaIdsRing = 256;
-constexpr int kMlaStageBytes = kMlaTile * kMlaPitch;                       // 18,688
-constexpr int kMlaHdrOff = kMlaStages * kMlaStageBytes;                   // tile headers: 32 B per stage
-constexpr int kMlaValidOff = kMlaHdrOff + kMlaStages * 32;                // per stage: one byte per row (slot >= 0)
-constexpr int kMlaSpartOff = kMlaValidOff + kMlaStages * kMlaTile;        // [warp][half][lane] float4 partial scores
-constexpr int kMlaIdsOff = kMlaSpartOff + kMlaWarps * 32 * 8 * 4;         // per-warp slot rings
-constexpr int kMlaPlanOff = kMlaIdsOff + kMlaWarps * kMlaIdsRing * 4;     // per-warp plan copies
-constexpr int kMlaSmemBytes = kMlaPlanOff + kMlaWarps * 32;
-static_assert(kMlaSmemBytes <= 113 * 1024, "two MLA CTAs per SM");
+
+// Shared memory of a CTA with ST ring stages.
+template <int ST>
+struct MlaLayout {
+  static constexpr int kStageBytes = kMlaTile * kMlaPitch;                 // 18,688
+  static constexpr int kHdrOff = ST * kStageBytes;                        // tile headers: 32 B per stage
+  static constexpr int kValidOff = kHdrOff + ST * 32;                     // per stage: one byte per row (slot >= 0)
+  static constexpr int kSpartOff = kValidOff + ST * kMlaTile;             // [warp][half][lane] float4 partial scores
+  static constexpr int kIdsOff = kSpartOff + kMlaWarps * 32 * 8 * 4;      // per-warp slot rings
+  static constexpr int kPlanOff = kIdsOff + kMlaWarps * kMlaIdsRing * 4;  // per-warp plan copies
+  static constexpr int kSmemBytes = kPlanOff + kMlaWarps * 32;
+};
+// the compiled shapes: (3 stages, 3 CTAs per SM) and (4 stages, 2 CTAs per SM)
+static_assert(3 * (MlaLayout<3>::kSmemBytes + 1024) <= 228 * 1024, "three 3-stage MLA CTAs per SM");
+static_assert(2 * (MlaLayout<4>::kSmemBytes + 1024) <= 228 * 1024, "two 4-stage MLA CTAs per SM");
 
 struct MlaSmemPlan {
   int64_t W1, q1, q2;
@@ -66,6 +72,7 @@ struct MlaSmemPlan {
 __global__ void __launch_bounds__(1024) gqa_mla_scan_kernel(const int* __restrict__ seqlens, int batch, int cap,
                                                             int* __restrict__ indptr) {
   __shared__ int warp_sum[32];
+  pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (batch + 1023) / 1024;
   const int lo = tid * per, hi = min(batch, lo + per);
@@ -98,25 +105,41 @@ __global__ void __launch_bounds__(1024) gqa_mla_scan_kernel(const int* __restric
 }
 
 // slots[indptr[b] + t] = block_table[b, t / page_size] * page_size + t % page_size, or -1.
-__global__ void __launch_bounds__(256) gqa_mla_fill_kernel(const int* __restrict__ indptr,
-                                                           const int* __restrict__ block_table, int batch,
-                                                           int width, int page_size, int num_blocks,
-                                                           int* __restrict__ slots) {
-  for (int b = blockIdx.x; b < batch; b += gridDim.x) {
-    const int base = __ldg(indptr + b), n = __ldg(indptr + b + 1) - base;
-    for (int t = threadIdx.x; t < n; t += blockDim.x) {
-      const int lp = t / page_size;
-      int slot = -1;
-      if (lp < width) {
-        const int page = __ldg(block_table + static_cast<int64_t>(b) * width + lp);
-        if (page >= 0 && page < num_blocks) slot = page * page_size + (t - lp * page_size);
-      }
-      slots[base + t] = slot;
-    }
+// One CTA per (sequence, chunk of kMlaFillChunk tokens), kMlaFillPer independent
+// lookups per thread.
+constexpr int kMlaFillThreads = 256;
+constexpr int kMlaFillPer = 4;
+constexpr int kMlaFillChunk = kMlaFillThreads * kMlaFillPer;
+__global__ void __launch_bounds__(kMlaFillThreads) gqa_mla_fill_kernel(const int* __restrict__ indptr,
+                                                                      const int* __restrict__ block_table,
+                                                                      int chunks, int width, int page_size,
+                                                                      int num_blocks, int* __restrict__ slots) {
+  pdl_launch_dependents();
+  pdl_wait();  // indptr comes from the scan kernel
+  const int b = blockIdx.x / chunks;
+  const int t0 = (blockIdx.x - b * chunks) * kMlaFillChunk + threadIdx.x;
+  const int base = __ldg(indptr + b), n = __ldg(indptr + b + 1) - base;
+  if (t0 - static_cast<int>(threadIdx.x) >= n) return;
+  const int* row = block_table + static_cast<int64_t>(b) * width;
+  int page[kMlaFillPer];
+#pragma unroll
+  for (int k = 0; k < kMlaFillPer; ++k) {
+    const int t = t0 + k * kMlaFillThreads, lp = t / page_size;
+    page[k] = (t < n && lp < width) ? __ldg(row + lp) : -1;
+  }
+#pragma unroll
+  for (int k = 0; k < kMlaFillPer; ++k) {
+    const int t = t0 + k * kMlaFillThreads;
+    if (t < n) slots[base + t] = (page[k] >= 0 && page[k] < num_blocks) ? page[k] * page_size + t % page_size : -1;
   }
 }
 
 // --------------------------------------------------------------- decode
+__device__ __forceinline__ void mla_store_lse(const MlaParams& p, int b, int r, float lse2) {
+  // natural log, [B][h_q][s_q]; r is the query row (i * h_q + h)
+  p.lse[static_cast<int64_t>(b) * p.rows + (r % p.h_q) * p.s_q + r / p.h_q] = lse2 * 0.6931471805599453f;
+}
+
 __device__ __forceinline__ SeqSplit mla_seq_split(const MlaSmemPlan* sp, int64_t u_lo, int64_t u_hi) {
   Plan pl;
   pl.W1 = sp->W1;
@@ -133,21 +156,24 @@ __device__ __forceinline__ void mla_write_rec(int4* rec, int cta, unsigned long 
   rec[gridDim.x + cta] = make_int4(hg, si.first_slot, 0, 0);
 }
 
-__global__ void __launch_bounds__(kMlaThreads, 2) gqa_mla_decode_kernel(const MlaParams p) {
+template <int ST, int CPS>
+__global__ void __launch_bounds__(kMlaThreads, CPS) gqa_mla_decode_kernel(const MlaParams p) {
+  using L = MlaLayout<ST>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
   const uint32_t sbase = smem_addr(smem);
-  const int* ids = reinterpret_cast<const int*>(smem + kMlaIdsOff + w * kMlaIdsRing * 4);
-  const uint32_t ids_base = sbase + kMlaIdsOff + w * kMlaIdsRing * 4;
+  const int* ids = reinterpret_cast<const int*>(smem + L::kIdsOff + w * kMlaIdsRing * 4);
+  const uint32_t ids_base = sbase + L::kIdsOff + w * kMlaIdsRing * 4;
 
   pdl_launch_dependents();
+  pdl_wait();  // kv_indptr and the slots come from the prep kernels
   const uint8_t* __restrict__ kv = static_cast<const uint8_t*>(p.kv);
   const __nv_bfloat16* __restrict__ qg = static_cast<const __nv_bfloat16*>(p.q);
   const int B = p.batch;
   const int T = __ldg(p.kv_indptr + B);
   const int HG = p.rows / kMlaRows;
-  MlaSmemPlan* splan = reinterpret_cast<MlaSmemPlan*>(smem + kMlaPlanOff + w * 32);
+  MlaSmemPlan* splan = reinterpret_cast<MlaSmemPlan*>(smem + L::kPlanOff + w * 32);
   int64_t u0, u1;
   {
     const Plan pl = make_plan(static_cast<int64_t>(T) * HG, p.plan);
@@ -238,8 +264,8 @@ __global__ void __launch_bounds__(kMlaThreads, 2) gqa_mla_decode_kernel(const Ml
   int issued = 0;
   bool more = true;
   auto issue = [&]() {
-    const int stage = issued % kMlaStages;
-    const uint32_t sb = sbase + stage * kMlaStageBytes;
+    const int stage = issued % ST;
+    const uint32_t sb = sbase + stage * L::kStageBytes;
     MTile tl;
     if (more && next_tile(tl)) {
       while (tl.tt >= ib + 32) {
@@ -257,11 +283,11 @@ __global__ void __launch_bounds__(kMlaThreads, 2) gqa_mla_decode_kernel(const Ml
         for (int k = 0; k < kMlaChunks / 8; ++k) cp_async_16(dst + k * 128, src + k * 128, valid ? 16u : 0u);
         // the row enters the softmax when it is one of the first cnt and its slot is valid
         if ((tid & 7) == 0)
-          asm volatile("st.shared.u8 [%0], %1;" ::"r"(sbase + kMlaValidOff + stage * kMlaTile + row),
+          asm volatile("st.shared.u8 [%0], %1;" ::"r"(sbase + L::kValidOff + stage * kMlaTile + row),
                        "r"(valid ? 1 : 0) : "memory");
       }
       if (tid == 0) {
-        const uint32_t hdr = sbase + kMlaHdrOff + stage * 32;
+        const uint32_t hdr = sbase + L::kHdrOff + stage * 32;
         st_shared_v4(hdr, tl.b, tl.cnt, tl.flags, tl.hg);
         st_shared_v4(hdr + 16, tl.si.S, tl.si.first_cta, tl.si.first_slot, 0);
       }
@@ -271,41 +297,46 @@ __global__ void __launch_bounds__(kMlaThreads, 2) gqa_mla_decode_kernel(const Ml
       }
     } else if (more) {
       more = false;
-      if (tid == 0) st_shared_v4(sbase + kMlaHdrOff + stage * 32, 0, 0, F_DONE, 0);
+      if (tid == 0) st_shared_v4(sbase + L::kHdrOff + stage * 32, 0, 0, F_DONE, 0);
     }
     cp_async_commit();
     ++issued;
   };
 
   // ----------------------------------------------------------- compute
+  // Iteration k computes the partial scores of tile k and, interleaved with
+  // them, P.V of tile k - 1 (its P is already in registers); after the
+  // exchange barrier it refills tile k - 1's stage and runs the softmax of
+  // tile k. Two barriers per tile, as without the overlap.
   uint32_t qa[kMlaKSteps][4];  // Q A-fragments: rows g / g+8, dims 144 w + 16 ks + {2c, 2c+8} (+1)
   float acc[kMlaVDims / 8][4];  // O rows g / g+8, dims 128 w + 8 nt + 2c (+1)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 #pragma unroll
   for (int nt = 0; nt < kMlaVDims / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < kMlaKSteps; ++ks) qa[ks][0] = qa[ks][1] = qa[ks][2] = qa[ks][3] = 0u;
   // per-lane ldmatrix addresses inside a stage
   const int mk = lane >> 3;
   const uint32_t k_lane = ((mk >> 1) * 8 + (lane & 7)) * kMlaPitch + (w * 144 + (mk & 1) * 8) * 2;
   const uint32_t v_lane = ((mk & 1) * 8 + (lane & 7)) * kMlaPitch + (w * kMlaVDims + (mk >> 1) * 8) * 2;
-  float* spart = reinterpret_cast<float*>(smem + kMlaSpartOff);
+  float4* my = reinterpret_cast<float4*>(smem + L::kSpartOff) + w * 64 + lane;  // [warp][half][lane]
+  const float4* spart = reinterpret_cast<const float4*>(smem + L::kSpartOff) + lane;
+  // the tile whose P.V is pending: its P fragments, stage and header fields
+  uint32_t pa0 = 0u, pa1 = 0u, pa2 = 0u, pa3 = 0u;
+  int pend_stage = -1, pend_hb = 0, pend_thg = 0, pend_flags = 0;
 
 #pragma unroll 1
-  for (int i = 0; i < kMlaStages - 1; ++i) issue();
+  for (int i = 0; i < ST - 1; ++i) issue();
 #pragma unroll 1
   for (int k = 0;; ++k) {
-    cp_async_wait<kMlaStages - 2>();  // this thread's copies of tile k have landed
-    __syncthreads();                  // everyone's have, and everyone is done with tile k - 1
-    issue();                          // tile k + 3 into the stage tile k - 1 used
-    const int stage = k % kMlaStages;
-    const uint32_t sb = sbase + stage * kMlaStageBytes;
+    cp_async_wait<ST - 2>();  // this thread's copies of tile k have landed
+    __syncthreads();          // everyone's have; the partial scores of tile k - 1 have been read
+    const int stage = k % ST;
+    const uint32_t sb = sbase + stage * L::kStageBytes;
     int hb, cnt, flags, thg;
-    ld_shared_v4(sbase + kMlaHdrOff + stage * 32, hb, cnt, flags, thg);
-    if (flags & F_DONE) break;
-    // validity of this lane's tokens 2c, 2c + 1, 8 + 2c, 9 + 2c (one byte per row)
-    const uint8_t* vrow = smem + kMlaValidOff + stage * kMlaTile;
-    const unsigned mask = (vrow[2 * c] ? 1u : 0u) << (2 * c) | (vrow[2 * c + 1] ? 1u : 0u) << (2 * c + 1) |
-                          (vrow[8 + 2 * c] ? 1u : 0u) << (8 + 2 * c) | (vrow[9 + 2 * c] ? 1u : 0u) << (9 + 2 * c);
-    if (flags & F_QLOAD) {
+    ld_shared_v4(sbase + L::kHdrOff + stage * 32, hb, cnt, flags, thg);
+    const bool done = flags & F_DONE;
+    if (!done && (flags & F_QLOAD)) {
       const __nv_bfloat16* qr = qg + (static_cast<int64_t>(hb) * p.rows + thg * kMlaRows) * kMlaDqk;
 #pragma unroll
       for (int ks = 0; ks < kMlaKSteps; ++ks) {
@@ -315,34 +346,99 @@ __global__ void __launch_bounds__(kMlaThreads, 2) gqa_mla_decode_kernel(const Ml
         qa[ks][2] = __ldg(reinterpret_cast<const uint32_t*>(qr + g * kMlaDqk + d + 8));
         qa[ks][3] = __ldg(reinterpret_cast<const uint32_t*>(qr + (g + 8) * kMlaDqk + d + 8));
       }
+    }
+    // partial scores of this warp's 144 dims (tokens 0-7 / 8-15), two chains each;
+    // on a done tile they are computed from stale stage data and never used
+    float sla[4] = {0.f, 0.f, 0.f, 0.f}, slb[4] = {0.f, 0.f, 0.f, 0.f};
+    float sha[4] = {0.f, 0.f, 0.f, 0.f}, shb[4] = {0.f, 0.f, 0.f, 0.f};
+    if (pend_stage >= 0) {
+      const uint32_t vb = sbase + pend_stage * L::kStageBytes + v_lane;
+#pragma unroll
+      for (int ks = 0; ks < kMlaKSteps; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(sb + k_lane + ks * 32, b0, b1, b2, b3);
+        mma_bf16_16816((ks & 1) ? slb : sla, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+        mma_bf16_16816((ks & 1) ? shb : sha, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+        if (ks < kMlaVDims / 16) {
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_trans(vb + ks * 32, v0, v1, v2, v3);
+          mma_bf16_16816(acc[2 * ks], pa0, pa1, pa2, pa3, v0, v1);
+          mma_bf16_16816(acc[2 * ks + 1], pa0, pa1, pa2, pa3, v2, v3);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < kMlaKSteps; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(sb + k_lane + ks * 32, b0, b1, b2, b3);
+        mma_bf16_16816((ks & 1) ? slb : sla, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+        mma_bf16_16816((ks & 1) ? shb : sha, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+      }
+    }
+    my[0] = make_float4(sla[0] + slb[0], sla[1] + slb[1], sla[2] + slb[2], sla[3] + slb[3]);
+    my[32] = make_float4(sha[0] + shb[0], sha[1] + shb[1], sha[2] + shb[2], sha[3] + shb[3]);
+    if (pend_stage >= 0 && (pend_flags & F_END)) {  // tile k - 1 ended its piece: write O and LSE
+      SplitInfo si;
+      int dummy;
+      ld_shared_v4(sbase + L::kHdrOff + pend_stage * 32 + 16, si.S, si.first_cta, si.first_slot, dummy);
+      float lt0 = l0, lt1 = l1;
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
+        lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
+      }
+      const float i0 = lt0 > 0.f ? 1.f / lt0 : 0.f, i1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
+      const float lse0 = lt0 > 0.f ? m0 + log2f(lt0) : -INFINITY;  // base 2
+      const float lse1 = lt1 > 0.f ? m1 + log2f(lt1) : -INFINITY;
+      const int r0 = pend_thg * kMlaRows + g, r1 = r0 + 8;  // query rows (i * h_q + h) of sequence pend_hb
+      if (pend_flags & F_FINAL) {
+        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(pend_hb) * p.rows * kMlaDv;
+#pragma unroll
+        for (int nt = 0; nt < kMlaVDims / 8; ++nt) {
+          const int d = w * kMlaVDims + nt * 8 + 2 * c;
+          *reinterpret_cast<uint32_t*>(ob + static_cast<int64_t>(r0) * kMlaDv + d) = pack_bf16(acc[nt][0] * i0, acc[nt][1] * i0);
+          *reinterpret_cast<uint32_t*>(ob + static_cast<int64_t>(r1) * kMlaDv + d) = pack_bf16(acc[nt][2] * i1, acc[nt][3] * i1);
+        }
+        if (w == 0 && c == 0 && p.lse != nullptr) {
+          mla_store_lse(p, pend_hb, r0, lse0);
+          mla_store_lse(p, pend_hb, r1, lse1);
+        }
+      } else {
+        const int64_t sid = slot_id(blockIdx.x, (pend_flags & F_SLOT1) ? 1 : 0);
+        float* po = p.part_o + sid * (kMlaRows * kMlaDv);
+#pragma unroll
+        for (int nt = 0; nt < kMlaVDims / 8; ++nt) {
+          const int d = w * kMlaVDims + nt * 8 + 2 * c;
+          *reinterpret_cast<float2*>(po + g * kMlaDv + d) = make_float2(acc[nt][0] * i0, acc[nt][1] * i0);
+          *reinterpret_cast<float2*>(po + (g + 8) * kMlaDv + d) = make_float2(acc[nt][2] * i1, acc[nt][3] * i1);
+        }
+        if (w == 0 && c == 0) {
+          p.part_lse[sid * kMlaRows + g] = lse0;
+          p.part_lse[sid * kMlaRows + g + 8] = lse1;
+        }
+      }
+    }
+    if (done) break;
+    if (flags & F_QLOAD) {  // tile k opens a piece
       m0 = m1 = -INFINITY;
       l0 = l1 = 0.f;
 #pragma unroll
       for (int nt = 0; nt < kMlaVDims / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     }
-    // partial scores of this warp's 144 dims: tokens 0-7 (s[0..3]) and 8-15 (s[4..7])
-    float sl[4] = {0.f, 0.f, 0.f, 0.f}, sh[4] = {0.f, 0.f, 0.f, 0.f};  // tokens 0-7 / 8-15
-#pragma unroll
-    for (int ks = 0; ks < kMlaKSteps; ++ks) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(sb + k_lane + ks * 32, b0, b1, b2, b3);
-      mma_bf16_16816(sl, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-      mma_bf16_16816(sh, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-    }
-    float4* my = reinterpret_cast<float4*>(spart) + w * 64 + lane;  // [warp][half][lane]: 16-byte lane stride
-    my[0] = make_float4(sl[0], sl[1], sl[2], sl[3]);
-    my[32] = make_float4(sh[0], sh[1], sh[2], sh[3]);
-    __syncthreads();
+    __syncthreads();  // partial scores complete; every warp is done with tile k - 1's stage
+    issue();          // tile k + ST - 1 into that stage
     float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ww = 0; ww < kMlaWarps; ++ww) {
-      const float4* o = reinterpret_cast<const float4*>(spart) + ww * 64 + lane;
-      const float4 x = o[0], y = o[32];
+      const float4 x = spart[ww * 64], y = spart[ww * 64 + 32];
       s[0] += x.x; s[1] += x.y; s[2] += x.z; s[3] += x.w;
       s[4] += y.x; s[5] += y.y; s[6] += y.z; s[7] += y.w;
     }
-    // scale, mask (tokens 2c, 2c + 1, 8 + 2c, 9 + 2c), online softmax in base 2 (rows g: s0,1,4,5; g+8: s2,3,6,7)
-    const unsigned um = mask;
+    // validity of this lane's tokens 2c, 2c + 1, 8 + 2c, 9 + 2c (one byte per row)
+    const uint8_t* vrow = smem + L::kValidOff + stage * kMlaTile;
+    const unsigned um = (vrow[2 * c] ? 1u : 0u) << (2 * c) | (vrow[2 * c + 1] ? 1u : 0u) << (2 * c + 1) |
+                        (vrow[8 + 2 * c] ? 1u : 0u) << (8 + 2 * c) | (vrow[9 + 2 * c] ? 1u : 0u) << (9 + 2 * c);
+    // scale, mask, online softmax in base 2 (rows g: s0,1,4,5; g+8: s2,3,6,7)
     const int tk[4] = {2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -369,63 +465,20 @@ __global__ void __launch_bounds__(kMlaThreads, 2) gqa_mla_decode_kernel(const Ml
     pr[2] = ex2(s[2] - sh1); pr[3] = ex2(s[3] - sh1); pr[6] = ex2(s[6] - sh1); pr[7] = ex2(s[7] - sh1);
     l0 = l0 * a0 + (pr[0] + pr[1] + pr[4] + pr[5]);
     l1 = l1 * a1 + (pr[2] + pr[3] + pr[6] + pr[7]);
-    const uint32_t pa0 = pack_bf16(pr[0], pr[1]), pa1 = pack_bf16(pr[2], pr[3]);
-    const uint32_t pa2 = pack_bf16(pr[4], pr[5]), pa3 = pack_bf16(pr[6], pr[7]);
+    pa0 = pack_bf16(pr[0], pr[1]);
+    pa1 = pack_bf16(pr[2], pr[3]);
+    pa2 = pack_bf16(pr[4], pr[5]);
+    pa3 = pack_bf16(pr[6], pr[7]);
     if (!__all_sync(0xffffffffu, a0 == 1.f && a1 == 1.f)) {  // some row's max moved: rescale O
 #pragma unroll
       for (int nt = 0; nt < kMlaVDims / 8; ++nt) {
         acc[nt][0] *= a0; acc[nt][1] *= a0; acc[nt][2] *= a1; acc[nt][3] *= a1;
       }
     }
-#pragma unroll
-    for (int np = 0; np < kMlaVDims / 16; ++np) {
-      uint32_t v0, v1, v2, v3;
-      ldsm_x4_trans(sb + v_lane + np * 32, v0, v1, v2, v3);
-      mma_bf16_16816(acc[2 * np], pa0, pa1, pa2, pa3, v0, v1);
-      mma_bf16_16816(acc[2 * np + 1], pa0, pa1, pa2, pa3, v2, v3);
-    }
-    if (flags & F_END) {
-      SplitInfo si;
-      int dummy;
-      ld_shared_v4(sbase + kMlaHdrOff + stage * 32 + 16, si.S, si.first_cta, si.first_slot, dummy);
-      float lt0 = l0, lt1 = l1;
-#pragma unroll
-      for (int o = 1; o < 4; o <<= 1) {
-        lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
-        lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
-      }
-      const float i0 = lt0 > 0.f ? 1.f / lt0 : 0.f, i1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
-      const float lse0 = lt0 > 0.f ? m0 + log2f(lt0) : -INFINITY;  // base 2
-      const float lse1 = lt1 > 0.f ? m1 + log2f(lt1) : -INFINITY;
-      const int r0 = thg * kMlaRows + g, r1 = r0 + 8;  // query rows (i * h_q + h) of sequence hb
-      if (flags & F_FINAL) {
-        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(hb) * p.rows * kMlaDv;
-#pragma unroll
-        for (int nt = 0; nt < kMlaVDims / 8; ++nt) {
-          const int d = w * kMlaVDims + nt * 8 + 2 * c;
-          *reinterpret_cast<uint32_t*>(ob + static_cast<int64_t>(r0) * kMlaDv + d) = pack_bf16(acc[nt][0] * i0, acc[nt][1] * i0);
-          *reinterpret_cast<uint32_t*>(ob + static_cast<int64_t>(r1) * kMlaDv + d) = pack_bf16(acc[nt][2] * i1, acc[nt][3] * i1);
-        }
-        if (w == 0 && c == 0 && p.lse != nullptr) {  // natural log, [B][h_q][s_q]
-          const float ln2 = 0.6931471805599453f;
-          p.lse[static_cast<int64_t>(hb) * p.rows + (r0 % p.h_q) * p.s_q + r0 / p.h_q] = lse0 * ln2;
-          p.lse[static_cast<int64_t>(hb) * p.rows + (r1 % p.h_q) * p.s_q + r1 / p.h_q] = lse1 * ln2;
-        }
-      } else {
-        const int64_t sid = slot_id(blockIdx.x, (flags & F_SLOT1) ? 1 : 0);
-        float* po = p.part_o + sid * (kMlaRows * kMlaDv);
-#pragma unroll
-        for (int nt = 0; nt < kMlaVDims / 8; ++nt) {
-          const int d = w * kMlaVDims + nt * 8 + 2 * c;
-          *reinterpret_cast<float2*>(po + g * kMlaDv + d) = make_float2(acc[nt][0] * i0, acc[nt][1] * i0);
-          *reinterpret_cast<float2*>(po + (g + 8) * kMlaDv + d) = make_float2(acc[nt][2] * i1, acc[nt][3] * i1);
-        }
-        if (w == 0 && c == 0) {
-          p.part_lse[sid * kMlaRows + g] = lse0;
-          p.part_lse[sid * kMlaRows + g + 8] = lse1;
-        }
-      }
-    }
+    pend_stage = stage;
+    pend_hb = hb;
+    pend_thg = thg;
+    pend_flags = flags;
   }
   cp_async_wait<0>();
   if (tid == 0 && u0 < u1 && walk_ok) mla_write_rec(p.split_rec, blockIdx.x, p.epoch, pb, hg, p_si);
@@ -435,9 +488,16 @@ __global__ void __launch_bounds__(kMlaThreads, 2) gqa_mla_decode_kernel(const Ml
 // One CTA per boundary between decode CTAs j and j + 1, as for the dense
 // path: it finds the sequence cut there from CTA j's record and, being rank
 // r of its S - 1 boundary CTAs, merges a share of the 512 output dims of the
-// 16 rows over all S pieces (running max; lanes over 4-dim columns, threads
-// over rows). It also writes the empty sequences.
-__global__ void __launch_bounds__(128) gqa_mla_merge_kernel(const MlaParams p) {
+// 16 rows over all S pieces. Up to kMlaMergeMaxS pieces, the weight of every
+// (piece, row), 2^(lse_s - max) / sum, is computed once into shared memory,
+// and each output element is then one weighted sum of independent loads;
+// longer chains take a running-max loop. It also writes the empty sequences.
+constexpr int kMlaMergeThreads = 256;
+constexpr int kMlaMergeMaxS = 64;
+constexpr int kMlaMergeBatch = 4;  // float4 columns per thread per pass
+
+__global__ void __launch_bounds__(kMlaMergeThreads) gqa_mla_merge_kernel(const MlaParams p) {
+  __shared__ float wsh[kMlaMergeMaxS][kMlaRows];
   const int tid = threadIdx.x;
   const int B = p.batch;
   const int j = blockIdx.x;
@@ -450,9 +510,9 @@ __global__ void __launch_bounds__(128) gqa_mla_merge_kernel(const MlaParams p) {
   for (int b = j; b < B; b += gridDim.x) {  // empty sequences: O = 0, LSE = -inf
     if (__ldg(p.kv_indptr + b) == __ldg(p.kv_indptr + b + 1)) {
       uint4* ob = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(b) * p.rows * kMlaDv);
-      for (int i = tid; i < p.rows * kMlaDv * 2 / 16; i += 128) ob[i] = make_uint4(0, 0, 0, 0);
+      for (int i = tid; i < p.rows * kMlaDv * 2 / 16; i += kMlaMergeThreads) ob[i] = make_uint4(0, 0, 0, 0);
       if (p.lse != nullptr)
-        for (int i = tid; i < p.rows; i += 128) p.lse[static_cast<int64_t>(b) * p.rows + i] = -INFINITY;
+        for (int i = tid; i < p.rows; i += kMlaMergeThreads) p.lse[static_cast<int64_t>(b) * p.rows + i] = -INFINITY;
     }
   }
   const int HG = p.rows / kMlaRows;
@@ -460,24 +520,73 @@ __global__ void __launch_bounds__(128) gqa_mla_merge_kernel(const MlaParams p) {
   if (!boundary || pl.begin(j + 1) >= pl.W) return;
   if (static_cast<unsigned>(rec0.x) != static_cast<unsigned>(p.epoch)) return;
   const int b = rec0.y, S = rec0.w, hg = rec1.x;
-  SeqSplit sp;
-  sp.first_cta = rec0.z;
-  sp.first_slot = rec1.y;
-  sp.last_cta = sp.first_cta + S - 1;
-  if (b < 0 || b >= B || hg < 0 || hg >= HG || S < 2 || sp.first_cta > j || sp.last_cta <= j) return;
-  const int rank = j - static_cast<int>(sp.first_cta), nranks = S - 1;
-  const int row = tid >> 3, col = tid & 7;  // 16 rows x 8 columns of 4 dims
-  const int per = ((kMlaDv / 32 + nranks - 1) / nranks) * 32;  // dims per rank, a multiple of 32
-  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) +
-                      (static_cast<int64_t>(b) * p.rows + hg * kMlaRows + row) * kMlaDv;
-  for (int d0 = rank * per; d0 < min(kMlaDv, (rank + 1) * per); d0 += 32) {
-    const int d = d0 + 4 * col;
+  const int first_cta = rec0.z, first_slot = rec1.y;
+  if (b < 0 || b >= B || hg < 0 || hg >= HG || S < 2 || first_cta > j || first_cta + S - 1 <= j) return;
+  const int rank = j - first_cta, nranks = S - 1;
+  const int cols = (kMlaDv / 4 + nranks - 1) / nranks;  // float4 columns per rank
+  const int c_lo = rank * cols, c_hi = min(kMlaDv / 4, c_lo + cols);
+  if (c_lo >= c_hi) return;
+  const int ncol = c_hi - c_lo, items = kMlaRows * ncol;
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(b) * p.rows + hg * kMlaRows) * kMlaDv;
+  auto part = [&](int s) {
+    return reinterpret_cast<const float4*>(p.part_o + slot_id(first_cta + s, s == 0 ? first_slot : 0) * (kMlaRows * kMlaDv));
+  };
+  if (S <= kMlaMergeMaxS) {
+    for (int i = tid; i < S * kMlaRows; i += kMlaMergeThreads) {
+      const int s = i / kMlaRows, r = i - s * kMlaRows;
+      wsh[s][r] = __ldcg(p.part_lse + slot_id(first_cta + s, s == 0 ? first_slot : 0) * kMlaRows + r);
+    }
+    __syncthreads();
+    if (tid < kMlaRows) {  // weights of row tid; pieces with no token (lse = -inf) weigh 0
+      float m = -INFINITY;
+      for (int s = 0; s < S; ++s) m = fmaxf(m, wsh[s][tid]);
+      float den = 0.f;
+      if (m != -INFINITY)
+        for (int s = 0; s < S; ++s) den += ex2(wsh[s][tid] - m);
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      for (int s = 0; s < S; ++s) wsh[s][tid] = m == -INFINITY ? 0.f : ex2(wsh[s][tid] - m) * inv;
+      if (rank == 0 && p.lse != nullptr) mla_store_lse(p, b, hg * kMlaRows + tid, den > 0.f ? m + log2f(den) : -INFINITY);
+    }
+    __syncthreads();
+    for (int i0 = tid; i0 < items; i0 += kMlaMergeThreads * kMlaMergeBatch) {
+      float4 a[kMlaMergeBatch];
+      int rr[kMlaMergeBatch], cc[kMlaMergeBatch];
+#pragma unroll
+      for (int k = 0; k < kMlaMergeBatch; ++k) {
+        const int it = min(i0 + k * kMlaMergeThreads, items - 1);  // past the end: repeat the last item, unstored
+        rr[k] = it / ncol;
+        cc[k] = c_lo + (it - rr[k] * ncol);
+        a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll 2
+      for (int s = 0; s < S; ++s) {
+        const float4* src = part(s);
+        float4 o[kMlaMergeBatch];
+#pragma unroll
+        for (int k = 0; k < kMlaMergeBatch; ++k) o[k] = __ldcg(src + rr[k] * (kMlaDv / 4) + cc[k]);
+#pragma unroll
+        for (int k = 0; k < kMlaMergeBatch; ++k) {
+          const float w = wsh[s][rr[k]];
+          a[k].x += w * o[k].x;
+          a[k].y += w * o[k].y;
+          a[k].z += w * o[k].z;
+          a[k].w += w * o[k].w;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kMlaMergeBatch; ++k)
+        if (i0 + k * kMlaMergeThreads < items)
+          *reinterpret_cast<uint2*>(ob + rr[k] * kMlaDv + cc[k] * 4) =
+              make_uint2(pack_bf16(a[k].x, a[k].y), pack_bf16(a[k].z, a[k].w));
+    }
+    return;
+  }
+  for (int it = tid; it < items; it += kMlaMergeThreads) {  // long chains: running max per element
+    const int r = it / ncol, col = c_lo + (it - r * ncol);
     float m = -INFINITY, den = 0.f, a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
     for (int s = 0; s < S; ++s) {
-      const int64_t sid = slot_id(sp.first_cta + s, s == 0 ? sp.first_slot : 0);
-      const float l = __ldcg(p.part_lse + sid * kMlaRows + row);
-      const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + (sid * kMlaRows + row) * kMlaDv + d));
+      const float l = __ldcg(p.part_lse + slot_id(first_cta + s, s == 0 ? first_slot : 0) * kMlaRows + r);
+      const float4 o = __ldcg(part(s) + r * (kMlaDv / 4) + col);
       const float mn = fmaxf(m, l);
       if (mn == -INFINITY) continue;
       const float sc = ex2(m - mn), wt = ex2(l - mn);
@@ -489,48 +598,65 @@ __global__ void __launch_bounds__(128) gqa_mla_merge_kernel(const MlaParams p) {
       m = mn;
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    *reinterpret_cast<uint2*>(ob + d) = make_uint2(pack_bf16(a[0] * inv, a[1] * inv), pack_bf16(a[2] * inv, a[3] * inv));
-    if (d == 0 && p.lse != nullptr) {
-      const int r = hg * kMlaRows + row;
-      p.lse[static_cast<int64_t>(b) * p.rows + (r % p.h_q) * p.s_q + r / p.h_q] =
-          den > 0.f ? (m + log2f(den)) * 0.6931471805599453f : -INFINITY;
-    }
+    *reinterpret_cast<uint2*>(ob + r * kMlaDv + col * 4) =
+        make_uint2(pack_bf16(a[0] * inv, a[1] * inv), pack_bf16(a[2] * inv, a[3] * inv));
+    if (col == 0 && p.lse != nullptr) mla_store_lse(p, b, hg * kMlaRows + r, den > 0.f ? m + log2f(den) : -INFINITY);
   }
 }
 
 // --------------------------------------------------------------- launch
-int mla_smem_bytes() { return kMlaSmemBytes; }
+int mla_smem_bytes(int stages) { return stages == 3 ? MlaLayout<3>::kSmemBytes : MlaLayout<4>::kSmemBytes; }
+int mla_ctas_per_sm(int stages) { return stages == 3 ? 3 : 2; }
 
-cudaError_t launch_mla(const MlaParams& p, const int* cache_seqlens, const int* block_table, int width,
-                       int page_size, int num_blocks, int sm_count, cudaStream_t stream) {
-  gqa_mla_scan_kernel<<<1, 1024, 0, stream>>>(cache_seqlens, p.batch, width * page_size, p.kv_indptr_mut);
-  int fill_grid = p.batch < sm_count * 4 ? p.batch : sm_count * 4;
-  if (fill_grid < 1) fill_grid = 1;
-  gqa_mla_fill_kernel<<<fill_grid, 256, 0, stream>>>(p.kv_indptr, block_table, p.batch, width, page_size,
-                                                     num_blocks, p.slots_mut);
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(gqa_mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
-  const int ctas = p.plan.tier1_ctas + p.plan.tier2_ctas;
-  gqa_mla_decode_kernel<<<ctas, kMlaThreads, kMlaSmemBytes, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+static cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void** args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ctas > 1 ? ctas - 1 : 1);
-  cfg.blockDim = dim3(128);
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gqa_mla_merge_kernel, p);
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+cudaError_t launch_mla(const MlaParams& p, const int* cache_seqlens, const int* block_table, int width,
+                       int page_size, int num_blocks, int stages, cudaStream_t stream) {
+  const int cap = width * page_size;
+  gqa_mla_scan_kernel<<<1, 1024, 0, stream>>>(cache_seqlens, p.batch, cap, p.kv_indptr_mut);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  {  // one CTA per (sequence, chunk); batch * cap < 2^31 bounds the grid
+    int chunks = (cap + kMlaFillChunk - 1) / kMlaFillChunk;
+    if (chunks < 1) chunks = 1;
+    const int* ip = p.kv_indptr;
+    int* sl = p.slots_mut;
+    void* args[] = {&ip, const_cast<int**>(&block_table), &chunks, &width, &page_size, &num_blocks, &sl};
+    e = launch_pdl(reinterpret_cast<const void*>(gqa_mla_fill_kernel), dim3(p.batch * chunks), dim3(kMlaFillThreads),
+                   0, stream, args);
+    if (e != cudaSuccess) return e;
+  }
+  const void* fn = stages == 3 ? reinterpret_cast<const void*>(gqa_mla_decode_kernel<3, 3>)
+                                : reinterpret_cast<const void*>(gqa_mla_decode_kernel<4, 2>);
+  const int smem = mla_smem_bytes(stages);
+  static int configured[64][2] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int vi = stages == 3 ? 0 : 1;
+  if (dev >= 0 && dev < 64 && !configured[dev][vi]) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured[dev][vi] = 1;
+  }
+  const int ctas = p.plan.tier1_ctas + p.plan.tier2_ctas;
+  MlaParams pc = p;
+  void* args[] = {&pc};
+  e = launch_pdl(fn, dim3(ctas), dim3(kMlaThreads), smem, stream, args);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(reinterpret_cast<const void*>(gqa_mla_merge_kernel), dim3(ctas > 1 ? ctas - 1 : 1),
+                    dim3(kMlaMergeThreads), 0, stream, args);
 }
 
 }  // namespace gqa

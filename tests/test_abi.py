@@ -185,6 +185,13 @@ def test_mla_argument_checks(lib):
         assert _lib.gqa_mla_decode(*args) == _lib.GQA_ERR_INVALID_ARGUMENT, (i, bad)
 
 
+def test_mla_set_tuning_checks(lib):
+    for bad in (-1, 1, 2, 5, 8):
+        assert _lib.gqa_mla_set_tuning(bad) == _lib.GQA_ERR_INVALID_ARGUMENT
+    for ok in (3, 4, 0):
+        assert _lib.gqa_mla_set_tuning(ok) == 0
+
+
 def test_mla_cpu_tensors_raise():
     from paged_kv_gqa_split_gb300 import workloads as wl
     w = wl.make_mla_workload([5, 9], 16, 1, 4, seed=1)

@@ -21,8 +21,10 @@ O_ATOL, O_RTOL, LSE_ATOL = 2e-2, 2e-2, 1e-3
 @pytest.fixture(autouse=True)
 def _defaults(cuda_device):
     _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0)
+    _lib.gqa_mla_set_tuning(0)
     yield
     _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0)
+    _lib.gqa_mla_set_tuning(0)
 
 
 def gpu_mla(w, with_lse=True):
@@ -76,6 +78,16 @@ def test_mla_invalid_blocks_and_long_lengths():
 def test_mla_split_plans(tuning):
     assert _lib.gqa_paged_decode_set_tuning(*tuning) == 0
     w = wl.make_mla_workload([3000, 40, 1200, 0, 7], 16, 1, 64, seed=12)
+    out, lse = gpu_mla(w)
+    check(w, out, lse)
+
+
+@pytest.mark.parametrize("stages", [3, 4])
+@pytest.mark.parametrize("tuning", [(0, 0, 0, 0, 0, 0), (50, 4, 0, 0, 0, 0, 0, 40, 300, 8)])
+def test_mla_ring_depths(stages, tuning):
+    assert _lib.gqa_mla_set_tuning(stages) == 0
+    assert _lib.gqa_paged_decode_set_tuning(*tuning) == 0
+    w = wl.make_mla_workload([2500, 1, 0, 640, 17, 900], 16, 2, 64, seed=14)
     out, lse = gpu_mla(w)
     check(w, out, lse)
 
