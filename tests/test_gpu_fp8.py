@@ -103,3 +103,21 @@ def test_fp8_named_workloads_sampled(name):
     lens = np.array(w.lens)
     seqs = sorted({0, w.batch // 2, int(np.argmax(lens)), w.batch - 1})
     check(w, out, lse, seqs)
+
+
+def test_fp8_int64_page_addressing():
+    """Pages above 2^31 / 528 sit more than 2^31 bytes into each 528-byte-per-page pool."""
+    base = (1 << 31) // _lib.FP8_ROW_BYTES + 1
+    num_pages = base + 4096
+    small = wl.make_fp8_workload([40, 0, 300], seed=61)
+    g = torch.Generator().manual_seed(6)
+    high = torch.randperm(num_pages - base, generator=g)[: small.total_tokens] + base
+    high[0] = num_pages - 1
+    k = torch.zeros((num_pages, _lib.FP8_ROW_BYTES), dtype=torch.uint8, device="cuda")
+    v = torch.zeros_like(k)
+    k[high.cuda()] = small.k_cache[small.kv_indices.long()].cuda()
+    v[high.cuda()] = small.v_cache[small.kv_indices.long()].cuda()
+    out, lse = _lib.run_fp8(small.q.cuda(), k, v, small.kv_indptr.cuda(), high.to(torch.int32).cuda(), small.sm_scale)
+    torch.cuda.synchronize()
+    check(small, out.float().cpu().double().numpy(), lse.cpu().double().numpy())
+    del k, v

@@ -104,3 +104,22 @@ def test_mla_config_sampled_sequences():
     out, lse = gpu_mla(w)
     lens = np.array(w.lens)
     check(w, out, lse, sorted({0, int(np.argmax(lens)), w.batch // 2, w.batch - 1}))
+
+
+def test_mla_int64_slot_addressing():
+    """Blocks past 2^31 / (64 * 1152) sit more than 2^31 bytes into the latent pool."""
+    ps = 64
+    base = (1 << 31) // (ps * 1152) + 1
+    num_blocks = base + 64
+    small = wl.make_mla_workload([700, 0, 130], 16, 1, ps, seed=15)
+    g = torch.Generator().manual_seed(7)
+    used = (small.block_table >= 0)
+    high = torch.randperm(num_blocks - base, generator=g)[: int(used.sum())] + base
+    table = small.block_table.clone()
+    table[used] = high.to(torch.int32)
+    kv = torch.zeros((num_blocks, ps, 1, 576), dtype=torch.bfloat16, device="cuda")
+    kv[table[used].long().cuda()] = small.kv_cache[small.block_table[used].long()].cuda()
+    out, lse = _lib.mla_run(small.q.cuda(), kv, table.cuda(), small.cache_seqlens.cuda(), small.softmax_scale)
+    torch.cuda.synchronize()
+    check(small, out.float().cpu().double().numpy(), lse.cpu().double().numpy())
+    del kv
