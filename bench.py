@@ -385,16 +385,26 @@ def bench_mla(device, steps, warmup, peak):
     def call():
         _lib.mla_run(g.q, g.kv_cache, g.block_table, g.cache_seqlens, w.softmax_scale, out=out, lse=lse,
                      stream=stream)
-    for _ in range(warmup):
-        call()
-    ms = statistics.median(time_steps(call, steps, stream, flush))
     t = w.total_tokens
     b = 1152 * t + (1152 + 1024 + 4) * rows * w.batch
     flops = 2 * (576 + 512) * t * rows
+
+    def timed(kernel):
+        _lib.gqa_mla_set_tuning(kernel)
+        try:
+            for _ in range(warmup):
+                call()
+            return statistics.median(time_steps(call, steps, stream, flush))
+        finally:
+            _lib.gqa_mla_set_tuning(0)
+    ms = timed(0)
+    ms_tc = timed(1)  # the tensor-memory (tcgen05) kernel on the same workload
     res = {"batch": w.batch, "h_q": int(w.q.shape[2]), "s_q": int(w.q.shape[1]), "page_size": w.page_size,
            "total_tokens": t, "us_per_batch": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9,
            "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak, "tflops": flops / (ms * 1e-3) / 1e12,
-           "counted_bytes": b, "launches_per_call": 4}
+           "counted_bytes": b, "launches_per_call": 4, "kernel": "mma.sync, 3-stage ring",
+           "tensor_memory_kernel": {"us_per_batch": ms_tc * 1e3, "gbs": b / (ms_tc * 1e-3) / 1e9,
+                                    "frac_of_peak": b / (ms_tc * 1e-3) / 1e9 / peak, "launches_per_call": 3}}
     del g, out, lse, flush
     return res
 

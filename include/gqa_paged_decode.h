@@ -232,14 +232,18 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
                    int num_blocks, int page_table_width, struct CUstream_st* stream);
 
 /*
- * Tuning of gqa_mla_decode for tests and benchmarks (process-wide): the ring
- * depth of its decode kernel, 3 (three CTAs per SM) or 4 (two CTAs per SM);
- * 0 restores the default (3). The tier settings of
- * gqa_paged_decode_set_tuning (tier-1 CTAs, smallest share, tier 2) apply to
- * gqa_mla_decode as well; with num_ctas 0 it takes one CTA per resident slot.
- * Returns GQA_ERR_INVALID_ARGUMENT for another value.
+ * Kernel choice of gqa_mla_decode for tests and benchmarks (process-wide):
+ * 0 - default: the mma.sync kernel with a 3-stage ring (three CTAs per SM);
+ * 1 - the tensor-memory kernel (tcgen05 MMAs into tensor memory with 128
+ *     tokens on M, 2D tensor copies of the latent rows, one CTA per SM) when
+ *     page_size is a multiple of 32, else the default;
+ * 3, 4 - the mma.sync kernel with a 3-stage ring (three CTAs per SM) or a
+ *     4-stage ring (two CTAs per SM).
+ * The tier settings of gqa_paged_decode_set_tuning (tier-1 CTAs, smallest
+ * share, tier 2) apply to gqa_mla_decode as well; with num_ctas 0 it takes one
+ * CTA per resident slot. Returns GQA_ERR_INVALID_ARGUMENT for another value.
  */
-int gqa_mla_set_tuning(int stages);
+int gqa_mla_set_tuning(int kernel);
 
 /*
  * Selected-token (sparse) paged GQA decode: the sparse split-K GQA path of

@@ -404,9 +404,10 @@ def run_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, kv_in
 MLA_D_QK, MLA_D_V = 576, 512
 
 
-def gqa_mla_set_tuning(stages: int) -> int:
-    """Ring depth of the MLA decode kernel: 3 or 4, 0 for the default."""
-    return load().gqa_mla_set_tuning(stages)
+def gqa_mla_set_tuning(kernel: int) -> int:
+    """MLA decode kernel: 0 default (mma.sync, 3 stages), 1 the tensor-memory kernel
+    (block sizes that are a multiple of 32), 3 or 4 the mma.sync kernel with that ring depth."""
+    return load().gqa_mla_set_tuning(kernel)
 
 
 def gqa_mla_decode(q, kv_cache, block_table, cache_seqlens, softmax_scale, out, lse, batch, s_q, h_q, page_size,

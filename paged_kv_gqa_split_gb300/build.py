@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libgqa_paged_decode.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 SOURCES = ["gqa_decode_lsu.cu", "gqa_decode_tma.cu", "gqa_merge.cu", "gqa_api.cu", "gqa_noalloc.cu", "gqa_kv_append.cu",
-           "gqa_sparse.cu", "gqa_mla.cu"]
+           "gqa_sparse.cu", "gqa_mla.cu", "gqa_mla_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -53,6 +53,7 @@ def _stale() -> bool:
         return True
     lib_t = os.path.getmtime(LIB_PATH)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
+    deps.append(os.path.abspath(__file__))  # the source list lives here
     return any(os.path.getmtime(d) > lib_t for d in deps)
 
 

@@ -53,7 +53,7 @@ struct Tuning {
   int tier2_min_units = kDefaultTier2MinUnits;
   int fuse_max_splits = gqa::kDefaultFuseMaxSplits;
   KernelChoice kernel = {gqa::kGatherLsu, 4, 16, 2};
-  int mla_stages = gqa::kMlaDefaultStages;
+  int mla_kernel = gqa::kMlaKernelDefault;
 };
 
 std::mutex g_mu;
@@ -422,15 +422,17 @@ int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_p
   }
   if (!valid_kernel(t.kernel)) return GQA_ERR_INVALID_ARGUMENT;
   std::lock_guard<std::mutex> lock(g_mu);
-  t.mla_stages = g_tune.mla_stages;  // set by gqa_mla_set_tuning
+  t.mla_kernel = g_tune.mla_kernel;  // set by gqa_mla_set_tuning
   g_tune = t;
   return GQA_OK;
 }
 
-int gqa_mla_set_tuning(int stages) {
-  if (stages != 0 && stages != 3 && stages != 4) return GQA_ERR_INVALID_ARGUMENT;
+int gqa_mla_set_tuning(int kernel) {
+  if (kernel != gqa::kMlaKernelDefault && kernel != gqa::kMlaKernelTensorMemory && kernel != gqa::kMlaKernelMma3 &&
+      kernel != gqa::kMlaKernelMma4)
+    return GQA_ERR_INVALID_ARGUMENT;
   std::lock_guard<std::mutex> lock(g_mu);
-  g_tune.mla_stages = stages == 0 ? gqa::kMlaDefaultStages : stages;
+  g_tune.mla_kernel = kernel;
   return GQA_OK;
 }
 
@@ -584,14 +586,31 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
   gqa::PlanConfig cfg;
   void* ws = nullptr;
   size_t off_indptr = 0, off_slots = 0, off_po = 0, off_pl = 0, off_rec = 0;
-  int mla_stages = gqa::kMlaDefaultStages;
+  gqa::MlaParams mp{};
+  mp.q = q;
+  mp.kv = kv_cache;
+  mp.batch = batch;
+  mp.rows = static_cast<int>(rows);
+  mp.block_table = block_table;
+  mp.width = page_table_width;
+  mp.page_size = page_size;
+  mp.num_blocks = num_blocks;
+  int mla_kind = gqa::kMlaKernelDefault;
+  gqa::MlaTcMaps maps;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     int rc = current_device(&dev, &st);
     if (rc != GQA_OK) return rc;
     const Tuning& t = g_tune;
-    mla_stages = t.mla_stages;
-    cfg.tier1_ctas = t.num_ctas > 0 ? t.num_ctas : st->sm_count * gqa::mla_ctas_per_sm(mla_stages);  // one wave
+    mla_kind = t.mla_kernel;
+    if (mla_kind == gqa::kMlaKernelDefault) mla_kind = gqa::kMlaKernelMma3;  // the faster at 16 rows per sequence
+    if (mla_kind == gqa::kMlaKernelTensorMemory) {
+      // where the block size allows it (and Q rows fit the 32-bit box coordinates); else the mma.sync kernel
+      const bool tc = gqa::mla_tc_supported(page_size) && static_cast<int64_t>(batch) * rows < INT32_MAX &&
+                      gqa::mla_tc_encode(mp, &maps);
+      mla_kind = tc ? gqa::kMlaKernelTensorMemory : gqa::kMlaKernelMma3;
+    }
+    cfg.tier1_ctas = t.num_ctas > 0 ? t.num_ctas : st->sm_count * gqa::mla_ctas_per_sm(mla_kind);  // one wave
     // one tier unless the tuning asks for tier 2: the MLA merge walks a sequence's pieces in turn
     cfg.tier2_ctas = t.tier2_ctas > 0 ? t.tier2_ctas : 0;
     cfg.min_units = t.min_units > 0 ? t.min_units : kDefaultMinUnits;
@@ -610,9 +629,6 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
   char* wsb = static_cast<char*>(ws);
   int* err_word = nullptr;
   if (gqa::device_error_word(&err_word) != cudaSuccess) return GQA_ERR_LAUNCH;
-  gqa::MlaParams mp{};
-  mp.q = q;
-  mp.kv = kv_cache;
   mp.kv_indptr_mut = reinterpret_cast<int*>(wsb + off_indptr);
   mp.kv_indptr = mp.kv_indptr_mut;
   mp.slots_mut = reinterpret_cast<int*>(wsb + off_slots);
@@ -625,13 +641,10 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
   mp.err = err_word;
   mp.plan = cfg;
   mp.epoch = (g_epoch.fetch_add(1) % ((1ull << 40) - 1)) + 1;
-  mp.batch = batch;
-  mp.rows = static_cast<int>(rows);
   mp.h_q = h_q;
   mp.s_q = s_q;
   mp.scale_log2 = softmax_scale * kLog2e;
-  return gqa::launch_mla(mp, cache_seqlens, block_table, page_table_width, page_size, num_blocks, mla_stages,
-                         stream) == cudaSuccess
+  return gqa::launch_mla(mp, cache_seqlens, mla_kind, &maps, stream) == cudaSuccess
              ? GQA_OK
              : GQA_ERR_LAUNCH;
 }

@@ -2,6 +2,7 @@
 // (gqa_decode_lsu.cu, gqa_decode_tma.cu, gqa_merge.cu). Not part of the public header.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -96,14 +97,25 @@ struct MlaParams {
   unsigned long long epoch;
   int batch, rows, h_q, s_q;
   float scale_log2;
+  const int* block_table;  // [batch][width]
+  int width, page_size, num_blocks;
 };
 
-// MLA decode shapes: stages 3 (3 CTAs per SM) or 4 (2 CTAs per SM).
-constexpr int kMlaDefaultStages = 3;
+// MLA decode kernels: the tensor-memory kernel (block sizes that are a
+// multiple of 32) and the mma.sync kernel with a 3-stage (3 CTAs per SM) or
+// 4-stage (2 CTAs per SM) ring.
+enum : int { kMlaKernelDefault = 0, kMlaKernelTensorMemory = 1, kMlaKernelMma3 = 3, kMlaKernelMma4 = 4 };
 int mla_smem_bytes(int stages);
-int mla_ctas_per_sm(int stages);
-cudaError_t launch_mla(const MlaParams& p, const int* cache_seqlens, const int* block_table, int width,
-                       int page_size, int num_blocks, int stages, cudaStream_t stream);
+int mla_ctas_per_sm(int kind);
+struct MlaTcMaps {  // 2D tensor maps of the latent cache (boxes of 64 x 32) and of Q (64 x 16)
+  CUtensorMap kv;
+  CUtensorMap q;
+};
+bool mla_tc_supported(int page_size);
+bool mla_tc_encode(const MlaParams& p, MlaTcMaps* maps);
+cudaError_t launch_mla_tc_decode(const MlaParams& p, const MlaTcMaps& maps, int ctas, cudaStream_t stream);
+cudaError_t launch_mla(const MlaParams& p, const int* cache_seqlens, int kind, const MlaTcMaps* maps,
+                       cudaStream_t stream);
 
 // Compile-time variant of the decode kernel.
 enum : int { kGatherLsu = 0, kGatherTma = 1, kGatherLsuF8 = 2 };  // kGatherLsuF8: FP8 caches only

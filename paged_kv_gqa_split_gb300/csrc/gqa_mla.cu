@@ -606,7 +606,7 @@ __global__ void __launch_bounds__(kMlaMergeThreads) gqa_mla_merge_kernel(const M
 
 // --------------------------------------------------------------- launch
 int mla_smem_bytes(int stages) { return stages == 3 ? MlaLayout<3>::kSmemBytes : MlaLayout<4>::kSmemBytes; }
-int mla_ctas_per_sm(int stages) { return stages == 3 ? 3 : 2; }
+int mla_ctas_per_sm(int kind) { return kind == kMlaKernelTensorMemory ? 1 : (kind == kMlaKernelMma4 ? 2 : 3); }
 
 static cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void** args) {
   cudaLaunchConfig_t cfg = {};
@@ -622,38 +622,45 @@ static cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-cudaError_t launch_mla(const MlaParams& p, const int* cache_seqlens, const int* block_table, int width,
-                       int page_size, int num_blocks, int stages, cudaStream_t stream) {
+cudaError_t launch_mla(const MlaParams& p, const int* cache_seqlens, int kind, const MlaTcMaps* maps,
+                       cudaStream_t stream) {
+  int width = p.width, page_size = p.page_size, num_blocks = p.num_blocks;
   const int cap = width * page_size;
   gqa_mla_scan_kernel<<<1, 1024, 0, stream>>>(cache_seqlens, p.batch, cap, p.kv_indptr_mut);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  {  // one CTA per (sequence, chunk); batch * cap < 2^31 bounds the grid
-    int chunks = (cap + kMlaFillChunk - 1) / kMlaFillChunk;
-    if (chunks < 1) chunks = 1;
-    const int* ip = p.kv_indptr;
-    int* sl = p.slots_mut;
-    void* args[] = {&ip, const_cast<int**>(&block_table), &chunks, &width, &page_size, &num_blocks, &sl};
-    e = launch_pdl(reinterpret_cast<const void*>(gqa_mla_fill_kernel), dim3(p.batch * chunks), dim3(kMlaFillThreads),
-                   0, stream, args);
-    if (e != cudaSuccess) return e;
-  }
-  const void* fn = stages == 3 ? reinterpret_cast<const void*>(gqa_mla_decode_kernel<3, 3>)
-                                : reinterpret_cast<const void*>(gqa_mla_decode_kernel<4, 2>);
-  const int smem = mla_smem_bytes(stages);
-  static int configured[64][2] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const int vi = stages == 3 ? 0 : 1;
-  if (dev >= 0 && dev < 64 && !configured[dev][vi]) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured[dev][vi] = 1;
-  }
   const int ctas = p.plan.tier1_ctas + p.plan.tier2_ctas;
   MlaParams pc = p;
   void* args[] = {&pc};
-  e = launch_pdl(fn, dim3(ctas), dim3(kMlaThreads), smem, stream, args);
+  if (kind == kMlaKernelTensorMemory) {  // reads the block table itself: no slot list
+    e = launch_mla_tc_decode(p, *maps, ctas, stream);
+  } else {
+    {  // one CTA per (sequence, chunk); batch * cap < 2^31 bounds the grid
+      int chunks = (cap + kMlaFillChunk - 1) / kMlaFillChunk;
+      if (chunks < 1) chunks = 1;
+      const int* ip = p.kv_indptr;
+      const int* bt = p.block_table;
+      int* sl = p.slots_mut;
+      void* fargs[] = {&ip, &bt, &chunks, &width, &page_size, &num_blocks, &sl};
+      e = launch_pdl(reinterpret_cast<const void*>(gqa_mla_fill_kernel), dim3(p.batch * chunks),
+                     dim3(kMlaFillThreads), 0, stream, fargs);
+      if (e != cudaSuccess) return e;
+    }
+    const int stages = kind == kMlaKernelMma4 ? 4 : 3;
+    const void* fn = stages == 3 ? reinterpret_cast<const void*>(gqa_mla_decode_kernel<3, 3>)
+                                  : reinterpret_cast<const void*>(gqa_mla_decode_kernel<4, 2>);
+    const int smem = mla_smem_bytes(stages);
+    static int configured[64][2] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int vi = stages == 3 ? 0 : 1;
+    if (dev >= 0 && dev < 64 && !configured[dev][vi]) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      configured[dev][vi] = 1;
+    }
+    e = launch_pdl(fn, dim3(ctas), dim3(kMlaThreads), smem, stream, args);
+  }
   if (e != cudaSuccess) return e;
   return launch_pdl(reinterpret_cast<const void*>(gqa_mla_merge_kernel), dim3(ctas > 1 ? ctas - 1 : 1),
                     dim3(kMlaMergeThreads), 0, stream, args);

@@ -186,9 +186,9 @@ def test_mla_argument_checks(lib):
 
 
 def test_mla_set_tuning_checks(lib):
-    for bad in (-1, 1, 2, 5, 8):
+    for bad in (-1, 2, 5, 8):
         assert _lib.gqa_mla_set_tuning(bad) == _lib.GQA_ERR_INVALID_ARGUMENT
-    for ok in (3, 4, 0):
+    for ok in (1, 3, 4, 0):
         assert _lib.gqa_mla_set_tuning(ok) == 0
 
 

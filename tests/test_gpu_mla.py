@@ -49,18 +49,40 @@ def check(w, out, lse, seqs=None):
     assert np.all(o[empty] == 0)
 
 
-@pytest.mark.parametrize("lens,h_q,s_q,ps,seed", [
+CASES = [
     ([1, 0, 17, 64, 65, 300], 16, 1, 64, 1),
     ([2000, 5, 700], 32, 1, 64, 2),             # two row groups
     ([900, 33, 0, 128], 16, 2, 16, 3),          # two query tokens per sequence
     ([500, 77], 8, 2, 1, 4),                    # page size 1, 8 heads x 2 tokens = 16 rows
     ([4000, 3, 1500], 16, 1, 128, 5),
     ([6000, 6000], 64, 1, 64, 6),               # rows cut across CTAs in 4 row groups
-])
-def test_mla_matches_oracle(lens, h_q, s_q, ps, seed):
+    ([31, 32, 33, 95, 96, 97], 16, 1, 32, 7),   # tiles of exactly one block
+]
+
+
+# kernel 1: the tensor-memory kernel (blocks of 32, 64, 128; mma.sync otherwise); 0: the default (mma.sync)
+@pytest.mark.parametrize("kernel", [0, 1])
+@pytest.mark.parametrize("lens,h_q,s_q,ps,seed", CASES)
+def test_mla_matches_oracle(lens, h_q, s_q, ps, seed, kernel):
+    assert _lib.gqa_mla_set_tuning(kernel) == 0
     w = wl.make_mla_workload(lens, h_q, s_q, ps, seed)
     out, lse = gpu_mla(w)
     check(w, out, lse)
+
+
+def test_mla_kernels_agree():
+    """The tensor-memory and mma.sync kernels on the same inputs: both within tolerance of
+    the oracle above; here, within twice that of each other on every element."""
+    w = wl.make_mla_workload([3000, 64, 0, 1, 777], 32, 1, 64, seed=21)
+    outs = []
+    for kernel in (1, 3):
+        assert _lib.gqa_mla_set_tuning(kernel) == 0
+        outs.append(gpu_mla(w))
+    (o1, l1), (o3, l3) = outs
+    assert np.all(np.abs(o1 - o3) <= 2 * (O_ATOL + O_RTOL * np.abs(o3)))
+    fin = np.isfinite(l3)
+    assert np.array_equal(np.isneginf(l1), np.isneginf(l3))
+    assert np.all(np.abs(l1[fin] - l3[fin]) <= 2 * LSE_ATOL)
 
 
 def test_mla_invalid_blocks_and_long_lengths():
@@ -82,10 +104,10 @@ def test_mla_split_plans(tuning):
     check(w, out, lse)
 
 
-@pytest.mark.parametrize("stages", [3, 4])
+@pytest.mark.parametrize("kernel", [1, 3, 4])
 @pytest.mark.parametrize("tuning", [(0, 0, 0, 0, 0, 0), (50, 4, 0, 0, 0, 0, 0, 40, 300, 8)])
-def test_mla_ring_depths(stages, tuning):
-    assert _lib.gqa_mla_set_tuning(stages) == 0
+def test_mla_kernel_choices(kernel, tuning):
+    assert _lib.gqa_mla_set_tuning(kernel) == 0
     assert _lib.gqa_paged_decode_set_tuning(*tuning) == 0
     w = wl.make_mla_workload([2500, 1, 0, 640, 17, 900], 16, 2, 64, seed=14)
     out, lse = gpu_mla(w)
