@@ -51,8 +51,8 @@ struct MlaLayout {
   static constexpr int kStageBytes = kMlaTile * kMlaPitch;                 // 18,688
   static constexpr int kHdrOff = ST * kStageBytes;                        // tile headers: 32 B per stage
   static constexpr int kValidOff = kHdrOff + ST * 32;                     // per stage: one byte per row (slot >= 0)
-  static constexpr int kSpartOff = kValidOff + ST * kMlaTile;             // [warp][half][lane] float4 partial scores
-  static constexpr int kIdsOff = kSpartOff + kMlaWarps * 32 * 8 * 4;      // per-warp slot rings
+  static constexpr int kSpartOff = kValidOff + ST * kMlaTile;             // [2][warp][half][lane] float4 partial scores
+  static constexpr int kIdsOff = kSpartOff + 2 * kMlaWarps * 32 * 8 * 4;  // per-warp slot rings
   static constexpr int kPlanOff = kIdsOff + kMlaWarps * kMlaIdsRing * 4;  // per-warp plan copies
   static constexpr int kSmemBytes = kPlanOff + kMlaWarps * 32;
 };
@@ -304,182 +304,185 @@ __global__ void __launch_bounds__(kMlaThreads, CPS) gqa_mla_decode_kernel(const 
   };
 
   // ----------------------------------------------------------- compute
-  // Iteration k computes the partial scores of tile k and, interleaved with
-  // them, P.V of tile k - 1 (its P is already in registers); after the
-  // exchange barrier it refills tile k - 1's stage and runs the softmax of
-  // tile k. Two barriers per tile, as without the overlap.
+  // One barrier per tile. Iteration k sums the partial scores of tile k
+  // (written by the four warps in iteration k - 1) and runs its softmax; in
+  // the same straight-line block this warp computes its partial scores of
+  // tile k + 1, independent MMAs that fill the softmax's latency; then P.V of
+  // tile k. The partial scores are double-buffered, so the barrier at the top
+  // of iteration k + 1 is the only exchange point.
   uint32_t qa[kMlaKSteps][4];  // Q A-fragments: rows g / g+8, dims 144 w + 16 ks + {2c, 2c+8} (+1)
   float acc[kMlaVDims / 8][4];  // O rows g / g+8, dims 128 w + 8 nt + 2c (+1)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 #pragma unroll
   for (int nt = 0; nt < kMlaVDims / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-#pragma unroll
-  for (int ks = 0; ks < kMlaKSteps; ++ks) qa[ks][0] = qa[ks][1] = qa[ks][2] = qa[ks][3] = 0u;
   // per-lane ldmatrix addresses inside a stage
   const int mk = lane >> 3;
   const uint32_t k_lane = ((mk >> 1) * 8 + (lane & 7)) * kMlaPitch + (w * 144 + (mk & 1) * 8) * 2;
   const uint32_t v_lane = ((mk & 1) * 8 + (lane & 7)) * kMlaPitch + (w * kMlaVDims + (mk >> 1) * 8) * 2;
-  float4* my = reinterpret_cast<float4*>(smem + L::kSpartOff) + w * 64 + lane;  // [warp][half][lane]
+  float4* my = reinterpret_cast<float4*>(smem + L::kSpartOff) + w * 64 + lane;  // [buf][warp][half][lane]
   const float4* spart = reinterpret_cast<const float4*>(smem + L::kSpartOff) + lane;
-  // the tile whose P.V is pending: its P fragments, stage and header fields
-  uint32_t pa0 = 0u, pa1 = 0u, pa2 = 0u, pa3 = 0u;
-  int pend_stage = -1, pend_hb = 0, pend_thg = 0, pend_flags = 0;
+  constexpr int kSpartBuf = kMlaWarps * 64;  // float4 per buffer
+  auto load_q = [&](int qb, int qhg) {
+    const __nv_bfloat16* qr = qg + (static_cast<int64_t>(qb) * p.rows + qhg * kMlaRows) * kMlaDqk;
+#pragma unroll
+    for (int ks = 0; ks < kMlaKSteps; ++ks) {
+      const int d = w * 144 + ks * 16 + 2 * c;
+      qa[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qr + g * kMlaDqk + d));
+      qa[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qr + (g + 8) * kMlaDqk + d));
+      qa[ks][2] = __ldg(reinterpret_cast<const uint32_t*>(qr + g * kMlaDqk + d + 8));
+      qa[ks][3] = __ldg(reinterpret_cast<const uint32_t*>(qr + (g + 8) * kMlaDqk + d + 8));
+    }
+  };
+  // this warp's partial scores (its 144 dims) of the tile in stage sb, into buffer buf:
+  // tokens 0-7 (my[0]) and 8-15 (my[32]), two accumulation chains each
+  auto partial_scores = [&](uint32_t sb, int buf) {
+    float sla[4] = {0.f, 0.f, 0.f, 0.f}, slb[4] = {0.f, 0.f, 0.f, 0.f};
+    float sha[4] = {0.f, 0.f, 0.f, 0.f}, shb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < kMlaKSteps; ++ks) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(sb + k_lane + ks * 32, b0, b1, b2, b3);
+      mma_bf16_16816((ks & 1) ? slb : sla, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+      mma_bf16_16816((ks & 1) ? shb : sha, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+    }
+    my[buf * kSpartBuf] = make_float4(sla[0] + slb[0], sla[1] + slb[1], sla[2] + slb[2], sla[3] + slb[3]);
+    my[buf * kSpartBuf + 32] = make_float4(sha[0] + shb[0], sha[1] + shb[1], sha[2] + shb[2], sha[3] + shb[3]);
+  };
 
 #pragma unroll 1
   for (int i = 0; i < ST - 1; ++i) issue();
+  cp_async_wait<ST - 2>();  // this thread's copies of tile 0 have landed
+  __syncthreads();
+  int hb, cnt, flags, thg;  // header of tile k (stage k % ST)
+  ld_shared_v4(sbase + L::kHdrOff, hb, cnt, flags, thg);
+  if (!(flags & F_DONE)) {
+    load_q(hb, thg);  // the first tile opens a piece
+    partial_scores(sbase, 0);
 #pragma unroll 1
-  for (int k = 0;; ++k) {
-    cp_async_wait<ST - 2>();  // this thread's copies of tile k have landed
-    __syncthreads();          // everyone's have; the partial scores of tile k - 1 have been read
-    const int stage = k % ST;
-    const uint32_t sb = sbase + stage * L::kStageBytes;
-    int hb, cnt, flags, thg;
-    ld_shared_v4(sbase + L::kHdrOff + stage * 32, hb, cnt, flags, thg);
-    const bool done = flags & F_DONE;
-    if (!done && (flags & F_QLOAD)) {
-      const __nv_bfloat16* qr = qg + (static_cast<int64_t>(hb) * p.rows + thg * kMlaRows) * kMlaDqk;
-#pragma unroll
-      for (int ks = 0; ks < kMlaKSteps; ++ks) {
-        const int d = w * 144 + ks * 16 + 2 * c;
-        qa[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qr + g * kMlaDqk + d));
-        qa[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qr + (g + 8) * kMlaDqk + d));
-        qa[ks][2] = __ldg(reinterpret_cast<const uint32_t*>(qr + g * kMlaDqk + d + 8));
-        qa[ks][3] = __ldg(reinterpret_cast<const uint32_t*>(qr + (g + 8) * kMlaDqk + d + 8));
+    for (int k = 0;; ++k) {
+      cp_async_wait<ST - 3>();  // this thread's copies of tile k + 1 have landed (tiles up to k + ST - 2 were issued)
+      __syncthreads();     // everyone's have; tile k's partial scores are complete; tile k - 1's stage is free
+      issue();             // tile k + 2 into that stage
+      const int st0 = k % ST, st1 = (k + 1) % ST;
+      const uint32_t sb0 = sbase + st0 * L::kStageBytes, sb1 = sbase + st1 * L::kStageBytes;
+      int hb1, cnt1, flags1, thg1;
+      ld_shared_v4(sbase + L::kHdrOff + st1 * 32, hb1, cnt1, flags1, thg1);
+      const bool done1 = flags1 & F_DONE;
+      if (!done1 && (flags1 & F_QLOAD)) load_q(hb1, thg1);  // tile k + 1 opens a piece (tile k no longer needs Q)
+      // tile k's scores: sum of the four warps' partials
+      float s[8];
+      {
+        const float4* sp = spart + (k & 1) * kSpartBuf;
+        const float4 x0 = sp[0], y0 = sp[32], x1 = sp[64], y1 = sp[96], x2 = sp[128], y2 = sp[160], x3 = sp[192],
+                     y3 = sp[224];
+        s[0] = (x0.x + x1.x) + (x2.x + x3.x); s[1] = (x0.y + x1.y) + (x2.y + x3.y);
+        s[2] = (x0.z + x1.z) + (x2.z + x3.z); s[3] = (x0.w + x1.w) + (x2.w + x3.w);
+        s[4] = (y0.x + y1.x) + (y2.x + y3.x); s[5] = (y0.y + y1.y) + (y2.y + y3.y);
+        s[6] = (y0.z + y1.z) + (y2.z + y3.z); s[7] = (y0.w + y1.w) + (y2.w + y3.w);
       }
-    }
-    // partial scores of this warp's 144 dims (tokens 0-7 / 8-15), two chains each;
-    // on a done tile they are computed from stale stage data and never used
-    float sla[4] = {0.f, 0.f, 0.f, 0.f}, slb[4] = {0.f, 0.f, 0.f, 0.f};
-    float sha[4] = {0.f, 0.f, 0.f, 0.f}, shb[4] = {0.f, 0.f, 0.f, 0.f};
-    if (pend_stage >= 0) {
-      const uint32_t vb = sbase + pend_stage * L::kStageBytes + v_lane;
+      // tile k + 1's partial scores (from stale stage data when it is the end marker: never used)
+      partial_scores(sb1, (k + 1) & 1);
+      // validity of this lane's tokens 2c, 2c + 1, 8 + 2c, 9 + 2c of tile k (one byte per row)
+      const uint8_t* vrow = smem + L::kValidOff + st0 * kMlaTile;
+      const unsigned um = (vrow[2 * c] ? 1u : 0u) << (2 * c) | (vrow[2 * c + 1] ? 1u : 0u) << (2 * c + 1) |
+                          (vrow[8 + 2 * c] ? 1u : 0u) << (8 + 2 * c) | (vrow[9 + 2 * c] ? 1u : 0u) << (9 + 2 * c);
+      // scale, mask, online softmax in base 2 (rows g: s0,1,4,5; g+8: s2,3,6,7)
+      const int tk[4] = {2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c};
 #pragma unroll
-      for (int ks = 0; ks < kMlaKSteps; ++ks) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(sb + k_lane + ks * 32, b0, b1, b2, b3);
-        mma_bf16_16816((ks & 1) ? slb : sla, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-        mma_bf16_16816((ks & 1) ? shb : sha, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-        if (ks < kMlaVDims / 16) {
-          uint32_t v0, v1, v2, v3;
-          ldsm_x4_trans(vb + ks * 32, v0, v1, v2, v3);
-          mma_bf16_16816(acc[2 * ks], pa0, pa1, pa2, pa3, v0, v1);
-          mma_bf16_16816(acc[2 * ks + 1], pa0, pa1, pa2, pa3, v2, v3);
-        }
+      for (int jj = 0; jj < 4; ++jj) {
+        const bool ok = (um >> tk[jj]) & 1u;
+        const int ia = jj < 2 ? jj : 2 + jj;  // row g entry of token tk[jj]
+        const int ib2 = ia + 2;               // row g + 8 entry
+        s[ia] = ok ? s[ia] * p.scale_log2 : -INFINITY;
+        s[ib2] = ok ? s[ib2] * p.scale_log2 : -INFINITY;
       }
-    } else {
-#pragma unroll
-      for (int ks = 0; ks < kMlaKSteps; ++ks) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(sb + k_lane + ks * 32, b0, b1, b2, b3);
-        mma_bf16_16816((ks & 1) ? slb : sla, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-        mma_bf16_16816((ks & 1) ? shb : sha, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-      }
-    }
-    my[0] = make_float4(sla[0] + slb[0], sla[1] + slb[1], sla[2] + slb[2], sla[3] + slb[3]);
-    my[32] = make_float4(sha[0] + shb[0], sha[1] + shb[1], sha[2] + shb[2], sha[3] + shb[3]);
-    if (pend_stage >= 0 && (pend_flags & F_END)) {  // tile k - 1 ended its piece: write O and LSE
-      SplitInfo si;
-      int dummy;
-      ld_shared_v4(sbase + L::kHdrOff + pend_stage * 32 + 16, si.S, si.first_cta, si.first_slot, dummy);
-      float lt0 = l0, lt1 = l1;
+      float mx0 = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[4], s[5]));
+      float mx1 = fmaxf(fmaxf(s[2], s[3]), fmaxf(s[6], s[7]));
 #pragma unroll
       for (int o = 1; o < 4; o <<= 1) {
-        lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
-        lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
       }
-      const float i0 = lt0 > 0.f ? 1.f / lt0 : 0.f, i1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
-      const float lse0 = lt0 > 0.f ? m0 + log2f(lt0) : -INFINITY;  // base 2
-      const float lse1 = lt1 > 0.f ? m1 + log2f(lt1) : -INFINITY;
-      const int r0 = pend_thg * kMlaRows + g, r1 = r0 + 8;  // query rows (i * h_q + h) of sequence pend_hb
-      if (pend_flags & F_FINAL) {
-        __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(pend_hb) * p.rows * kMlaDv;
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float sh0 = mn0 == -INFINITY ? 0.f : mn0, sh1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float a0 = ex2(m0 - sh0), a1 = ex2(m1 - sh1);
+      m0 = mn0;
+      m1 = mn1;
+      float pr[8];
+      pr[0] = ex2(s[0] - sh0); pr[1] = ex2(s[1] - sh0); pr[4] = ex2(s[4] - sh0); pr[5] = ex2(s[5] - sh0);
+      pr[2] = ex2(s[2] - sh1); pr[3] = ex2(s[3] - sh1); pr[6] = ex2(s[6] - sh1); pr[7] = ex2(s[7] - sh1);
+      l0 = l0 * a0 + (pr[0] + pr[1] + pr[4] + pr[5]);
+      l1 = l1 * a1 + (pr[2] + pr[3] + pr[6] + pr[7]);
+      const uint32_t pa0 = pack_bf16(pr[0], pr[1]), pa1 = pack_bf16(pr[2], pr[3]);
+      const uint32_t pa2 = pack_bf16(pr[4], pr[5]), pa3 = pack_bf16(pr[6], pr[7]);
+      if (!__all_sync(0xffffffffu, a0 == 1.f && a1 == 1.f)) {  // some row's max moved: rescale O
 #pragma unroll
         for (int nt = 0; nt < kMlaVDims / 8; ++nt) {
-          const int d = w * kMlaVDims + nt * 8 + 2 * c;
-          *reinterpret_cast<uint32_t*>(ob + static_cast<int64_t>(r0) * kMlaDv + d) = pack_bf16(acc[nt][0] * i0, acc[nt][1] * i0);
-          *reinterpret_cast<uint32_t*>(ob + static_cast<int64_t>(r1) * kMlaDv + d) = pack_bf16(acc[nt][2] * i1, acc[nt][3] * i1);
-        }
-        if (w == 0 && c == 0 && p.lse != nullptr) {
-          mla_store_lse(p, pend_hb, r0, lse0);
-          mla_store_lse(p, pend_hb, r1, lse1);
-        }
-      } else {
-        const int64_t sid = slot_id(blockIdx.x, (pend_flags & F_SLOT1) ? 1 : 0);
-        float* po = p.part_o + sid * (kMlaRows * kMlaDv);
-#pragma unroll
-        for (int nt = 0; nt < kMlaVDims / 8; ++nt) {
-          const int d = w * kMlaVDims + nt * 8 + 2 * c;
-          *reinterpret_cast<float2*>(po + g * kMlaDv + d) = make_float2(acc[nt][0] * i0, acc[nt][1] * i0);
-          *reinterpret_cast<float2*>(po + (g + 8) * kMlaDv + d) = make_float2(acc[nt][2] * i1, acc[nt][3] * i1);
-        }
-        if (w == 0 && c == 0) {
-          p.part_lse[sid * kMlaRows + g] = lse0;
-          p.part_lse[sid * kMlaRows + g + 8] = lse1;
+          acc[nt][0] *= a0; acc[nt][1] *= a0; acc[nt][2] *= a1; acc[nt][3] *= a1;
         }
       }
-    }
-    if (done) break;
-    if (flags & F_QLOAD) {  // tile k opens a piece
-      m0 = m1 = -INFINITY;
-      l0 = l1 = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < kMlaVDims / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    }
-    __syncthreads();  // partial scores complete; every warp is done with tile k - 1's stage
-    issue();          // tile k + ST - 1 into that stage
-    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int ww = 0; ww < kMlaWarps; ++ww) {
-      const float4 x = spart[ww * 64], y = spart[ww * 64 + 32];
-      s[0] += x.x; s[1] += x.y; s[2] += x.z; s[3] += x.w;
-      s[4] += y.x; s[5] += y.y; s[6] += y.z; s[7] += y.w;
-    }
-    // validity of this lane's tokens 2c, 2c + 1, 8 + 2c, 9 + 2c (one byte per row)
-    const uint8_t* vrow = smem + L::kValidOff + stage * kMlaTile;
-    const unsigned um = (vrow[2 * c] ? 1u : 0u) << (2 * c) | (vrow[2 * c + 1] ? 1u : 0u) << (2 * c + 1) |
-                        (vrow[8 + 2 * c] ? 1u : 0u) << (8 + 2 * c) | (vrow[9 + 2 * c] ? 1u : 0u) << (9 + 2 * c);
-    // scale, mask, online softmax in base 2 (rows g: s0,1,4,5; g+8: s2,3,6,7)
-    const int tk[4] = {2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const bool ok = (um >> tk[j]) & 1u;
-      const int ia = j < 2 ? j : 2 + j;      // row g entry of token tk[j]
-      const int ib2 = ia + 2;                // row g + 8 entry
-      s[ia] = ok ? s[ia] * p.scale_log2 : -INFINITY;
-      s[ib2] = ok ? s[ib2] * p.scale_log2 : -INFINITY;
-    }
-    float mx0 = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[4], s[5]));
-    float mx1 = fmaxf(fmaxf(s[2], s[3]), fmaxf(s[6], s[7]));
-#pragma unroll
-    for (int o = 1; o < 4; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-    }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float sh0 = mn0 == -INFINITY ? 0.f : mn0, sh1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float a0 = ex2(m0 - sh0), a1 = ex2(m1 - sh1);
-    m0 = mn0;
-    m1 = mn1;
-    float pr[8];
-    pr[0] = ex2(s[0] - sh0); pr[1] = ex2(s[1] - sh0); pr[4] = ex2(s[4] - sh0); pr[5] = ex2(s[5] - sh0);
-    pr[2] = ex2(s[2] - sh1); pr[3] = ex2(s[3] - sh1); pr[6] = ex2(s[6] - sh1); pr[7] = ex2(s[7] - sh1);
-    l0 = l0 * a0 + (pr[0] + pr[1] + pr[4] + pr[5]);
-    l1 = l1 * a1 + (pr[2] + pr[3] + pr[6] + pr[7]);
-    pa0 = pack_bf16(pr[0], pr[1]);
-    pa1 = pack_bf16(pr[2], pr[3]);
-    pa2 = pack_bf16(pr[4], pr[5]);
-    pa3 = pack_bf16(pr[6], pr[7]);
-    if (!__all_sync(0xffffffffu, a0 == 1.f && a1 == 1.f)) {  // some row's max moved: rescale O
-#pragma unroll
-      for (int nt = 0; nt < kMlaVDims / 8; ++nt) {
-        acc[nt][0] *= a0; acc[nt][1] *= a0; acc[nt][2] *= a1; acc[nt][3] *= a1;
+      for (int np = 0; np < kMlaVDims / 16; ++np) {  // O += P V of tile k (this warp's 128 dims)
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_trans(sb0 + v_lane + np * 32, v0, v1, v2, v3);
+        mma_bf16_16816(acc[2 * np], pa0, pa1, pa2, pa3, v0, v1);
+        mma_bf16_16816(acc[2 * np + 1], pa0, pa1, pa2, pa3, v2, v3);
       }
+      if (flags & F_END) {  // tile k ends its piece: write O and LSE
+        SplitInfo si;
+        int dummy;
+        ld_shared_v4(sbase + L::kHdrOff + st0 * 32 + 16, si.S, si.first_cta, si.first_slot, dummy);
+        float lt0 = l0, lt1 = l1;
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1) {
+          lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
+          lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
+        }
+        const float i0 = lt0 > 0.f ? 1.f / lt0 : 0.f, i1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
+        const float lse0 = lt0 > 0.f ? m0 + log2f(lt0) : -INFINITY;  // base 2
+        const float lse1 = lt1 > 0.f ? m1 + log2f(lt1) : -INFINITY;
+        const int r0 = thg * kMlaRows + g, r1 = r0 + 8;  // query rows (i * h_q + h) of sequence hb
+        if (flags & F_FINAL) {
+          __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(hb) * p.rows * kMlaDv;
+#pragma unroll
+          for (int nt = 0; nt < kMlaVDims / 8; ++nt) {
+            const int d = w * kMlaVDims + nt * 8 + 2 * c;
+            *reinterpret_cast<uint32_t*>(ob + static_cast<int64_t>(r0) * kMlaDv + d) = pack_bf16(acc[nt][0] * i0, acc[nt][1] * i0);
+            *reinterpret_cast<uint32_t*>(ob + static_cast<int64_t>(r1) * kMlaDv + d) = pack_bf16(acc[nt][2] * i1, acc[nt][3] * i1);
+          }
+          if (w == 0 && c == 0 && p.lse != nullptr) {
+            mla_store_lse(p, hb, r0, lse0);
+            mla_store_lse(p, hb, r1, lse1);
+          }
+        } else {
+          const int64_t sid = slot_id(blockIdx.x, (flags & F_SLOT1) ? 1 : 0);
+          float* po = p.part_o + sid * (kMlaRows * kMlaDv);
+#pragma unroll
+          for (int nt = 0; nt < kMlaVDims / 8; ++nt) {
+            const int d = w * kMlaVDims + nt * 8 + 2 * c;
+            *reinterpret_cast<float2*>(po + g * kMlaDv + d) = make_float2(acc[nt][0] * i0, acc[nt][1] * i0);
+            *reinterpret_cast<float2*>(po + (g + 8) * kMlaDv + d) = make_float2(acc[nt][2] * i1, acc[nt][3] * i1);
+          }
+          if (w == 0 && c == 0) {
+            p.part_lse[sid * kMlaRows + g] = lse0;
+            p.part_lse[sid * kMlaRows + g + 8] = lse1;
+          }
+        }
+      }
+      if (done1) break;
+      if (flags1 & F_QLOAD) {  // tile k + 1 opens a piece
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < kMlaVDims / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+      }
+      hb = hb1;
+      cnt = cnt1;
+      flags = flags1;
+      thg = thg1;
     }
-    pend_stage = stage;
-    pend_hb = hb;
-    pend_thg = thg;
-    pend_flags = flags;
   }
+  (void)cnt;
   cp_async_wait<0>();
   if (tid == 0 && u0 < u1 && walk_ok) mla_write_rec(p.split_rec, blockIdx.x, p.epoch, pb, hg, p_si);
 }
