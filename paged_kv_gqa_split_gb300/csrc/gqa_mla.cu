@@ -12,8 +12,8 @@
 // the dense path's two-tier split plan, walker, split records and tiers
 // apply unchanged; the unit is one cached token for one group of 16 query
 // rows. A decode CTA has 4 warps that share 16-token tiles of 1152-byte
-// latent rows (gathered with 16-byte cp.async into a 4-deep ring at a
-// 1168-byte pitch) and compute:
+// latent rows (gathered with 16-byte cp.async into a 3-deep ring, or 4-deep
+// at two CTAs per SM, at a 1168-byte pitch) and compute:
 //   S = Q K^T: each warp contracts 144 of the 576 dims (its Q fragments stay
 //     in registers), the 4 partial 16 x 16 score tiles are summed through
 //     shared memory, so every warp holds the full tile in the mma accumulator
@@ -21,6 +21,9 @@
 //   online softmax in base 2, identical in every warp;
 //   O += P V: each warp owns 128 of the 512 output dims (V fragments by
 //     ldmatrix.trans from the same latent rows).
+// With double-buffered partial scores one CTA barrier per tile suffices: the
+// softmax and P V of tile k share a straight-line block with the partial
+// scores of tile k + 1.
 // Pieces of a sequence cut across CTAs leave fp32 partials [16 rows][512]
 // that gqa_mla_merge_kernel combines.
 #include <cuda_runtime.h>
