@@ -128,8 +128,10 @@ def test_mla_config_sampled_sequences():
     check(w, out, lse, sorted({0, int(np.argmax(lens)), w.batch // 2, w.batch - 1}))
 
 
-def test_mla_int64_slot_addressing():
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_mla_int64_slot_addressing(kernel):
     """Blocks past 2^31 / (64 * 1152) sit more than 2^31 bytes into the latent pool."""
+    assert _lib.gqa_mla_set_tuning(kernel) == 0
     ps = 64
     base = (1 << 31) // (ps * 1152) + 1
     num_blocks = base + 64
@@ -145,3 +147,24 @@ def test_mla_int64_slot_addressing():
     torch.cuda.synchronize()
     check(small, out.float().cpu().double().numpy(), lse.cpu().double().numpy())
     del kv
+
+
+@pytest.mark.parametrize("lens,h_q,s_q,ps,seed,ctas", [
+    ([129, 1, 0, 255, 256, 257], 48, 1, 64, 31, 0),       # three row groups per sequence
+    ([600, 2, 130], 16, 3, 128, 32, 0),                   # three query tokens: 48 rows
+    ([128] * 9 + [0, 1, 127], 16, 1, 32, 33, 5),          # tiles of exactly one 128-token window, few CTAs
+    ([5000, 17, 4100], 16, 1, 64, 34, 77),                # pieces cut inside 128-token tiles
+    (list(range(1, 200, 7)), 16, 1, 64, 35, 0),           # many short sequences
+])
+def test_mla_tensor_memory_shapes(lens, h_q, s_q, ps, seed, ctas):
+    """Tile edges of the tensor-memory kernel (128-token windows, 32- or 64-row copies, row groups),
+    against the oracle, and against the mma.sync kernel on the same inputs."""
+    w = wl.make_mla_workload(lens, h_q, s_q, ps, seed)
+    assert _lib.gqa_paged_decode_set_tuning(ctas, 0, 0, 0, 0, 0) == 0
+    outs = []
+    for kernel in (1, 3):
+        assert _lib.gqa_mla_set_tuning(kernel) == 0
+        outs.append(gpu_mla(w))
+    check(w, *outs[0])
+    (o1, l1), (o3, l3) = outs
+    assert np.all(np.abs(o1 - o3) <= 2 * (O_ATOL + O_RTOL * np.abs(o3)))
