@@ -245,8 +245,12 @@ def bench_workload_gpu(w, device, steps, warmup, world, with_hooks=True):
         finally:
             _lib.gqa_paged_decode_set_profile_events(None, None)
         dec_ms = [a.elapsed_time(b) for a, b in evs]
+    warm_ms = None
+    if with_hooks:  # the same calls with L2 left warm between steps (inputs smaller than L2 stay resident)
+        warm_ms = time_steps(call, steps, stream, lambda: None)
     del flush
-    return {"step_ms": step_ms, "decode_ms": dec_ms, "wall_s": wall, "gpu": g, "out": out, "lse": lse}
+    return {"step_ms": step_ms, "decode_ms": dec_ms, "warm_ms": warm_ms, "wall_s": wall, "gpu": g, "out": out,
+            "lse": lse}
 
 
 def bench_e2e(w, device, steps, warmup):
@@ -368,13 +372,14 @@ def bench_fp8(w, g, device, steps, warmup, peak):
 
 
 # ------------------------------------------------------------ MLA decode
-def bench_mla(device, steps, warmup, peak):
+def bench_mla(device, steps, warmup, peak, wide: bool = False):
     """Dense MLA decode of the MLA workload (128 sequences of U[1024, 8192]
-    cached tokens, 16 query heads, blocks of 64): µs per call and GB/s of the
-    counted bytes, 1152 B of latent row per cached token plus q (1152 B),
-    O (1024 B) and LSE (4 B) per query row. FLOPs: 2 * (576 + 512) per
-    (token, query row)."""
-    w = wl.make_mla_config()
+    cached tokens, 16 query heads, blocks of 64; with `wide`, 64 query heads on
+    the same lengths): µs per call and GB/s of the counted bytes, 1152 B of
+    latent row per cached token plus q (1152 B), O (1024 B) and LSE (4 B) per
+    query row. FLOPs: 2 * (576 + 512) per (token, query row). Both kernels are
+    timed; the line's figures are the default one's."""
+    w = wl.make_mla_config(wide)
     g = w.to(device)
     rows = int(w.q.shape[1] * w.q.shape[2])
     out = torch.empty((w.batch, w.q.shape[1], w.q.shape[2], 512), dtype=torch.bfloat16, device=device)
@@ -394,17 +399,21 @@ def bench_mla(device, steps, warmup, peak):
         try:
             for _ in range(warmup):
                 call()
-            return statistics.median(time_steps(call, steps, stream, flush))
+            ms = statistics.median(time_steps(call, steps, stream, flush))
         finally:
             _lib.gqa_mla_set_tuning(0)
-    ms = timed(0)
-    ms_tc = timed(1)  # the tensor-memory (tcgen05) kernel on the same workload
+        return {"us_per_batch": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9, "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
+                "tflops": flops / (ms * 1e-3) / 1e12}
+    tc = timed(1)   # the tensor-memory (tcgen05) kernel: 16- or 64-row pieces
+    mma = timed(3)  # the mma.sync kernel: 16-row pieces
+    default_tc = rows % 64 == 0 and w.page_size % 32 == 0
+    d = tc if default_tc else mma
     res = {"batch": w.batch, "h_q": int(w.q.shape[2]), "s_q": int(w.q.shape[1]), "page_size": w.page_size,
-           "total_tokens": t, "us_per_batch": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9,
-           "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak, "tflops": flops / (ms * 1e-3) / 1e12,
-           "counted_bytes": b, "launches_per_call": 4, "kernel": "mma.sync, 3-stage ring",
-           "tensor_memory_kernel": {"us_per_batch": ms_tc * 1e3, "gbs": b / (ms_tc * 1e-3) / 1e9,
-                                    "frac_of_peak": b / (ms_tc * 1e-3) / 1e9 / peak, "launches_per_call": 3}}
+           "total_tokens": t, "us_per_batch": d["us_per_batch"], "gbs": d["gbs"], "frac_of_peak": d["frac_of_peak"],
+           "tflops": d["tflops"], "counted_bytes": b,
+           "kernel": ("tensor memory, %d-row pieces" % (64 if rows % 64 == 0 else 16)) if default_tc
+           else "mma.sync, 3-stage ring",
+           "tensor_memory_kernel": dict(tc, launches_per_call=3), "mma_sync_kernel": dict(mma, launches_per_call=4)}
     del g, out, lse, flush
     return res
 
@@ -523,7 +532,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="time every decode variant instead of the contract line")
-    ap.add_argument("--only", choices=["fp8", "sparse", "mla"], default=None,
+    ap.add_argument("--only", choices=["fp8", "sparse", "mla", "mla-wide"], default=None,
                     help="time only the FP8-cache decode of --workload, or only the selected-token decode, and "
                          "print its result (for profiling a small case)")
     args = ap.parse_args()
@@ -556,6 +565,8 @@ def main():
             res = bench_fp8(w, w.to(device), device, args.steps, warmup, peak)
         elif args.only == "mla":
             res = bench_mla(device, args.steps, warmup, peak)
+        elif args.only == "mla-wide":
+            res = bench_mla(device, args.steps, warmup, peak, wide=True)
         else:
             res = bench_sparse(device, args.steps, warmup, peak)
         if rank == 0:
@@ -595,17 +606,18 @@ def main():
             table[name] = {"us_per_batch": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9,
                            "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
                            "decode_kernel_us": dm * 1e3, "batch": ww.batch, "total_tokens": ww.total_tokens,
-                           "counted_bytes": b}
+                           "counted_bytes": b, "us_per_batch_l2_warm": statistics.median(rr["warm_ms"]) * 1e3}
             del rr
             if ww is not w:
                 del ww
 
-    append = sparse = fp8 = mla = None
+    append = sparse = fp8 = mla = mla_wide = None
     if not args.no_workloads:
         append = bench_append(device, args.steps, warmup, w.batch, peak)
         sparse = bench_sparse(device, args.steps, warmup, peak)
         fp8 = bench_fp8(w, w.to(device), device, args.steps, warmup, peak)
         mla = bench_mla(device, args.steps, warmup, peak)
+        mla_wide = bench_mla(device, args.steps, warmup, peak, wide=True)
 
     cpu, parity = None, None
     if rank == 0 and not args.no_cpu_baseline:
@@ -651,6 +663,7 @@ def main():
         "sparse_decode": sparse,
         "fp8_decode": fp8,
         "mla_decode": mla,
+        "mla_decode_64_heads": mla_wide,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

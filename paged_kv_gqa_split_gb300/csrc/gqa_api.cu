@@ -603,11 +603,17 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
     if (rc != GQA_OK) return rc;
     const Tuning& t = g_tune;
     mla_kind = t.mla_kernel;
-    if (mla_kind == gqa::kMlaKernelDefault) mla_kind = gqa::kMlaKernelMma3;  // the faster at 16 rows per sequence
+    // default: the tensor-memory kernel when a sequence's rows come in multiples of 64 (one pass over the
+    // latent rows serves 64 rows, where the mma.sync kernel reads them once per 16); mma.sync otherwise
+    mp.piece_rows = 16;
+    if (mla_kind == gqa::kMlaKernelDefault)
+      mla_kind = rows % 64 == 0 ? gqa::kMlaKernelTensorMemory : gqa::kMlaKernelMma3;
     if (mla_kind == gqa::kMlaKernelTensorMemory) {
       // where the block size allows it (and Q rows fit the 32-bit box coordinates); else the mma.sync kernel
+      mp.piece_rows = gqa::mla_tc_piece_rows(static_cast<int>(rows));
       const bool tc = gqa::mla_tc_supported(page_size) && static_cast<int64_t>(batch) * rows < INT32_MAX &&
                       gqa::mla_tc_encode(mp, &maps);
+      if (!tc) mp.piece_rows = 16;
       mla_kind = tc ? gqa::kMlaKernelTensorMemory : gqa::kMlaKernelMma3;
     }
     cfg.tier1_ctas = t.num_ctas > 0 ? t.num_ctas : st->sm_count * gqa::mla_ctas_per_sm(mla_kind);  // one wave
@@ -620,8 +626,9 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
     off_indptr = 0;
     off_slots = round256(static_cast<size_t>(batch + 1) * 4);
     off_po = off_slots + round256(static_cast<size_t>(max_tokens) * 4);
-    off_pl = off_po + round256(2 * ctas * 16 * 512 * sizeof(float));
-    off_rec = off_pl + round256(2 * ctas * 16 * sizeof(float));
+    const size_t pr = static_cast<size_t>(mp.piece_rows);
+    off_pl = off_po + round256(2 * ctas * pr * 512 * sizeof(float));
+    off_rec = off_pl + round256(2 * ctas * pr * sizeof(float));
     const size_t need = off_rec + round256(2 * ctas * 16);
     rc = library_workspace(st, need, &ws);
     if (rc != GQA_OK) return rc;

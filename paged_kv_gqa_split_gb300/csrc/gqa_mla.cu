@@ -494,16 +494,19 @@ __global__ void __launch_bounds__(kMlaThreads, CPS) gqa_mla_decode_kernel(const 
 // One CTA per boundary between decode CTAs j and j + 1, as for the dense
 // path: it finds the sequence cut there from CTA j's record and, being rank
 // r of its S - 1 boundary CTAs, merges a share of the 512 output dims of the
-// 16 rows over all S pieces. Up to kMlaMergeMaxS pieces, the weight of every
-// (piece, row), 2^(lse_s - max) / sum, is computed once into shared memory,
-// and each output element is then one weighted sum of independent loads;
-// longer chains take a running-max loop. It also writes the empty sequences.
+// piece's rows (p.piece_rows: 16 for the mma.sync kernel, 16 or 64 for the
+// tensor-memory kernel) over all S pieces. While S * rows fits the weight
+// table, the weight of every (piece, row), 2^(lse_s - max) / sum, is
+// computed once into shared memory and each output element is then one
+// weighted sum of independent loads; longer chains take a running-max loop.
+// It also writes the empty sequences.
 constexpr int kMlaMergeThreads = 256;
-constexpr int kMlaMergeMaxS = 64;
+constexpr int kMlaMergeWeights = 1024;  // (piece, row) weights in the table: 64 pieces of 16 rows, 16 of 64
 constexpr int kMlaMergeBatch = 4;  // float4 columns per thread per pass
 
 __global__ void __launch_bounds__(kMlaMergeThreads) gqa_mla_merge_kernel(const MlaParams p) {
-  __shared__ float wsh[kMlaMergeMaxS][kMlaRows];
+  __shared__ float wsh[kMlaMergeWeights];  // [piece][row]
+  const int R = p.piece_rows;                // rows per piece: 16 or 64
   const int tid = threadIdx.x;
   const int B = p.batch;
   const int j = blockIdx.x;
@@ -521,7 +524,7 @@ __global__ void __launch_bounds__(kMlaMergeThreads) gqa_mla_merge_kernel(const M
         for (int i = tid; i < p.rows; i += kMlaMergeThreads) p.lse[static_cast<int64_t>(b) * p.rows + i] = -INFINITY;
     }
   }
-  const int HG = p.rows / kMlaRows;
+  const int HG = p.rows / R;
   const Plan pl = make_plan(static_cast<int64_t>(T) * HG, p.plan);
   if (!boundary || pl.begin(j + 1) >= pl.W) return;
   if (static_cast<unsigned>(rec0.x) != static_cast<unsigned>(p.epoch)) return;
@@ -532,26 +535,26 @@ __global__ void __launch_bounds__(kMlaMergeThreads) gqa_mla_merge_kernel(const M
   const int cols = (kMlaDv / 4 + nranks - 1) / nranks;  // float4 columns per rank
   const int c_lo = rank * cols, c_hi = min(kMlaDv / 4, c_lo + cols);
   if (c_lo >= c_hi) return;
-  const int ncol = c_hi - c_lo, items = kMlaRows * ncol;
-  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(b) * p.rows + hg * kMlaRows) * kMlaDv;
+  const int ncol = c_hi - c_lo, items = R * ncol;
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(b) * p.rows + hg * R) * kMlaDv;
   auto part = [&](int s) {
-    return reinterpret_cast<const float4*>(p.part_o + slot_id(first_cta + s, s == 0 ? first_slot : 0) * (kMlaRows * kMlaDv));
+    return reinterpret_cast<const float4*>(p.part_o + slot_id(first_cta + s, s == 0 ? first_slot : 0) * (static_cast<int64_t>(R) * kMlaDv));
   };
-  if (S <= kMlaMergeMaxS) {
-    for (int i = tid; i < S * kMlaRows; i += kMlaMergeThreads) {
-      const int s = i / kMlaRows, r = i - s * kMlaRows;
-      wsh[s][r] = __ldcg(p.part_lse + slot_id(first_cta + s, s == 0 ? first_slot : 0) * kMlaRows + r);
+  if (S * R <= kMlaMergeWeights) {
+    for (int i = tid; i < S * R; i += kMlaMergeThreads) {
+      const int s = i / R, r = i - s * R;
+      wsh[s * R + r] = __ldcg(p.part_lse + slot_id(first_cta + s, s == 0 ? first_slot : 0) * R + r);
     }
     __syncthreads();
-    if (tid < kMlaRows) {  // weights of row tid; pieces with no token (lse = -inf) weigh 0
+    if (tid < R) {  // weights of row tid; pieces with no token (lse = -inf) weigh 0
       float m = -INFINITY;
-      for (int s = 0; s < S; ++s) m = fmaxf(m, wsh[s][tid]);
+      for (int s = 0; s < S; ++s) m = fmaxf(m, wsh[s * R + tid]);
       float den = 0.f;
       if (m != -INFINITY)
-        for (int s = 0; s < S; ++s) den += ex2(wsh[s][tid] - m);
+        for (int s = 0; s < S; ++s) den += ex2(wsh[s * R + tid] - m);
       const float inv = den > 0.f ? 1.f / den : 0.f;
-      for (int s = 0; s < S; ++s) wsh[s][tid] = m == -INFINITY ? 0.f : ex2(wsh[s][tid] - m) * inv;
-      if (rank == 0 && p.lse != nullptr) mla_store_lse(p, b, hg * kMlaRows + tid, den > 0.f ? m + log2f(den) : -INFINITY);
+      for (int s = 0; s < S; ++s) wsh[s * R + tid] = m == -INFINITY ? 0.f : ex2(wsh[s * R + tid] - m) * inv;
+      if (rank == 0 && p.lse != nullptr) mla_store_lse(p, b, hg * R + tid, den > 0.f ? m + log2f(den) : -INFINITY);
     }
     __syncthreads();
     for (int i0 = tid; i0 < items; i0 += kMlaMergeThreads * kMlaMergeBatch) {
@@ -572,7 +575,7 @@ __global__ void __launch_bounds__(kMlaMergeThreads) gqa_mla_merge_kernel(const M
         for (int k = 0; k < kMlaMergeBatch; ++k) o[k] = __ldcg(src + rr[k] * (kMlaDv / 4) + cc[k]);
 #pragma unroll
         for (int k = 0; k < kMlaMergeBatch; ++k) {
-          const float w = wsh[s][rr[k]];
+          const float w = wsh[s * R + rr[k]];
           a[k].x += w * o[k].x;
           a[k].y += w * o[k].y;
           a[k].z += w * o[k].z;
@@ -591,7 +594,7 @@ __global__ void __launch_bounds__(kMlaMergeThreads) gqa_mla_merge_kernel(const M
     const int r = it / ncol, col = c_lo + (it - r * ncol);
     float m = -INFINITY, den = 0.f, a[4] = {0.f, 0.f, 0.f, 0.f};
     for (int s = 0; s < S; ++s) {
-      const float l = __ldcg(p.part_lse + slot_id(first_cta + s, s == 0 ? first_slot : 0) * kMlaRows + r);
+      const float l = __ldcg(p.part_lse + slot_id(first_cta + s, s == 0 ? first_slot : 0) * R + r);
       const float4 o = __ldcg(part(s) + r * (kMlaDv / 4) + col);
       const float mn = fmaxf(m, l);
       if (mn == -INFINITY) continue;
@@ -606,7 +609,7 @@ __global__ void __launch_bounds__(kMlaMergeThreads) gqa_mla_merge_kernel(const M
     const float inv = den > 0.f ? 1.f / den : 0.f;
     *reinterpret_cast<uint2*>(ob + r * kMlaDv + col * 4) =
         make_uint2(pack_bf16(a[0] * inv, a[1] * inv), pack_bf16(a[2] * inv, a[3] * inv));
-    if (col == 0 && p.lse != nullptr) mla_store_lse(p, b, hg * kMlaRows + r, den > 0.f ? m + log2f(den) : -INFINITY);
+    if (col == 0 && p.lse != nullptr) mla_store_lse(p, b, hg * R + r, den > 0.f ? m + log2f(den) : -INFINITY);
   }
 }
 

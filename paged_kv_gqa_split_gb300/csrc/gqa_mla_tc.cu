@@ -4,27 +4,30 @@
 // values, V = its first 512, natural-log LSE), for block sizes that are a
 // multiple of 32 tokens.
 //
-// A tcgen05.mma costs about 45 cycles at small shapes, so the tiles put 128
-// tokens on M: S^T = K Q^T (M = 128 tokens, N = 16 query rows, K = 576: 36
-// MMAs) and O^T += V^T P^T (M = 128 dims x 4 blocks, N = 16, K = 128 tokens:
-// 32 MMAs) per 128-token tile. A tile's 147 KB of latent rows do not fit
-// beside a ring, so they stream through a 6-deep ring of 32 KB units (two
-// 64-dim regions of the 128 rows, loaded by 2D tensor copies with 128-byte
-// swizzle): five units feed S^T, and the four V units are loaded again (from
-// L2) for the P.V of the tile once its softmax is done.
+// A tcgen05.mma costs about 45-80 cycles at small shapes, so the tiles put 128
+// tokens on M and the R query rows of a piece (16, or 64 when the rows of a
+// sequence come in multiples of 64) on N: S^T = K Q^T (M = 128 tokens, N = R,
+// K = 576: 36 MMAs) and O^T += V^T P^T (M = 128 dims x 4 blocks, N = R,
+// K = 128 tokens: 32 MMAs) per 128-token tile. With R = 64 one pass over the
+// latent rows serves 64 heads, where 16-row pieces would read them four times.
+// A tile's 147 KB of latent rows do not fit beside a ring, so they stream
+// through a ring of 32 KB units (two 64-dim regions of the 128 rows, loaded by
+// 2D tensor copies with 128-byte swizzle): five units feed S^T, and the four V
+// units are loaded again (from L2) for the P.V of the tile once its softmax is
+// done.
 //
-// One CTA per SM, 320 threads in roles:
-//   warps 0-3  softmax: thread t owns token t of the tile (tensor-memory lane
-//              t of S^T) and its 16 scores; the running max of a row moves
-//              only when a score passes it by more than 2^8 (a vote over the
-//              128 threads decides), so P = 2^(s - m) < 256 in bf16 and the
-//              row sums stay per thread until the end of a piece;
-//   warps 4-7  correction and epilogue: rescale O^T when a max moved, and
-//              write O (or the fp32 partial) at the end of a piece;
-//   warp 8     MMA issue (one thread);
-//   warp 9     producer: the tensor copies of Q and of the ring units.
-// Every hand-off is an mbarrier (or a named barrier inside the softmax
-// group); every wait is bounded: on a timeout the CTA flags kErrTimeoutFull or
+// One CTA per SM, in roles:
+//   softmax groups (4 warps each, one per 32-lane quarter of tensor memory):
+//              thread t owns token t of the tile and RG = min(R, 32) of its
+//              scores; the running max of a row moves only when a score
+//              passes it by more than 2^8 (a vote over the group decides), so
+//              P = 2^(s - m) < 256 in bf16 and the row sums stay per thread
+//              until the end of a piece; R / RG groups;
+//   4 correction warps: rescale O^T when a max moved, and write O (or the
+//              fp32 partial) at the end of a piece;
+//   1 MMA warp (one thread issues), 1 producer warp (tensor copies).
+// Every hand-off is an mbarrier (or a named barrier inside a softmax group);
+// every wait is bounded: on a timeout the CTA flags kErrTimeoutFull or
 // kErrTimeoutEmpty and returns after draining its copies and MMAs.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -42,50 +45,57 @@ namespace {
 
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
-constexpr int kRows = 16;                          // query rows per piece (one row group)
-constexpr int kTile = 128;                         // tokens per tile (MMA M)
-constexpr int kRegionBytes = kTile * 128;          // 16 KB: 128 rows x 64 dims
-constexpr int kUnitBytes = 2 * kRegionBytes;       // 32 KB ring unit: two regions
-constexpr int kRing = 6;
-constexpr int kSUnits = 5;                         // regions (0,1) (2,3) (4,5) (6,7) (8)
-constexpr int kVUnits = 4;                         // regions (0,1) .. (6,7): dim blocks of 128
-constexpr int kQRegion = kRows * 128;              // 2 KB: 16 rows x 64 dims
-constexpr int kPBytes = kRows * kTile * 2;         // 4 KB: P^T, 16 rows x 128 tokens
-constexpr int kQOff = kRing * kUnitBytes;          // 196,608
-constexpr int kPOff = kQOff + 9 * kQRegion;        // 215,040
-constexpr int kAlphaOff = kPOff + 2 * kPBytes;     // [2][16] f32
-constexpr int kLinvOff = kAlphaOff + 2 * kRows * 4;
-constexpr int kFlagOff = kLinvOff + 2 * kRows * 4;  // [2] int
-constexpr int kRedOff = kFlagOff + 16;             // [4][16] f32: per-warp row reductions
-constexpr int kBarOff = kRedOff + 4 * kRows * 4;
-enum : int {
-  B_FULL = 0,                 // [kRing] unit loaded (producer arrival + bytes)
-  B_EMPTY = B_FULL + kRing,   // [kRing] unit consumed (MMA commit)
-  B_QFULL = B_EMPTY + kRing,  // Q of the piece loaded
-  B_QFREE,                    // S^T MMAs of the piece's last tile done
-  B_SFULL,                    // [2] S^T buffer written (MMA commit)
-  B_SFREE = B_SFULL + 2,      // [2] S^T buffer read by the softmax group
-  B_DEC = B_SFREE + 2,        // [2] P^T written, rescale decided
-  B_PREADY = B_DEC + 2,       // [2] O^T ready for this tile's P.V
-  B_PVDONE = B_PREADY + 2,    // [2] P.V of the tile done (MMA commit)
-  B_OFREE = B_PVDONE + 2,     // O^T read by the epilogue
-  B_CORR,                     // the four correction warps are done with O^T (4 arrivals)
-  B_FINAL,                    // every MMA of the CTA done
-  B_DACK,                     // [2] the correction warps copied the tile's flag, alpha and 1/l (4 arrivals)
-  kBars = B_DACK + 2
-};
-constexpr int kSlotOff = kBarOff + kBars * 8;
-constexpr int kAbortOff = kSlotOff + 4;
-constexpr int kSmemUsed = kAbortOff + 4;
-constexpr int kSmemBytes = kSmemUsed + 1024;  // the base is rounded up to 1024 B (swizzle atoms)
-constexpr int kThreads = 320;
-constexpr int kMmaWarp = 8, kProdWarp = 9;
-constexpr uint32_t kCols = 128;               // S^T buffers at columns 0 and 16, O^T blocks at 32 + 16 mb
+constexpr int kTile = 128;                    // tokens per tile (MMA M)
+constexpr int kRegionBytes = kTile * 128;     // 16 KB: 128 rows x 64 dims
+constexpr int kUnitBytes = 2 * kRegionBytes;  // 32 KB ring unit: two regions
+constexpr int kSUnits = 5;                    // regions (0,1) (2,3) (4,5) (6,7) (8)
+constexpr int kVUnits = 4;                    // regions (0,1) .. (6,7): dim blocks of 128
 constexpr float kRescaleThreshold = 8.f;      // log2 units
 constexpr uint64_t kWaitNs = 2000000000ull;
-static_assert(kSmemBytes <= 227 * 1024, "tensor-memory MLA decode exceeds shared memory");
-static_assert(kQOff % 1024 == 0 && kPOff % 1024 == 0, "swizzle atoms need 1024-byte alignment");
-static_assert(kBarOff % 8 == 0, "mbarriers need 8-byte alignment");
+
+// Shared memory and roles for R query rows per piece.
+template <int R>
+struct TcCfg {
+  static constexpr int RG = R < 32 ? R : 32;         // rows per softmax group
+  static constexpr int kGroups = R / RG;             // 1 or 2
+  static constexpr int kSoftWarps = 4 * kGroups;
+  static constexpr int kMmaWarp = kSoftWarps;
+  static constexpr int kProdWarp = kSoftWarps + 1;
+  static constexpr int kThreads = (kSoftWarps + 2) * 32;
+  static constexpr int kRing = R == 16 ? 6 : 3;
+  static constexpr int kQRegion = R * 128;           // R rows x 64 dims
+  static constexpr int kPBytes = R * kTile * 2;      // P^T: R rows x 128 tokens
+  static constexpr int kQOff = kRing * kUnitBytes;
+  static constexpr int kPOff = kQOff + 9 * kQRegion;
+  static constexpr int kAlphaOff = kPOff + 2 * kPBytes;  // [R] f32: the rescale factor of each row
+  static constexpr int kLinvOff = kAlphaOff + R * 4;     // [R] f32: 1 / l of each row at a piece's end
+  static constexpr int kRedOff = kLinvOff + R * 4;       // [kGroups][4][RG] f32: per-warp row reductions
+  static constexpr int kBarOff = (kRedOff + kGroups * 4 * RG * 4 + 7) / 8 * 8;
+  // mbarriers
+  static constexpr int B_FULL = 0;                 // [kRing] unit loaded (producer arrival + bytes)
+  static constexpr int B_EMPTY = B_FULL + kRing;   // [kRing] unit consumed (MMA commit)
+  static constexpr int B_QFULL = B_EMPTY + kRing;  // Q of the piece loaded
+  static constexpr int B_QFREE = B_QFULL + 1;      // S^T MMAs of the piece's last tile done
+  static constexpr int B_SFULL = B_QFREE + 1;      // [2] S^T buffer written (MMA commit)
+  static constexpr int B_SFREE = B_SFULL + 2;      // [2] S^T buffer read (one arrival per softmax group)
+  static constexpr int B_PREADY = B_SFREE + 2;     // [2] P^T written and O^T rescaled (one per group)
+  static constexpr int B_PVDONE = B_PREADY + 2;    // [2] P.V of the tile done (MMA commit)
+  static constexpr int B_OFREE = B_PVDONE + 2;     // O^T read by the epilogue (one per group)
+  static constexpr int B_FINAL = B_OFREE + 1;      // every MMA of the CTA done
+  static constexpr int kBars = B_FINAL + 1;
+  static constexpr int kSlotOff = kBarOff + kBars * 8;
+  static constexpr int kAbortOff = kSlotOff + 4;
+  static constexpr int kSmemBytes = kAbortOff + 4 + 1024;  // the base is rounded up to 1024 B (swizzle atoms)
+  static constexpr uint32_t kCols = R == 16 ? 128 : 512;  // S^T at columns 0 and R, O^T block mb at 2R + R mb
+  static_assert(kSmemBytes <= 227 * 1024, "tensor-memory MLA decode exceeds shared memory");
+  static_assert(kQOff % 1024 == 0 && kPOff % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+  static_assert(2 * R + 4 * R <= static_cast<int>(kCols), "tensor memory columns");
+  __host__ __device__ static constexpr uint32_t bar_count(int i) {
+    return (i == B_SFREE || i == B_SFREE + 1 || i == B_PREADY || i == B_PREADY + 1 || i == B_OFREE)
+               ? static_cast<uint32_t>(kGroups)
+               : 1u;
+  }
+};
 
 struct TcTile {
   int b, hg, tt, t_loc, cnt, flags;
@@ -196,32 +206,33 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// Named barrier 1 over the four softmax warps (threads 0-127), with an AND / OR of a predicate.
-__device__ __forceinline__ bool group_and(bool v) {
+// Named barrier 1 + gi over the four warps of softmax group gi, with an AND / OR of a predicate.
+__device__ __forceinline__ bool group_and(int gi, bool v) {
   int r;
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.and.pred q, %2, 128, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(v ? 1 : 0)
+      : "r"(v ? 1 : 0), "r"(1 + gi)
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ bool group_or(bool v) {
+__device__ __forceinline__ bool group_or(int gi, bool v) {
   int r;
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, %2, 128, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(v ? 1 : 0)
+      : "r"(v ? 1 : 0), "r"(1 + gi)
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void group_sync(int gi) { asm volatile("bar.sync %0, 128;" ::"r"(1 + gi) : "memory"); }
 
-// Softmax group: warp 0 waits, the four warps get the same answer.
-__device__ __forceinline__ bool group_wait(uint32_t bar, uint32_t parity, volatile int* abort_s, int* err) {
+// Softmax group gi: its first warp waits, the four warps get the same answer.
+__device__ __forceinline__ bool group_wait(int gi, bool first_warp, uint32_t bar, uint32_t parity,
+                                           volatile int* abort_s, int* err) {
   bool ok = true;
-  if (threadIdx.x < 32) ok = warp_wait(bar, parity, abort_s, err, kErrTimeoutFull);
-  return group_and(ok);
+  if (first_warp) ok = warp_wait(bar, parity, abort_s, err, kErrTimeoutFull);
+  return group_and(gi, ok);
 }
 
 // Row of the 2D tensor copy that loads chunk c (BR rows) of the tile of
@@ -238,45 +249,55 @@ __device__ __forceinline__ int chunk_row(const MlaParams& p, int b, int tb, int 
   return (blk >= 0 && blk < p.num_blocks) ? blk * p.page_size + c_lo % p.page_size : zero_row;
 }
 
-template <int BR>
-__global__ void __launch_bounds__(kThreads, 1)
+// Register-array element i (i uniform or not) without local memory.
+template <int N>
+__device__ __forceinline__ float pick(const float (&a)[N], int i) {
+  float v = a[0];
+#pragma unroll
+  for (int k = 1; k < N; ++k) v = k == i ? a[k] : v;
+  return v;
+}
+
+template <int BR, int R>
+__global__ void __launch_bounds__(TcCfg<R>::kThreads, 1)
     gqa_mla_tc_decode_kernel(const MlaParams p, const __grid_constant__ MlaTcMaps maps) {
+  using C = TcCfg<R>;
+  constexpr int RG = C::RG;
   constexpr int kChunks = kTile / BR;
+  constexpr int kRing = C::kRing;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sm = smem_raw + (base - raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  volatile int* abort_s = reinterpret_cast<volatile int*>(sm + kAbortOff);
-  volatile int* flag_s = reinterpret_cast<volatile int*>(sm + kFlagOff);
-  float* alpha_s = reinterpret_cast<float*>(sm + kAlphaOff);
-  float* linv_s = reinterpret_cast<float*>(sm + kLinvOff);
-  float* red_s = reinterpret_cast<float*>(sm + kRedOff);
-  auto bar = [&](int i) { return base + kBarOff + 8u * static_cast<uint32_t>(i); };
+  volatile int* abort_s = reinterpret_cast<volatile int*>(sm + C::kAbortOff);
+  float* alpha_s = reinterpret_cast<float*>(sm + C::kAlphaOff);
+  float* linv_s = reinterpret_cast<float*>(sm + C::kLinvOff);
+  auto bar = [&](int i) { return base + C::kBarOff + 8u * static_cast<uint32_t>(i); };
 
   if (tid == 0) {
-    for (int i = 0; i < kBars; ++i) mbar_init(bar(i), (i == B_CORR || i == B_DACK || i == B_DACK + 1) ? 4u : 1u);
+    for (int i = 0; i < C::kBars; ++i) mbar_init(bar(i), C::bar_count(i));
     *abort_s = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
-  if (warp == 0) tc_alloc(base + kSlotOff, kCols);
+  if (warp == 0) tc_alloc(base + C::kSlotOff, C::kCols);
   pdl_launch_dependents();
   pdl_wait();  // kv_indptr comes from the scan kernel
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + kSlotOff);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + C::kSlotOff);
 
   const int T = __ldg(p.kv_indptr + p.batch);
-  const int HG = p.rows / kRows;
+  const int HG = p.rows / R;
   const Plan pl = make_plan(static_cast<int64_t>(T) * HG, p.plan);
   TcWalker wk;
   wk.init(p.kv_indptr, p.batch, T, pl, blockIdx.x);
   TcTile tl;
   int* err = p.err;
 
-  if (warp == kProdWarp) {
+  if (warp == C::kProdWarp) {
     // ------------------------------------------------------------ producer
     int n = 0, piece = 0;
     int prev_rows[kChunks];  // the previous tile: its V units follow this tile's S units
@@ -286,9 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ring unit n: regions r0 (and r0 + 1 when nreg = 2) of the tile's chunks
     auto load_unit = [&](int r0, int nreg, const int (&rows)[kChunks]) -> bool {
       const int s = n % kRing;
-      if (n >= kRing && !warp_wait(bar(B_EMPTY + s), ((n / kRing) - 1) & 1, abort_s, err, kErrTimeoutEmpty)) return false;
+      if (n >= kRing && !warp_wait(bar(C::B_EMPTY + s), ((n / kRing) - 1) & 1, abort_s, err, kErrTimeoutEmpty))
+        return false;
       if (lane == 0) {
-        const uint32_t full = bar(B_FULL + s);
+        const uint32_t full = bar(C::B_FULL + s);
         mbar_arrive_expect_tx(full, nreg * kRegionBytes);
         for (int g = 0; g < nreg; ++g)
 #pragma unroll
@@ -301,14 +323,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     while (wk.next(tl, lane, err)) {
       if (tl.flags & F_QLOAD) {
-        if (piece >= 1 && !warp_wait(bar(B_QFREE), (piece - 1) & 1, abort_s, err, kErrTimeoutEmpty)) {
+        if (piece >= 1 && !warp_wait(bar(C::B_QFREE), (piece - 1) & 1, abort_s, err, kErrTimeoutEmpty)) {
           good = false;
           break;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar(B_QFULL), 9 * kQRegion);
-          const int y = tl.b * p.rows + tl.hg * kRows;
-          for (int r = 0; r < 9; ++r) tma_load_2d(base + kQOff + r * kQRegion, &maps.q, 64 * r, y, bar(B_QFULL));
+          mbar_arrive_expect_tx(bar(C::B_QFULL), 9 * C::kQRegion);
+          const int y = tl.b * p.rows + tl.hg * R;
+          for (int r = 0; r < 9; ++r) tma_load_2d(base + C::kQOff + r * C::kQRegion, &maps.q, 64 * r, y, bar(C::B_QFULL));
         }
         __syncwarp();
         ++piece;
@@ -327,30 +349,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int u = 0; u < kVUnits && good && have_prev; ++u) good = load_unit(2 * u, 2, prev_rows);
     if (lane == 0) {  // no tensor copy may still be writing shared memory when the CTA exits
-      for (int i = n > kRing ? n - kRing : 0; i < n; ++i) drain_wait(bar(B_FULL + i % kRing), (i / kRing) & 1);
-      if (piece >= 1) drain_wait(bar(B_QFULL), (piece - 1) & 1);
+      for (int i = n > kRing ? n - kRing : 0; i < n; ++i) drain_wait(bar(C::B_FULL + i % kRing), (i / kRing) & 1);
+      if (piece >= 1) drain_wait(bar(C::B_QFULL), (piece - 1) & 1);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+  } else if (warp == C::kMmaWarp) {
     // ----------------------------------------------------------------- MMA
-    constexpr uint32_t idesc_s = tc_idesc_bf16(kTile, kRows, false, false);
-    constexpr uint32_t idesc_o = tc_idesc_bf16(128, kRows, true, false);
+    constexpr uint32_t idesc_s = tc_idesc_bf16(kTile, R, false, false);
+    constexpr uint32_t idesc_o = tc_idesc_bf16(128, R, true, false);
     int n = 0, j = 0, piece = -1;
     int pj = -1, p_first = 0, p_piece = 0;  // the tile whose P.V is pending
     bool good = true;
     auto take_unit = [&](int& s) -> bool {
       s = n % kRing;
-      if (!warp_wait(bar(B_FULL + s), (n / kRing) & 1, abort_s, err, kErrTimeoutFull)) return false;
+      if (!warp_wait(bar(C::B_FULL + s), (n / kRing) & 1, abort_s, err, kErrTimeoutFull)) return false;
       ++n;
       return true;
     };
     auto issue_pv = [&]() -> bool {
-      if (!warp_wait(bar(B_PREADY + (pj & 1)), (pj >> 1) & 1, abort_s, err, kErrTimeoutFull)) return false;
-      if (p_first && p_piece >= 1 && !warp_wait(bar(B_OFREE), (p_piece - 1) & 1, abort_s, err, kErrTimeoutFull))
+      if (!warp_wait(bar(C::B_PREADY + (pj & 1)), (pj >> 1) & 1, abort_s, err, kErrTimeoutFull)) return false;
+      if (p_first && p_piece >= 1 && !warp_wait(bar(C::B_OFREE), (p_piece - 1) & 1, abort_s, err, kErrTimeoutFull))
         return false;
       tc_fence_after();  // P^T and any O^T rescale were written by other threads before the barrier
-      // P^T: N = 16 rows in 8-row groups (SBO 2048), K = tokens in 8-token core matrices (LBO 128), no swizzle
-      const uint64_t dp = tc_sdesc(base + kPOff + (pj & 1) * kPBytes, 128, 16 * 128, kSwizzleNone);
+      // P^T: N = R rows in 8-row groups (SBO 2048), K = tokens in 8-token core matrices (LBO 128), no swizzle
+      const uint64_t dp = tc_sdesc(base + C::kPOff + (pj & 1) * C::kPBytes, 128, 16 * 128, kSwizzleNone);
       for (int u = 0; u < kVUnits; ++u) {
         int s;
         if (!take_unit(s)) return false;
@@ -359,13 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t dv = tc_sdesc(base + s * kUnitBytes, kRegionBytes, 1024, kSwizzle128B);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            tc_mma_bf16(tmem + 32 + 16 * u, dv + ((kk * 2048) >> 4), dp + ((kk * 256) >> 4), idesc_o,
+            tc_mma_bf16(tmem + 2 * R + R * u, dv + ((kk * 2048) >> 4), dp + ((kk * 256) >> 4), idesc_o,
                         (p_first && kk == 0) ? 0u : 1u);
-          tc_commit(bar(B_EMPTY + s));
+          tc_commit(bar(C::B_EMPTY + s));
         }
         __syncwarp();
       }
-      if (lane == 0) tc_commit(bar(B_PVDONE + (pj & 1)));
+      if (lane == 0) tc_commit(bar(C::B_PVDONE + (pj & 1)));
       __syncwarp();
       return true;
     };
@@ -373,17 +395,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sb = j & 1;
       if (tl.flags & F_QLOAD) {
         ++piece;
-        if (!warp_wait(bar(B_QFULL), piece & 1, abort_s, err, kErrTimeoutFull)) {
+        if (!warp_wait(bar(C::B_QFULL), piece & 1, abort_s, err, kErrTimeoutFull)) {
           good = false;
           break;
         }
       }
-      if (j >= 2 && !warp_wait(bar(B_SFREE + sb), ((j >> 1) - 1) & 1, abort_s, err, kErrTimeoutFull)) {
+      if (j >= 2 && !warp_wait(bar(C::B_SFREE + sb), ((j >> 1) - 1) & 1, abort_s, err, kErrTimeoutFull)) {
         good = false;
         break;
       }
-      // Q as B: N = 16 rows (SBO 1024), K-major, 128-byte swizzle, one 2 KB region per 64 dims
-      const uint64_t dq = tc_sdesc(base + kQOff, 16, 1024, kSwizzle128B);
+      // Q as B: N = R rows (SBO 1024 per 8 rows), K-major, 128-byte swizzle, one region per 64 dims
+      const uint64_t dq = tc_sdesc(base + C::kQOff, 16, 1024, kSwizzle128B);
       for (int u = 0; u < kSUnits && good; ++u) {
         int s;
         if (!take_unit(s)) {
@@ -391,22 +413,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (lane == 0) {
-          // K rows as A (tensor-copied data: the full barrier alone orders it before the MMA): M = 128 tokens (SBO 1024), K-major, 128-byte swizzle, 16 KB per region
+          // K rows as A (tensor-copied data: the full barrier alone orders it before the MMA):
+          // M = 128 tokens (SBO 1024), K-major, 128-byte swizzle, 16 KB per region
           const uint64_t dk = tc_sdesc(base + s * kUnitBytes, 16, 1024, kSwizzle128B);
           const int nreg = u < 4 ? 2 : 1;
           for (int g = 0; g < nreg; ++g)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              tc_mma_bf16(tmem + 16 * sb, dk + ((g * kRegionBytes + kk * 32) >> 4),
-                          dq + (((2 * u + g) * kQRegion + kk * 32) >> 4), idesc_s, (u | g | kk) ? 1u : 0u);
-          tc_commit(bar(B_EMPTY + s));
+              tc_mma_bf16(tmem + R * sb, dk + ((g * kRegionBytes + kk * 32) >> 4),
+                          dq + (((2 * u + g) * C::kQRegion + kk * 32) >> 4), idesc_s, (u | g | kk) ? 1u : 0u);
+          tc_commit(bar(C::B_EMPTY + s));
         }
         __syncwarp();
       }
       if (!good) break;
       if (lane == 0) {
-        tc_commit(bar(B_SFULL + sb));
-        if (tl.flags & F_END) tc_commit(bar(B_QFREE));
+        tc_commit(bar(C::B_SFULL + sb));
+        if (tl.flags & F_END) tc_commit(bar(C::B_QFREE));
       }
       __syncwarp();
       if (pj >= 0 && !issue_pv()) {
@@ -420,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (good && pj >= 0) issue_pv();
     if (lane == 0) {  // every MMA done before tensor memory is freed
-      tc_commit(bar(B_FINAL));
-      drain_wait(bar(B_FINAL), 0);
+      tc_commit(bar(C::B_FINAL));
+      drain_wait(bar(C::B_FINAL), 0);
       if (wk.u0 < wk.u1 && wk.ok) {  // the split record of the CTA's last piece, as the merge reads it
         p.split_rec[blockIdx.x] =
             make_int4(static_cast<int>(static_cast<unsigned>(p.epoch)), wk.pb, wk.p_si.first_cta, wk.p_si.S);
@@ -429,13 +452,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ------------------------------------------------------------- softmax
-    const int tok = 32 * warp + lane;  // token of the tile = tensor-memory lane of S^T
+  } else if (warp < C::kSoftWarps) {
+    // ----------------------------------------------- softmax, rescale, epilogue (group gi: rows gi RG ..)
+    const int gi = warp >> 2, wq = warp & 3;  // group, tensor-memory quarter (tokens / dims 32 wq ..)
+    const int ti = tid - 128 * gi;            // thread within the group
+    const bool first_warp = wq == 0;
+    const int tok = 32 * wq + lane;           // token of the tile = tensor-memory lane of S^T
     const bool even = (lane & 1) == 0;
-    float m_used[kRows], l_part[kRows];
+    float* red_s = reinterpret_cast<float*>(sm + C::kRedOff) + gi * 4 * RG;
+    const uint32_t orow = tmem + (static_cast<uint32_t>(32 * wq) << 16) + 2 * R + gi * RG;  // this group's O^T columns
+    float m_used[RG], l_part[RG];
 #pragma unroll
-    for (int r = 0; r < kRows; ++r) {
+    for (int r = 0; r < RG; ++r) {
       m_used[r] = -INFINITY;
       l_part[r] = 0.f;
     }
@@ -445,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool first = (tl.flags & F_QLOAD) != 0;
       if (first) {
 #pragma unroll
-        for (int r = 0; r < kRows; ++r) {
+        for (int r = 0; r < RG; ++r) {
           m_used[r] = -INFINITY;
           l_part[r] = 0.f;
         }
@@ -454,195 +482,153 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tb = tl.t_loc & ~(kTile - 1);
       int blk_ok = 1;
       if (lane == 0) {
-        const int lp = (tb + 32 * warp) / p.page_size;
+        const int lp = (tb + 32 * wq) / p.page_size;
         const int blk = lp < p.width ? __ldg(p.block_table + static_cast<int64_t>(tl.b) * p.width + lp) : -1;
         blk_ok = blk >= 0 && blk < p.num_blocks;
       }
       blk_ok = __shfl_sync(0xffffffffu, blk_ok, 0);
       const int t_abs = tb + tok;
       const bool valid = blk_ok && t_abs >= tl.t_loc && t_abs < tl.t_loc + tl.cnt;
-      if (!group_wait(bar(B_SFULL + sb), (j >> 1) & 1, abort_s, err)) break;
+      if (!group_wait(gi, first_warp, bar(C::B_SFULL + sb), (j >> 1) & 1, abort_s, err)) break;
       tc_fence_after();
-      uint32_t v[16];
-      tc_ld16(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 16 * sb, v);
-      tc_wait_ld();
-      float x[kRows];
+      float x[RG];
       bool exceed = false;
 #pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        x[r] = valid ? __uint_as_float(v[r]) * p.scale_log2 : -INFINITY;
-        exceed |= x[r] > m_used[r] + kRescaleThreshold;
+      for (int h = 0; h < RG / 16; ++h) {
+        uint32_t v[16];
+        tc_ld16(tmem + (static_cast<uint32_t>(32 * wq) << 16) + R * sb + gi * RG + 16 * h, v);
+        tc_wait_ld();
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          x[16 * h + r] = valid ? __uint_as_float(v[r]) * p.scale_log2 : -INFINITY;
+          exceed |= x[16 * h + r] > m_used[16 * h + r] + kRescaleThreshold;
+        }
       }
       tc_fence_before();
-      const bool any_exceed = group_or(exceed);  // also: every warp has read S^T buffer sb
-      if (threadIdx.x == 0) mbar_arrive(bar(B_SFREE + sb));
-      float alpha[kRows];
-#pragma unroll
-      for (int r = 0; r < kRows; ++r) alpha[r] = 1.f;
+      const bool any_exceed = group_or(gi, exceed);  // also: the group's four warps have read S^T buffer sb
+      if (ti == 0) mbar_arrive(bar(C::B_SFREE + sb));
       bool moved = false;
       if (any_exceed) {  // per-row maximum of the tile over the 128 tokens; move the rows it passes by > 2^8
 #pragma unroll
-        for (int r = 0; r < kRows; ++r) {
+        for (int r = 0; r < RG; ++r) {
           float m = x[r];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          if (lane == r) red_s[warp * kRows + r] = m;
+          if (lane == r) red_s[wq * RG + r] = m;
         }
-        group_sync();
+        group_sync(gi);
 #pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-          const float tmax =
-              fmaxf(fmaxf(red_s[r], red_s[kRows + r]), fmaxf(red_s[2 * kRows + r], red_s[3 * kRows + r]));
+        for (int r = 0; r < RG; ++r) {
+          const float tmax = fmaxf(fmaxf(red_s[r], red_s[RG + r]), fmaxf(red_s[2 * RG + r], red_s[3 * RG + r]));
+          float a = 1.f;
           if (tmax > m_used[r] + kRescaleThreshold) {
-            alpha[r] = m_used[r] == -INFINITY ? 0.f : ex2(m_used[r] - tmax);
+            a = m_used[r] == -INFINITY ? 0.f : ex2(m_used[r] - tmax);
             m_used[r] = tmax;
-            l_part[r] *= alpha[r];
+            l_part[r] *= a;
             moved = true;
           }
+          if (ti == r) alpha_s[gi * RG + r] = a;
         }
-        group_sync();  // red_s is reused
+        group_sync(gi);  // red_s is reused; alpha_s is written
       }
-      const bool rescale = moved && !first;  // the same in every thread
-      float pr[kRows];
-#pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        pr[r] = m_used[r] == -INFINITY ? 0.f : ex2(x[r] - m_used[r]);
-        l_part[r] += pr[r];
-      }
-      // P^T as the K-major B operand (N = 16 rows, K = 128 tokens, no swizzle): element (r, t) at
-      // (r / 8) * 2048 + (t / 8) * 128 + (r % 8) * 16 + (t % 8) * 2. Lane pairs swap halves so the even
-      // lane writes rows 0-7 and the odd lane rows 8-15 of tokens (t, t + 1), 4 bytes each.
-      uint32_t pk[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float other = __shfl_xor_sync(0xffffffffu, even ? pr[8 + i] : pr[i], 1);
-        pk[i] = even ? pack_bf16(pr[i], other) : pack_bf16(other, pr[8 + i]);
-      }
+      const bool rescale = moved && !first;  // the same in every thread of the group
       // P^T buffer sb was last read by the P.V of tile j - 2
-      if (j >= 2 && !group_wait(bar(B_PVDONE + sb), ((j >> 1) - 1) & 1, abort_s, err)) break;
+      if (j >= 2 && !group_wait(gi, first_warp, bar(C::B_PVDONE + sb), ((j >> 1) - 1) & 1, abort_s, err)) break;
+      // P = 2^(s - m), row sums, and P^T as the K-major B operand (N = R rows, K = 128 tokens, no
+      // swizzle): element (r, t) at (r / 8) * 2048 + (t / 8) * 128 + (r % 8) * 16 + (t % 8) * 2. Lane
+      // pairs swap halves so the even lane writes the group's first RG / 2 rows and the odd lane the
+      // others, for tokens (t, t + 1), 4 bytes each.
       {
         const int te = tok & ~1;
-        const uint32_t pb0 = base + kPOff + sb * kPBytes + (even ? 0 : 2048) + (te >> 3) * 128 + (te & 7) * 2;
+        const uint32_t pbase = base + C::kPOff + sb * C::kPBytes + (te >> 3) * 128 + (te & 7) * 2;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) asm volatile("st.shared.u32 [%0], %1;" ::"r"(pb0 + i * 16), "r"(pk[i]) : "memory");
+        for (int i = 0; i < RG / 2; ++i) {
+          const int hi = RG / 2 + i;
+          const float plo = m_used[i] == -INFINITY ? 0.f : ex2(x[i] - m_used[i]);
+          const float phi = m_used[hi] == -INFINITY ? 0.f : ex2(x[hi] - m_used[hi]);
+          l_part[i] += plo;
+          l_part[hi] += phi;
+          const float other = __shfl_xor_sync(0xffffffffu, even ? phi : plo, 1);
+          const uint32_t pk = even ? pack_bf16(plo, other) : pack_bf16(other, phi);
+          const int r = gi * RG + (even ? 0 : RG / 2) + i;
+          asm volatile("st.shared.u32 [%0], %1;" ::"r"(pbase + (r >> 3) * 2048 + (r & 7) * 16), "r"(pk) : "memory");
+        }
       }
       fence_proxy_async_smem();
-      // the correction warps copied slot sb's flag, alpha and 1/l of tile j - 2
-      if (j >= 2 && !group_wait(bar(B_DACK + sb), ((j >> 1) - 1) & 1, abort_s, err)) break;
-      if (rescale && threadIdx.x < kRows) {
-        float a = alpha[0];
-#pragma unroll
-        for (int r = 1; r < kRows; ++r) a = r == static_cast<int>(threadIdx.x) ? alpha[r] : a;
-        alpha_s[sb * kRows + threadIdx.x] = a;
-      }
-      if (tl.flags & F_END) {  // row sums over the 128 threads; 1/l and the LSE of each row
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-          float s = l_part[r];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-          if (lane == r) red_s[warp * kRows + r] = s;
-        }
-        group_sync();
-        if (threadIdx.x < kRows) {
-          const int r = threadIdx.x;
-          const float l = red_s[r] + red_s[kRows + r] + red_s[2 * kRows + r] + red_s[3 * kRows + r];
-          linv_s[sb * kRows + r] = l > 0.f ? 1.f / l : 0.f;
-          float mr = m_used[0];
-#pragma unroll
-          for (int rr = 1; rr < kRows; ++rr) mr = rr == r ? m_used[rr] : mr;
-          const float lse2 = l > 0.f ? mr + log2f(l) : -INFINITY;  // base 2
-          if (tl.flags & F_FINAL) {
-            if (p.lse != nullptr) store_lse_nat(p, tl.b, tl.hg * kRows + r, lse2);
-          } else {
-            p.part_lse[slot_id(blockIdx.x, (tl.flags & F_SLOT1) ? 1 : 0) * kRows + r] = lse2;
-          }
-        }
-      }
-      group_sync();  // P^T, alpha and 1/l written by the whole group; red_s free again
-      if (threadIdx.x == 0) {
-        flag_s[sb] = rescale ? 1 : 0;
-        mbar_arrive(bar(B_DEC + sb));
-        if (!rescale) mbar_arrive(bar(B_PREADY + sb));
-      }
-      ++j;
-    }
-  } else if (warp < 8) {
-    // ------------------------------------------------ correction, epilogue
-    const int q = warp - 4;  // tensor-memory lanes 32 q .. 32 q + 31: dims 128 mb + 32 q + lane
-    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16) + 32;
-    int j = 0, uses = 0;
-    while (wk.next(tl, lane, err)) {
-      const int sb = j & 1;
-      if (!warp_wait(bar(B_DEC + sb), (j >> 1) & 1, abort_s, err, kErrTimeoutFull)) break;
-      const bool fix = flag_s[sb] != 0, end = (tl.flags & F_END) != 0;
-      float a[kRows], inv[kRows];
-#pragma unroll
-      for (int rr = 0; rr < kRows; ++rr) {
-        a[rr] = fix ? alpha_s[sb * kRows + rr] : 1.f;
-        inv[rr] = end ? linv_s[sb * kRows + rr] : 0.f;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DACK + sb));  // slot sb may be reused for tile j + 2
-      if (fix) {  // O^T *= alpha per row, after the P.V of tile j - 1
-        if (!warp_wait(bar(B_PVDONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_s, err, kErrTimeoutFull)) break;
+      if (rescale) {  // O^T *= alpha on this group's rows, once the P.V of tile j - 1 is done
+        if (!group_wait(gi, first_warp, bar(C::B_PVDONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_s, err)) break;
         tc_fence_after();
+#pragma unroll 1
+        for (int mb = 0; mb < kDv / 128; ++mb)
 #pragma unroll
-        for (int mb = 0; mb < kDv / 128; ++mb) {
-          uint32_t o[16];
-          tc_ld16(trow + 16 * mb, o);
-          tc_wait_ld();
+          for (int c = 0; c < RG / 16; ++c) {
+            uint32_t o[16];
+            tc_ld16(orow + R * mb + 16 * c, o);
+            tc_wait_ld();
 #pragma unroll
-          for (int rr = 0; rr < kRows; ++rr) o[rr] = __float_as_uint(__uint_as_float(o[rr]) * a[rr]);
-          tc_st16(trow + 16 * mb, o);
-        }
+            for (int rr = 0; rr < 16; ++rr)
+              o[rr] = __float_as_uint(__uint_as_float(o[rr]) * alpha_s[gi * RG + 16 * c + rr]);
+            tc_st16(orow + R * mb + 16 * c, o);
+          }
         tc_wait_st();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_CORR));
-        if (q == 0) {
-          if (!warp_wait(bar(B_CORR), uses & 1, abort_s, err, kErrTimeoutFull)) break;
-          if (lane == 0) mbar_arrive(bar(B_PREADY + sb));
-        }
-        ++uses;
       }
-      if (end) {  // O = O^T / l after the piece's last P.V
-        if (!warp_wait(bar(B_PVDONE + sb), (j >> 1) & 1, abort_s, err, kErrTimeoutFull)) break;
+      group_sync(gi);  // P^T written (and O^T rescaled) by the whole group
+      if (ti == 0) mbar_arrive(bar(C::B_PREADY + sb));
+      if (tl.flags & F_END) {  // row sums over the 128 threads, 1/l and the LSE; O = O^T / l after P.V of tile j
+#pragma unroll
+        for (int r = 0; r < RG; ++r) {
+          float sum = l_part[r];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          if (lane == r) red_s[wq * RG + r] = sum;
+        }
+        group_sync(gi);
+        if (ti < RG) {
+          const float l = red_s[ti] + red_s[RG + ti] + red_s[2 * RG + ti] + red_s[3 * RG + ti];
+          linv_s[gi * RG + ti] = l > 0.f ? 1.f / l : 0.f;
+          const float lse2 = l > 0.f ? pick(m_used, ti) + log2f(l) : -INFINITY;  // base 2
+          const int row = gi * RG + ti;  // row of the piece
+          if (tl.flags & F_FINAL) {
+            if (p.lse != nullptr) store_lse_nat(p, tl.b, tl.hg * R + row, lse2);
+          } else {
+            p.part_lse[slot_id(blockIdx.x, (tl.flags & F_SLOT1) ? 1 : 0) * R + row] = lse2;
+          }
+        }
+        if (!group_wait(gi, first_warp, bar(C::B_PVDONE + sb), (j >> 1) & 1, abort_s, err)) break;  // also syncs linv_s
         tc_fence_after();
         const bool fin = (tl.flags & F_FINAL) != 0;
         const int64_t sid = slot_id(blockIdx.x, (tl.flags & F_SLOT1) ? 1 : 0);
+#pragma unroll 1
+        for (int mb = 0; mb < kDv / 128; ++mb)
 #pragma unroll
-        for (int mb = 0; mb < kDv / 128; ++mb) {
-          uint32_t o[16];
-          tc_ld16(trow + 16 * mb, o);
-          tc_wait_ld();
-          const int dim = 128 * mb + 32 * q + lane;
-          if (fin) {
-            __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) +
-                                (static_cast<int64_t>(tl.b) * p.rows + tl.hg * kRows) * kDv + dim;
+          for (int c = 0; c < RG / 16; ++c) {
+            uint32_t o[16];
+            tc_ld16(orow + R * mb + 16 * c, o);
+            tc_wait_ld();
+            const int dim = 128 * mb + tok;  // tensor-memory lane of O^T = dim within the 128-dim block
+            const int row0 = gi * RG + 16 * c;
+            if (fin) {
+              __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) +
+                                  (static_cast<int64_t>(tl.b) * p.rows + tl.hg * R + row0) * kDv + dim;
 #pragma unroll
-            for (int rr = 0; rr < kRows; ++rr) ob[rr * kDv] = __float2bfloat16(__uint_as_float(o[rr]) * inv[rr]);
-          } else {
-            float* po = p.part_o + sid * (kRows * kDv) + dim;
+              for (int rr = 0; rr < 16; ++rr) ob[rr * kDv] = __float2bfloat16(__uint_as_float(o[rr]) * linv_s[row0 + rr]);
+            } else {
+              float* po = p.part_o + (sid * R + row0) * kDv + dim;
 #pragma unroll
-            for (int rr = 0; rr < kRows; ++rr) po[rr * kDv] = __uint_as_float(o[rr]) * inv[rr];
+              for (int rr = 0; rr < 16; ++rr) po[rr * kDv] = __uint_as_float(o[rr]) * linv_s[row0 + rr];
+            }
           }
-        }
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_CORR));
-        if (q == 0) {
-          if (!warp_wait(bar(B_CORR), uses & 1, abort_s, err, kErrTimeoutFull)) break;
-          if (lane == 0) mbar_arrive(bar(B_OFREE));
-        }
-        ++uses;
+        group_sync(gi);  // the group's O^T reads are done (and linv_s / red_s may be reused)
+        if (ti == 0) mbar_arrive(bar(C::B_OFREE));
       }
       ++j;
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tc_dealloc(tmem, kCols);
+  if (warp == 0) tc_dealloc(tmem, C::kCols);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
@@ -672,41 +658,46 @@ bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, int box_rows)
 
 int box_rows_for(int page_size) { return page_size % 64 == 0 ? 64 : 32; }
 
-}  // namespace
-
-bool mla_tc_supported(int page_size) { return page_size > 0 && page_size % 32 == 0; }
-
-bool mla_tc_encode(const MlaParams& p, MlaTcMaps* maps) {
-  return encode_rows(&maps->kv, p.kv, static_cast<int64_t>(p.num_blocks) * p.page_size, box_rows_for(p.page_size)) &&
-         encode_rows(&maps->q, p.q, static_cast<int64_t>(p.batch) * p.rows, kRows);
-}
-
-cudaError_t launch_mla_tc_decode(const MlaParams& p, const MlaTcMaps& maps, int ctas, cudaStream_t stream) {
-  const bool br64 = box_rows_for(p.page_size) == 64;
-  static int configured[64][2] = {};
+template <int BR, int R>
+cudaError_t launch_tc(const MlaParams& p, const MlaTcMaps& maps, int ctas, cudaStream_t stream) {
+  static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  const int vi = br64 ? 1 : 0;
-  if (dev >= 0 && dev < 64 && !configured[dev][vi]) {
-    const cudaError_t e = br64 ? cudaFuncSetAttribute(gqa_mla_tc_decode_kernel<64>,
-                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)
-                               : cudaFuncSetAttribute(gqa_mla_tc_decode_kernel<32>,
-                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(gqa_mla_tc_decode_kernel<BR, R>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<R>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[dev][vi] = 1;
+    configured[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.blockDim = dim3(TcCfg<R>::kThreads);
+  cfg.dynamicSmemBytes = TcCfg<R>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return br64 ? cudaLaunchKernelEx(&cfg, gqa_mla_tc_decode_kernel<64>, p, maps)
-              : cudaLaunchKernelEx(&cfg, gqa_mla_tc_decode_kernel<32>, p, maps);
+  return cudaLaunchKernelEx(&cfg, gqa_mla_tc_decode_kernel<BR, R>, p, maps);
+}
+
+}  // namespace
+
+bool mla_tc_supported(int page_size) { return page_size > 0 && page_size % 32 == 0; }
+
+int mla_tc_piece_rows(int rows) { return rows % 64 == 0 ? 64 : 16; }
+
+bool mla_tc_encode(const MlaParams& p, MlaTcMaps* maps) {
+  return encode_rows(&maps->kv, p.kv, static_cast<int64_t>(p.num_blocks) * p.page_size, box_rows_for(p.page_size)) &&
+         encode_rows(&maps->q, p.q, static_cast<int64_t>(p.batch) * p.rows, p.piece_rows);
+}
+
+cudaError_t launch_mla_tc_decode(const MlaParams& p, const MlaTcMaps& maps, int ctas, cudaStream_t stream) {
+  const bool br64 = box_rows_for(p.page_size) == 64;
+  if (p.piece_rows == 64)
+    return br64 ? launch_tc<64, 64>(p, maps, ctas, stream) : launch_tc<32, 64>(p, maps, ctas, stream);
+  return br64 ? launch_tc<64, 16>(p, maps, ctas, stream) : launch_tc<32, 16>(p, maps, ctas, stream);
 }
 
 }  // namespace gqa

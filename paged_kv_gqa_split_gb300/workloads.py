@@ -444,9 +444,14 @@ def make_mla_workload(lens: Sequence[int], h_q: int, s_q: int, page_size: int, s
 MLA_CONFIG = dict(batch=128, h_q=16, s_q=1, page_size=64, len_lo=1024, len_hi=8192, seed=6, pool_factor=1.25)
 
 
-def make_mla_config() -> MlaWorkload:
-    c = MLA_CONFIG
+# The same batch with 64 query heads sharing each latent row (h_q = 64, as in a
+# 128-head model split over two GPUs): one pass over the cache serves 64 rows.
+MLA_WIDE_CONFIG = dict(MLA_CONFIG, h_q=64)
+
+
+def make_mla_config(wide: bool = False) -> MlaWorkload:
+    c = MLA_WIDE_CONFIG if wide else MLA_CONFIG
     g = torch.Generator().manual_seed(c["seed"])
     lens = torch.randint(c["len_lo"], c["len_hi"] + 1, (c["batch"],), generator=g).tolist()
     return make_mla_workload(lens, c["h_q"], c["s_q"], c["page_size"], c["seed"] + 1000,
-                             pool_factor=c["pool_factor"], name="mla")
+                             pool_factor=c["pool_factor"], name="mla_wide" if wide else "mla")

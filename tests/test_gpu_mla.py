@@ -168,3 +168,34 @@ def test_mla_tensor_memory_shapes(lens, h_q, s_q, ps, seed, ctas):
     check(w, *outs[0])
     (o1, l1), (o3, l3) = outs
     assert np.all(np.abs(o1 - o3) <= 2 * (O_ATOL + O_RTOL * np.abs(o3)))
+
+
+@pytest.mark.parametrize("lens,h_q,s_q,ps,seed,ctas,kernel", [
+    ([900, 1, 0, 130], 64, 1, 64, 41, 0, 0),              # one 64-row piece per sequence (default kernel)
+    ([700, 257], 128, 1, 64, 42, 0, 1),                   # two 64-row groups
+    ([600, 33, 128], 32, 2, 32, 43, 0, 1),                # 2 query tokens x 32 heads, 32-row copies
+    ([3000, 5, 2000], 64, 1, 128, 44, 9, 1),              # few CTAs: several pieces and Q reloads per CTA
+    ([4096, 4096, 4095], 64, 1, 64, 45, 300, 1),          # many pieces per sequence: the merge's long chains
+])
+def test_mla_wide_pieces(lens, h_q, s_q, ps, seed, ctas, kernel):
+    """64-row pieces of the tensor-memory kernel (a sequence's rows in multiples of 64), against the
+    oracle and against the mma.sync kernel (16-row pieces) on the same inputs."""
+    w = wl.make_mla_workload(lens, h_q, s_q, ps, seed)
+    assert _lib.gqa_paged_decode_set_tuning(ctas, 0, 0, 0, 0, 0) == 0
+    assert _lib.gqa_mla_set_tuning(kernel) == 0
+    o1, l1 = gpu_mla(w)
+    check(w, o1, l1)
+    assert _lib.gqa_mla_set_tuning(3) == 0
+    o3, l3 = gpu_mla(w)
+    assert np.all(np.abs(o1 - o3) <= 2 * (O_ATOL + O_RTOL * np.abs(o3)))
+
+
+def test_mla_wide_holes_and_long_lengths():
+    w = wl.make_mla_workload([700, 300, 129], 64, 1, 64, seed=46)
+    w.block_table[0, 3] = -1                    # a hole: tokens 192..255 of sequence 0 are left out
+    w.block_table[1, 1] = w.kv_cache.shape[0] + 7
+    w.cache_seqlens[2] = 10 ** 6                # past the table: counts as width * page_size
+    w.lens[2] = 10 ** 6
+    assert _lib.gqa_mla_set_tuning(1) == 0
+    out, lse = gpu_mla(w)
+    check(w, out, lse)
