@@ -62,12 +62,13 @@ struct TcCfg {
   static constexpr int kMmaWarp = kSoftWarps;
   static constexpr int kProdWarp = kSoftWarps + 1;
   static constexpr int kThreads = (kSoftWarps + 2) * 32;
-  static constexpr int kRing = R == 16 ? 6 : 3;
+  static constexpr int kRing = R == 16 ? 6 : 4;
+  static constexpr int kPBufs = R == 16 ? 2 : 1;    // P^T buffers (one at R = 64 leaves room for a 4th unit)
   static constexpr int kQRegion = R * 128;           // R rows x 64 dims
   static constexpr int kPBytes = R * kTile * 2;      // P^T: R rows x 128 tokens
   static constexpr int kQOff = kRing * kUnitBytes;
   static constexpr int kPOff = kQOff + 9 * kQRegion;
-  static constexpr int kAlphaOff = kPOff + 2 * kPBytes;  // [R] f32: the rescale factor of each row
+  static constexpr int kAlphaOff = kPOff + kPBufs * kPBytes;  // [R] f32: the rescale factor of each row
   static constexpr int kLinvOff = kAlphaOff + R * 4;     // [R] f32: 1 / l of each row at a piece's end
   static constexpr int kRedOff = kLinvOff + R * 4;       // [kGroups][4][RG] f32: per-warp row reductions
   static constexpr int kBarOff = (kRedOff + kGroups * 4 * RG * 4 + 7) / 8 * 8;
@@ -372,7 +373,7 @@ __global__ void __launch_bounds__(TcCfg<R>::kThreads, 1)
         return false;
       tc_fence_after();  // P^T and any O^T rescale were written by other threads before the barrier
       // P^T: N = R rows in 8-row groups (SBO 2048), K = tokens in 8-token core matrices (LBO 128), no swizzle
-      const uint64_t dp = tc_sdesc(base + C::kPOff + (pj & 1) * C::kPBytes, 128, 16 * 128, kSwizzleNone);
+      const uint64_t dp = tc_sdesc(base + C::kPOff + (pj % C::kPBufs) * C::kPBytes, 128, 16 * 128, kSwizzleNone);
       for (int u = 0; u < kVUnits; ++u) {
         int s;
         if (!take_unit(s)) return false;
@@ -532,15 +533,18 @@ __global__ void __launch_bounds__(TcCfg<R>::kThreads, 1)
         group_sync(gi);  // red_s is reused; alpha_s is written
       }
       const bool rescale = moved && !first;  // the same in every thread of the group
-      // P^T buffer sb was last read by the P.V of tile j - 2
-      if (j >= 2 && !group_wait(gi, first_warp, bar(C::B_PVDONE + sb), ((j >> 1) - 1) & 1, abort_s, err)) break;
+      // P^T buffer j % kPBufs was last read by the P.V of tile j - kPBufs
+      if (j >= C::kPBufs) {
+        const int jp = j - C::kPBufs;
+        if (!group_wait(gi, first_warp, bar(C::B_PVDONE + (jp & 1)), (jp >> 1) & 1, abort_s, err)) break;
+      }
       // P = 2^(s - m), row sums, and P^T as the K-major B operand (N = R rows, K = 128 tokens, no
       // swizzle): element (r, t) at (r / 8) * 2048 + (t / 8) * 128 + (r % 8) * 16 + (t % 8) * 2. Lane
       // pairs swap halves so the even lane writes the group's first RG / 2 rows and the odd lane the
       // others, for tokens (t, t + 1), 4 bytes each.
       {
         const int te = tok & ~1;
-        const uint32_t pbase = base + C::kPOff + sb * C::kPBytes + (te >> 3) * 128 + (te & 7) * 2;
+        const uint32_t pbase = base + C::kPOff + (j % C::kPBufs) * C::kPBytes + (te >> 3) * 128 + (te & 7) * 2;
 #pragma unroll
         for (int i = 0; i < RG / 2; ++i) {
           const int hi = RG / 2 + i;
