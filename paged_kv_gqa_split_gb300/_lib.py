@@ -405,8 +405,9 @@ MLA_D_QK, MLA_D_V = 576, 512
 
 
 def gqa_mla_set_tuning(kernel: int) -> int:
-    """MLA decode kernel: 0 default (mma.sync, 3 stages), 1 the tensor-memory kernel
-    (block sizes that are a multiple of 32), 3 or 4 the mma.sync kernel with that ring depth."""
+    """MLA decode kernel: 0 default (the tensor-memory kernel for 64-row multiples and block sizes
+    that are a multiple of 32, else mma.sync with 3 stages), 1 the tensor-memory kernel (block
+    sizes that are a multiple of 32), 3 or 4 the mma.sync kernel with that ring depth."""
     return load().gqa_mla_set_tuning(kernel)
 
 
