@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(kMlaThreads, CPS) gqa_mla_decode_kernel(const 
 // path: it finds the sequence cut there from CTA j's record and, being rank
 // r of its S - 1 boundary CTAs, merges a share of the 512 output dims of the
 // piece's rows (p.piece_rows: 16 for the mma.sync kernel, 16 or 64 for the
-// tensor-memory kernel) over all S pieces. While S * rows fits the weight
+// tensor-memory kernel; one CTA per 16 rows of a piece) over all S pieces. While S * rows fits the weight
 // table, the weight of every (piece, row), 2^(lse_s - max) / sum, is
 // computed once into shared memory and each output element is then one
 // weighted sum of independent loads; longer chains take a running-max loop.
@@ -507,16 +507,17 @@ constexpr int kMlaMergeBatch = 4;  // float4 columns per thread per pass
 __global__ void __launch_bounds__(kMlaMergeThreads) gqa_mla_merge_kernel(const MlaParams p) {
   __shared__ float wsh[kMlaMergeWeights];  // [piece][row]
   const int R = p.piece_rows;                // rows per piece: 16 or 64
+  const int G = R / kMlaRows;                // CTAs per boundary, each merging 16 rows of the piece
   const int tid = threadIdx.x;
   const int B = p.batch;
-  const int j = blockIdx.x;
+  const int j = blockIdx.x / G, row0 = (blockIdx.x - j * G) * kMlaRows;
   const bool boundary = j + 1 < p.plan.tier1_ctas + p.plan.tier2_ctas;
   const int T = __ldg(p.kv_indptr + B);
   pdl_wait();
   const int4 rec0 = boundary ? __ldcg(p.split_rec + j) : make_int4(0, 0, 0, 0);
   const int4 rec1 = boundary ? __ldcg(p.split_rec + (p.plan.tier1_ctas + p.plan.tier2_ctas) + j)
                              : make_int4(0, 0, 0, 0);
-  for (int b = j; b < B; b += gridDim.x) {  // empty sequences: O = 0, LSE = -inf
+  for (int b = blockIdx.x; b < B; b += gridDim.x) {  // empty sequences: O = 0, LSE = -inf
     if (__ldg(p.kv_indptr + b) == __ldg(p.kv_indptr + b + 1)) {
       uint4* ob = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(b) * p.rows * kMlaDv);
       for (int i = tid; i < p.rows * kMlaDv * 2 / 16; i += kMlaMergeThreads) ob[i] = make_uint4(0, 0, 0, 0);
@@ -535,26 +536,28 @@ __global__ void __launch_bounds__(kMlaMergeThreads) gqa_mla_merge_kernel(const M
   const int cols = (kMlaDv / 4 + nranks - 1) / nranks;  // float4 columns per rank
   const int c_lo = rank * cols, c_hi = min(kMlaDv / 4, c_lo + cols);
   if (c_lo >= c_hi) return;
-  const int ncol = c_hi - c_lo, items = R * ncol;
-  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(b) * p.rows + hg * R) * kMlaDv;
+  const int ncol = c_hi - c_lo, items = kMlaRows * ncol;
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(b) * p.rows + hg * R + row0) * kMlaDv;
   auto part = [&](int s) {
-    return reinterpret_cast<const float4*>(p.part_o + slot_id(first_cta + s, s == 0 ? first_slot : 0) * (static_cast<int64_t>(R) * kMlaDv));
+    return reinterpret_cast<const float4*>(p.part_o + (slot_id(first_cta + s, s == 0 ? first_slot : 0) * R + row0) *
+                                                          static_cast<int64_t>(kMlaDv));
   };
-  if (S * R <= kMlaMergeWeights) {
-    for (int i = tid; i < S * R; i += kMlaMergeThreads) {
-      const int s = i / R, r = i - s * R;
-      wsh[s * R + r] = __ldcg(p.part_lse + slot_id(first_cta + s, s == 0 ? first_slot : 0) * R + r);
+  constexpr int W = kMlaRows;  // rows of this CTA
+  if (S * W <= kMlaMergeWeights) {
+    for (int i = tid; i < S * W; i += kMlaMergeThreads) {
+      const int s = i / W, r = i - s * W;
+      wsh[s * W + r] = __ldcg(p.part_lse + slot_id(first_cta + s, s == 0 ? first_slot : 0) * R + row0 + r);
     }
     __syncthreads();
-    if (tid < R) {  // weights of row tid; pieces with no token (lse = -inf) weigh 0
+    if (tid < W) {  // weights of row tid; pieces with no token (lse = -inf) weigh 0
       float m = -INFINITY;
-      for (int s = 0; s < S; ++s) m = fmaxf(m, wsh[s * R + tid]);
+      for (int s = 0; s < S; ++s) m = fmaxf(m, wsh[s * W + tid]);
       float den = 0.f;
       if (m != -INFINITY)
-        for (int s = 0; s < S; ++s) den += ex2(wsh[s * R + tid] - m);
+        for (int s = 0; s < S; ++s) den += ex2(wsh[s * W + tid] - m);
       const float inv = den > 0.f ? 1.f / den : 0.f;
-      for (int s = 0; s < S; ++s) wsh[s * R + tid] = m == -INFINITY ? 0.f : ex2(wsh[s * R + tid] - m) * inv;
-      if (rank == 0 && p.lse != nullptr) mla_store_lse(p, b, hg * R + tid, den > 0.f ? m + log2f(den) : -INFINITY);
+      for (int s = 0; s < S; ++s) wsh[s * W + tid] = m == -INFINITY ? 0.f : ex2(wsh[s * W + tid] - m) * inv;
+      if (rank == 0 && p.lse != nullptr) mla_store_lse(p, b, hg * R + row0 + tid, den > 0.f ? m + log2f(den) : -INFINITY);
     }
     __syncthreads();
     for (int i0 = tid; i0 < items; i0 += kMlaMergeThreads * kMlaMergeBatch) {
@@ -575,7 +578,7 @@ __global__ void __launch_bounds__(kMlaMergeThreads) gqa_mla_merge_kernel(const M
         for (int k = 0; k < kMlaMergeBatch; ++k) o[k] = __ldcg(src + rr[k] * (kMlaDv / 4) + cc[k]);
 #pragma unroll
         for (int k = 0; k < kMlaMergeBatch; ++k) {
-          const float w = wsh[s * R + rr[k]];
+          const float w = wsh[s * W + rr[k]];
           a[k].x += w * o[k].x;
           a[k].y += w * o[k].y;
           a[k].z += w * o[k].z;
@@ -594,7 +597,7 @@ __global__ void __launch_bounds__(kMlaMergeThreads) gqa_mla_merge_kernel(const M
     const int r = it / ncol, col = c_lo + (it - r * ncol);
     float m = -INFINITY, den = 0.f, a[4] = {0.f, 0.f, 0.f, 0.f};
     for (int s = 0; s < S; ++s) {
-      const float l = __ldcg(p.part_lse + slot_id(first_cta + s, s == 0 ? first_slot : 0) * R + r);
+      const float l = __ldcg(p.part_lse + slot_id(first_cta + s, s == 0 ? first_slot : 0) * R + row0 + r);
       const float4 o = __ldcg(part(s) + r * (kMlaDv / 4) + col);
       const float mn = fmaxf(m, l);
       if (mn == -INFINITY) continue;
@@ -609,7 +612,7 @@ __global__ void __launch_bounds__(kMlaMergeThreads) gqa_mla_merge_kernel(const M
     const float inv = den > 0.f ? 1.f / den : 0.f;
     *reinterpret_cast<uint2*>(ob + r * kMlaDv + col * 4) =
         make_uint2(pack_bf16(a[0] * inv, a[1] * inv), pack_bf16(a[2] * inv, a[3] * inv));
-    if (col == 0 && p.lse != nullptr) mla_store_lse(p, b, hg * R + r, den > 0.f ? m + log2f(den) : -INFINITY);
+    if (col == 0 && p.lse != nullptr) mla_store_lse(p, b, hg * R + row0 + r, den > 0.f ? m + log2f(den) : -INFINITY);
   }
 }
 
@@ -671,7 +674,8 @@ cudaError_t launch_mla(const MlaParams& p, const int* cache_seqlens, int kind, c
     e = launch_pdl(fn, dim3(ctas), dim3(kMlaThreads), smem, stream, args);
   }
   if (e != cudaSuccess) return e;
-  return launch_pdl(reinterpret_cast<const void*>(gqa_mla_merge_kernel), dim3(ctas > 1 ? ctas - 1 : 1),
+  const int per_boundary = p.piece_rows / kMlaRows;  // one merge CTA per 16 rows of a piece
+  return launch_pdl(reinterpret_cast<const void*>(gqa_mla_merge_kernel), dim3((ctas > 1 ? ctas - 1 : 1) * per_boundary),
                     dim3(kMlaMergeThreads), 0, stream, args);
 }
 
