@@ -283,7 +283,9 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
 
   const bool profile = ev0 != nullptr && ev1 != nullptr;
   if (profile && cudaEventRecord(ev0, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
-  const cudaError_t le = sj != nullptr ? gqa::launch_decode_lsu_sparse(dp, ctas, stream)
+  // selected-token mode: the decode is a programmatic dependent of the resolve
+  // kernel unless events (or the checked path's validation) sit between them
+  const cudaError_t le = sj != nullptr ? gqa::launch_decode_lsu_sparse(dp, ctas, stream, !profile && !checked)
                                        : gqa::launch_decode(tune.kernel, dp, ctas, stream);
   if (le != cudaSuccess) return GQA_ERR_LAUNCH;
   if (profile && cudaEventRecord(ev1, stream) != cudaSuccess) return GQA_ERR_LAUNCH;

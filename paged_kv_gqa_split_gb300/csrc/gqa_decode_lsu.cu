@@ -106,6 +106,10 @@ __global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kern
 
   // The merge grid may become resident now; it waits for this grid to finish.
   pdl_launch_dependents();
+  // Selected-token mode is launched as a dependent of the slot-resolving
+  // kernel: nothing that kernel writes is read before this returns. Without a
+  // programmatic dependency (every other launch) it returns at once.
+  pdl_wait();
   if (p.skip_if_set != nullptr && *p.skip_if_set != 0) return;
 
   const uint8_t* __restrict__ kc = static_cast<const uint8_t*>(p.k_cache);
@@ -387,7 +391,7 @@ __global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kern
 }
 
 template <int NG, int D, bool SP, bool F8 = false>
-static cudaError_t launch_lsu(const DecodeParams& p, int num_ctas, cudaStream_t stream) {
+static cudaError_t launch_lsu(const DecodeParams& p, int num_ctas, cudaStream_t stream, bool pdl = false) {
   using C = LsuCfg<NG, D, F8>;
   static int configured[64] = {0};
   int dev = 0;
@@ -398,8 +402,21 @@ static cudaError_t launch_lsu(const DecodeParams& p, int num_ctas, cudaStream_t 
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  gqa_decode_lsu_kernel<NG, D, SP, F8><<<num_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  if (!pdl) {
+    gqa_decode_lsu_kernel<NG, D, SP, F8><<<num_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_ctas);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gqa_decode_lsu_kernel<NG, D, SP, F8>, p);
 }
 
 #define GQA_LSU_VARIANTS(X) X(4, 3) X(4, 4) X(4, 2) X(2, 3) X(2, 2) X(2, 5) X(1, 3) X(1, 2) X(1, 4) X(1, 6)
@@ -420,9 +437,10 @@ cudaError_t launch_decode_lsu(int ng, int stages, const DecodeParams& p, int num
   return cudaErrorInvalidValue;
 }
 
-// Selected-token mode: one variant, 4 KV heads per CTA and a 2-deep ring.
-cudaError_t launch_decode_lsu_sparse(const DecodeParams& p, int num_ctas, cudaStream_t stream) {
-  return launch_lsu<4, 2, true>(p, num_ctas, stream);
+// Selected-token mode: one variant, 4 KV heads per CTA and a 2-deep ring;
+// pdl: launched as a programmatic dependent of the kernel before it.
+cudaError_t launch_decode_lsu_sparse(const DecodeParams& p, int num_ctas, cudaStream_t stream, bool pdl) {
+  return launch_lsu<4, 2, true>(p, num_ctas, stream, pdl);
 }
 
 // FP8-cache variants: 4 KV heads per CTA, 2, 3 or 4 stages.

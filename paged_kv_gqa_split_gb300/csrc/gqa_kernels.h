@@ -134,7 +134,7 @@ int lsu_f8_smem_bytes(int stages);
 cudaError_t launch_decode_lsu_f8(int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream);
 cudaError_t launch_decode_lsu(int ng, int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream);
 // The selected-token variant (p.sparse_topk > 0): 4 KV heads per CTA, 2 stages.
-cudaError_t launch_decode_lsu_sparse(const DecodeParams& p, int num_ctas, cudaStream_t stream);
+cudaError_t launch_decode_lsu_sparse(const DecodeParams& p, int num_ctas, cudaStream_t stream, bool pdl);
 // Resolve the selected columns of a sparse batch to slots (-1: invalid column).
 cudaError_t launch_sparse_resolve(const int* logical_indices, const int* block_table, const int* token_to_req,
                                   int* slots, int rows, int topk, int page_size, int page_table_width,

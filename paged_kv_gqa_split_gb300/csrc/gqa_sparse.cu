@@ -18,6 +18,7 @@
 #include <cstdint>
 
 #include "gqa_kernels.h"
+#include "gqa_ptx.cuh"
 
 namespace gqa {
 
@@ -27,6 +28,9 @@ __global__ void __launch_bounds__(kResolveThreads)
     gqa_sparse_resolve_kernel(const int* __restrict__ logical_indices, const int* __restrict__ block_table,
                               const int* __restrict__ token_to_req, int* __restrict__ slots, int64_t n, int topk,
                               int page_size, int page_table_width, int num_requests, int num_cache_blocks) {
+  // The decode grid may become resident now; it waits for this grid's slots
+  // before its first gather.
+  pdl_launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
     const int row = static_cast<int>(i / topk);
