@@ -393,15 +393,10 @@ __global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kern
 template <int NG, int D, bool SP, bool F8 = false>
 static cudaError_t launch_lsu(const DecodeParams& p, int num_ctas, cudaStream_t stream, bool pdl = false) {
   using C = LsuCfg<NG, D, F8>;
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gqa_decode_lsu_kernel<NG, D, SP, F8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
+  static std::atomic<int> configured[kMaxDevices];
+  const cudaError_t e = set_smem_limit_once(
+      configured, reinterpret_cast<const void*>(gqa_decode_lsu_kernel<NG, D, SP, F8>), C::kSmemBytes);
+  if (e != cudaSuccess) return e;
   if (!pdl) {
     gqa_decode_lsu_kernel<NG, D, SP, F8><<<num_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
     return cudaGetLastError();

@@ -349,15 +349,10 @@ __global__ void __launch_bounds__((NG + 1) * 32, 1) gqa_decode_tma_kernel(const 
 template <int NG, int TILE, int STAGES>
 static cudaError_t launch_tma(const DecodeParams& p, int num_ctas, cudaStream_t stream) {
   using C = TmaCfg<NG, TILE, STAGES>;
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gqa_decode_tma_kernel<NG, TILE, STAGES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
+  static std::atomic<int> configured[kMaxDevices];
+  const cudaError_t e = set_smem_limit_once(
+      configured, reinterpret_cast<const void*>(gqa_decode_tma_kernel<NG, TILE, STAGES>), C::kSmemBytes);
+  if (e != cudaSuccess) return e;
   gqa_decode_tma_kernel<NG, TILE, STAGES><<<num_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "gqa_plan.h"
@@ -172,5 +173,22 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int* sl
                              int n, int num_pages, int sm_count, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(int* out);
 cudaError_t device_error_word(int** ptr);  // device address of the error word (current device)
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` once per device
+// (`done` is the kernel's own flag table, zero-initialised static storage).
+// Safe to call from several host threads at once: the attribute call is
+// idempotent and the flags are atomic. Devices past the table set it on
+// every call.
+constexpr int kMaxDevices = 64;
+inline cudaError_t set_smem_limit_once(std::atomic<int> (&done)[kMaxDevices], const void* fn, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool tracked = dev >= 0 && dev < kMaxDevices;
+  if (tracked && done[dev].load(std::memory_order_acquire) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && tracked) done[dev].store(1, std::memory_order_release);
+  return e;
+}
 
 }  // namespace gqa

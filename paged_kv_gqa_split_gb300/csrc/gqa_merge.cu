@@ -333,18 +333,20 @@ cudaError_t read_and_clear_device_error(int* out) {
 }
 
 cudaError_t device_error_word(int** ptr) {
-  static int* cached[64] = {nullptr};
+  static std::atomic<int*> cached[kMaxDevices];  // one address per device; racing threads store the same one
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (cached[dev] == nullptr) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int* word = cached[dev].load(std::memory_order_acquire);
+  if (word == nullptr) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_device_error);
     if (e != cudaSuccess) return e;
-    cached[dev] = static_cast<int*>(p);
+    word = static_cast<int*>(p);
+    cached[dev].store(word, std::memory_order_release);
   }
-  *ptr = cached[dev];
+  *ptr = word;
   return cudaSuccess;
 }
 

@@ -662,15 +662,9 @@ cudaError_t launch_mla(const MlaParams& p, const int* cache_seqlens, int kind, c
     const void* fn = stages == 3 ? reinterpret_cast<const void*>(gqa_mla_decode_kernel<3, 3>)
                                   : reinterpret_cast<const void*>(gqa_mla_decode_kernel<4, 2>);
     const int smem = mla_smem_bytes(stages);
-    static int configured[64][2] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const int vi = stages == 3 ? 0 : 1;
-    if (dev >= 0 && dev < 64 && !configured[dev][vi]) {
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      configured[dev][vi] = 1;
-    }
+    static std::atomic<int> configured[2][kMaxDevices];
+    e = set_smem_limit_once(configured[stages == 3 ? 0 : 1], fn, smem);
+    if (e != cudaSuccess) return e;
     e = launch_pdl(fn, dim3(ctas), dim3(kMlaThreads), smem, stream, args);
   }
   if (e != cudaSuccess) return e;

@@ -664,15 +664,10 @@ int box_rows_for(int page_size) { return page_size % 64 == 0 ? 64 : 32; }
 
 template <int BR, int R>
 cudaError_t launch_tc(const MlaParams& p, const MlaTcMaps& maps, int ctas, cudaStream_t stream) {
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(gqa_mla_tc_decode_kernel<BR, R>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<R>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
-  }
+  static std::atomic<int> configured[kMaxDevices];
+  const cudaError_t e = set_smem_limit_once(
+      configured, reinterpret_cast<const void*>(gqa_mla_tc_decode_kernel<BR, R>), TcCfg<R>::kSmemBytes);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(TcCfg<R>::kThreads);
