@@ -48,6 +48,7 @@ WORKLOAD_TEXT = {
                "pool 2x sum(lens), q ~ 3 N(0,1)"),
 }
 FLUSH_BYTES = 256 << 20
+TABLE_MIN_STEPS, TABLE_MIN_WARMUP = 50, 10
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -80,6 +81,11 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_value(bytes_per_rank: int, step_ms_max: float, world: int) -> float:
+    """Whole-job GB/s of N replicas: every rank's bytes over the slowest rank's step time."""
+    return world * bytes_per_rank / (step_ms_max * 1e-3) / 1e9
 
 
 def barrier(world: int, device=None):
@@ -275,12 +281,17 @@ def bench_e2e(w, device, steps, warmup):
         out_h.copy_(out_d, non_blocking=True)
         lse_h.copy_(lse_d, non_blocking=True)
 
+    def copies():
+        for hd, dd in zip(host, dev):
+            dd.copy_(hd, non_blocking=True)
+
     for _ in range(max(1, warmup)):
         call()
     torch.cuda.synchronize()
     ms = time_steps(call, steps, stream, flush)
+    copy_ms = time_steps(copies, steps, stream, flush)  # the same host-to-device copies alone
     del flush, dev
-    return ms, h2d, d2h
+    return ms, copy_ms, h2d, d2h
 
 
 # ------------------------------------------------------------- KV append
@@ -419,58 +430,56 @@ def bench_mla(device, steps, warmup, peak, wide: bool = False):
 
 
 # -------------------------------------------------------------- CPU oracle
-def oracle_sample(w, budget_s: float):
-    """Run the float64 oracle over the workload's sequences in order until about
-    budget_s seconds have passed (at least one non-empty sequence). Returns the
-    sequences done, the seconds taken and the oracle's (O, lse) rows for them."""
-    from oracle import gqa_paged_decode_oracle
-    done, outs, t0 = [], [], time.perf_counter()
-    order = [b for b in range(w.batch) if w.lens[b] > 0] or [0]
-    for b in order:
-        o, l = gqa_paged_decode_oracle(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices, w.sm_scale, seqs=[b])
-        done.append(b)
-        outs.append((o[b], l[b]))
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return done, dt, outs
+# CPU work (core-seconds) the oracle baseline aims for: enough repeated rounds
+# over the workload that the median round is stable, bounded to a few seconds of
+# wall time on the host's cores.
+ORACLE_TARGET_CPU_S = 12.0
+ORACLE_MAX_ROUNDS = 20
 
 
-def blas_threads():
-    try:
-        from threadpoolctl import threadpool_info
-        info = threadpool_info()
-        n = max((d.get("num_threads", 1) for d in info), default=1)
-        return int(n)
-    except Exception:
-        return 1
+def oracle_rounds(w, rounds=None, target_cpu_s=ORACLE_TARGET_CPU_S):
+    """The float64 oracle over every sequence of `w`, on all host cores (one worker
+    process per core, one BLAS thread each). Runs `rounds` rounds (default: enough
+    for about target_cpu_s core-seconds) and returns the first round's (O, lse),
+    the per-round wall times and the worker count."""
+    from oracle.pool import OraclePool
+    with OraclePool(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices, w.sm_scale) as pool:
+        o_ref, l_ref, first = pool.run()
+        if rounds is None:
+            rounds = max(1, min(ORACLE_MAX_ROUNDS, math.ceil(target_cpu_s / max(first * pool.cores, 1e-3))))
+        times = [first] + [pool.run()[2] for _ in range(rounds - 1)]
+        return o_ref, l_ref, times, pool.cores
 
 
-def cpu_baseline(w, out=None, lse=None, budget_s: float = 10.0):
-    """The oracle timed on the host on a bounded sample of the workload. With
-    the GPU's (out, lse) of the timed run, the same sampled sequences also give
-    the run's parity figures."""
+def parity_summary(w, out, lse, o_ref, l_ref):
+    """Element-wise comparison of the GPU's (out, lse) with the oracle over every sequence."""
     import numpy as np
-    seqs, dt, outs = oracle_sample(w, budget_s)
-    lens = [w.lens[b] for b in seqs]
-    gbs = counted_bytes(lens) / dt / 1e9
-    base = {"value": gbs, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"{len(lens)} of {w.batch} sequences ({sum(lens)} tokens) of the {w.name} workload, "
-                      f"float64 NumPy oracle, {dt:.2f} s",
-            "host_cores_available": len(os.sched_getaffinity(0))}
-    parity = None
-    if out is not None:
-        o = out.float().cpu().double().numpy()[seqs]
-        l = lse.cpu().double().numpy()[seqs]
-        o_ref = np.stack([x[0] for x in outs])
-        l_ref = np.stack([x[1] for x in outs])
-        fin = np.isfinite(l_ref)
-        o_err = float(np.abs(o - o_ref).max())
-        l_err = float(np.abs(l[fin] - l_ref[fin]).max()) if fin.any() else 0.0
-        ok = bool(np.all(np.abs(o - o_ref) <= 2e-2 + 2e-2 * np.abs(o_ref)) and l_err <= 1e-3 and
-                  np.array_equal(np.isneginf(l), np.isneginf(l_ref)))
-        parity = {"sequences": len(seqs), "tokens": sum(lens), "max_abs_dO": o_err, "max_abs_dlse": l_err,
-                  "within_tolerance": ok}
+    o = out.float().cpu().double().numpy()
+    l = lse.cpu().double().numpy()
+    fin = np.isfinite(l_ref)
+    o_err = float(np.abs(o - o_ref).max())
+    l_err = float(np.abs(l[fin] - l_ref[fin]).max()) if fin.any() else 0.0
+    ok = bool(np.all(np.abs(o - o_ref) <= 2e-2 + 2e-2 * np.abs(o_ref)) and l_err <= 1e-3 and
+              np.array_equal(np.isneginf(l), np.isneginf(l_ref)))
+    return {"sequences": w.batch, "tokens": w.total_tokens, "max_abs_dO": o_err, "max_abs_dlse": l_err,
+            "within_tolerance": ok}
+
+
+def cpu_baseline(w, out=None, lse=None):
+    """The oracle timed on the host's cores over the whole workload (median of
+    repeated rounds). With the GPU's (out, lse) of the timed run, the first round
+    also gives the run's parity figures over every sequence."""
+    from oracle.pool import host_cores
+    o_ref, l_ref, times, cores = oracle_rounds(w)
+    dt = statistics.median(times)
+    gbs = counted_bytes(w.lens) / dt / 1e9
+    base = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"all {w.batch} sequences ({w.total_tokens} tokens) of the {w.name} workload per round, "
+                      f"float64 NumPy oracle in {cores} worker processes (one BLAS thread each); "
+                      f"median of {len(times)} rounds, {dt:.3f} s per round",
+            "host_cores_available": host_cores(), "threads_per_worker": 1,
+            "rounds_s": [round(t, 4) for t in times]}
+    parity = parity_summary(w, out, lse, o_ref, l_ref) if out is not None else None
     return base, parity
 
 
@@ -578,33 +587,41 @@ def main():
     cb = counted_bytes(w.lens)
     with ClockSampler(local) as clk:
         r = bench_workload_gpu(w, device, args.steps, warmup, world)
-    step_ms = statistics.mean(r["step_ms"])
+    step_ms = statistics.median(r["step_ms"])
     step_ms_max = max_over_ranks(step_ms, world, device)
-    dec_ms = statistics.mean(r["decode_ms"])
-    value = world * cb / (step_ms_max * 1e-3) / 1e9
+    dec_ms = statistics.median(r["decode_ms"])
+    value = replica_value(cb, step_ms_max, world)
     achieved = cb / (dec_ms * 1e-3) / 1e9
 
     # the GPU result of the timed run, for the parity check of the CPU-baseline leg
     run_out, run_lse = r["out"].cpu(), r["lse"].cpu()
+    step_ms_mean = statistics.mean(r["step_ms"])
     del r
 
     e2e = None
     if not args.no_e2e:
-        ms, h2d, d2h = bench_e2e(w, device, max(3, args.steps // 4), 1)
-        e_ms = max_over_ranks(statistics.mean(ms), world, device)
+        ms, copy_ms, h2d, d2h = bench_e2e(w, device, max(3, args.steps // 4), 1)
+        e_ms = max_over_ranks(statistics.median(ms), world, device)
+        c_ms = statistics.median(copy_ms)
         e2e = {"value": world * cb / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e_ms,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "h2d_gbs": h2d / (c_ms * 1e-3) / 1e9, "h2d_ms": c_ms,
+               "note": "each step copies the whole K/V pool (pinned host -> HBM), runs the call and reads "
+                       "out/lse back; h2d_gbs times the same copies alone in the same run"}
 
     table = {}
     if not args.no_workloads:
         for name in ["tiny", "mid", "long", "large", "skewed"]:
             ww = w if name == args.workload else wl.make_config(name)
-            rr = bench_workload_gpu(ww, device, args.steps, warmup, world)
-            ms = statistics.mean(rr["step_ms"])
-            dm = statistics.mean(rr["decode_ms"])
+            # at least 10 warm-up and 50 timed calls per workload; the table reports their median
+            rr = bench_workload_gpu(ww, device, max(args.steps, TABLE_MIN_STEPS), max(warmup, TABLE_MIN_WARMUP),
+                                    world)
+            ms = statistics.median(rr["step_ms"])
+            dm = statistics.median(rr["decode_ms"])
             b = counted_bytes(ww.lens)
             table[name] = {"us_per_batch": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9,
                            "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
+                           "us_per_batch_mean": statistics.mean(rr["step_ms"]) * 1e3,
                            "decode_kernel_us": dm * 1e3, "batch": ww.batch, "total_tokens": ww.total_tokens,
                            "counted_bytes": b, "us_per_batch_l2_warm": statistics.median(rr["warm_ms"]) * 1e3}
             del rr
@@ -638,6 +655,8 @@ def main():
         "steps": args.steps,
         "warmup": warmup,
         "ms_per_step": step_ms_max,
+        "ms_per_step_mean": step_ms_mean,
+        "timing": "median of the timed steps (CUDA events; ms_per_step_mean is their mean)",
         "us_per_batch": step_ms_max * 1e3,
         "frac_of_peak": value / world / peak,
         "higher_is_better": True,
@@ -672,21 +691,20 @@ def main():
 
 
 def main_reference(args, world, rank, warmup):
+    """The float64 oracle on the host's cores: each step evaluates the whole
+    workload once across the worker pool (one process per core)."""
     if rank != 0:
         return
+    from oracle.pool import OraclePool, host_cores
     w = wl.make_config(args.workload)
-    budget = max(0.5, 120.0 / max(1, args.steps + warmup))
-    for _ in range(warmup):
-        oracle_sample(w, budget)
-    rates, secs, lens_done = [], [], []
-    for _ in range(args.steps):
-        seqs, dt, _ = oracle_sample(w, budget)
-        lens = [w.lens[b] for b in seqs]
-        rates.append(counted_bytes(lens) / dt / 1e9)
-        secs.append(dt)
-        lens_done = lens
-    value = statistics.mean(rates)
-    ms_equiv = counted_bytes(w.lens) / (value * 1e9) * 1e3
+    cb = counted_bytes(w.lens)
+    with OraclePool(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices, w.sm_scale) as pool:
+        for _ in range(warmup):
+            pool.run()
+        secs = [pool.run()[2] for _ in range(args.steps)]
+        cores = pool.cores
+    dt = statistics.median(secs)
+    value = cb / dt / 1e9
     line = {
         "impl": "reference",
         "metric": METRIC,
@@ -695,18 +713,19 @@ def main_reference(args, world, rank, warmup):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": warmup,
-        "ms_per_step": ms_equiv,
+        "ms_per_step": dt * 1e3,
+        "ms_per_step_mean": statistics.mean(secs) * 1e3,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded torch.Generator)",
         "config": {"workload": WORKLOAD_TEXT[args.workload], "batch": w.batch, "total_tokens": w.total_tokens,
-                   "parallelism": "single process"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": blas_threads(),
-                         "sample": f"each step: the first {len(lens_done)} non-empty sequences "
-                                   f"({sum(lens_done)} tokens), about {budget:.1f} s of float64 oracle work; "
-                                   f"ms_per_step is the whole batch at that rate"},
+                   "parallelism": f"{cores} host worker processes"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": cores,
+                         "host_cores_available": host_cores(), "threads_per_worker": 1,
+                         "sample": f"each step: all {w.batch} sequences ({w.total_tokens} tokens) of the workload, "
+                                   f"float64 NumPy oracle across {cores} worker processes; median step time"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }

@@ -291,10 +291,33 @@ int gqa_sparse_paged_decode(const void* q, const void* k_cache, const void* v_ca
 
 /*
  * Synchronise the current device, then read and clear the sticky device error
- * word: bit 1 / 2 = a pipeline wait gave up after ~2 s (the kernel returned
- * early), bit 4 = bad page id, bit 8 = bad kv_indptr. 0 means no error.
+ * word: bit 1 / 2 = a pipeline wait of the TMA-gather decode variant or the
+ * tensor-memory MLA kernel gave up (after ~2 s by default; the kernel drained
+ * its copies in flight and returned early, so that call's outputs are not
+ * valid), bit 4 = bad page id, bit 8 = bad kv_indptr. 0 means no error.
  */
 int gqa_paged_decode_device_error(int* flags);
+
+/*
+ * Test hooks for the library's failure paths; production code has no reason
+ * to call them. Both are process-wide.
+ *
+ * gqa_paged_decode_test_fail_allocs(count): the next `count` allocations of
+ * the library-owned workspace fail exactly as a failing cudaMalloc would (the
+ * call returns GQA_ERR_WORKSPACE without launching and without writing out /
+ * lse; the device workspace is left unallocated). 0 turns it off. Returns
+ * GQA_ERR_INVALID_ARGUMENT for count < 0.
+ *
+ * gqa_paged_decode_test_wait_limit_ns(ns): the give-up limit of the bounded
+ * mbarrier waits of the TMA-gather decode variant (gather = 1 in
+ * gqa_paged_decode_set_tuning), in nanoseconds; 0 restores the default of
+ * 2 s. A wait that runs out sets bit 1 or 2 of the device error word and the
+ * CTA returns after its copies in flight have landed (that drain keeps the
+ * 2 s limit), so a call made with a tiny limit completes, with outputs that
+ * are not valid.
+ */
+int gqa_paged_decode_test_fail_allocs(int count);
+int gqa_paged_decode_test_wait_limit_ns(uint64_t ns);
 
 /*
  * The pages this library follows have no counterpart to this entry point: it
@@ -321,6 +344,11 @@ int gqa_paged_decode_device_error(int* flags);
  * it and give wrong results: order them on one stream. 32 MiB holds the
  * tier-1 partials of every occupancy-limited launch (16 decode warps per SM,
  * two 4 KB partials each) on a GPU of up to 240 SMs.
+ *
+ * The array's device address is looked up once per device and kept for the
+ * life of the process, so resetting a device (cudaDeviceReset, or destroying
+ * its primary context) between calls is not supported: after a reset the
+ * kept address no longer belongs to the device's new context.
  */
 #define GQA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 

@@ -48,6 +48,8 @@ _SIGNATURES = {
     "gqa_paged_decode_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_int, _vp]),
     "gqa_mla_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp] + [ctypes.c_int] * 6 + [_vp]),
     "gqa_mla_set_tuning": (ctypes.c_int, [ctypes.c_int]),
+    "gqa_paged_decode_test_fail_allocs": (ctypes.c_int, [ctypes.c_int]),
+    "gqa_paged_decode_test_wait_limit_ns": (ctypes.c_int, [ctypes.c_uint64]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -145,6 +147,14 @@ def gqa_paged_decode_device_error() -> int:
     if rc != GQA_OK:
         raise GqaError(rc, "gqa_paged_decode_device_error")
     return flags.value
+
+
+def gqa_paged_decode_test_fail_allocs(count: int) -> int:
+    return load().gqa_paged_decode_test_fail_allocs(count)
+
+
+def gqa_paged_decode_test_wait_limit_ns(ns: int) -> int:
+    return load().gqa_paged_decode_test_wait_limit_ns(ns)
 
 
 def gqa_paged_kv_append(k_new, v_new, slots, k_cache, v_cache, num_tokens, num_pages, stream) -> int:

@@ -59,6 +59,11 @@ struct Tuning {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 Tuning g_tune;
+// Test hooks (gqa_paged_decode_test_fail_allocs / _test_wait_limit_ns): library
+// workspace allocations still to fail as if cudaMalloc had failed, and the
+// give-up limit of the TMA variant's bounded waits (0: the default).
+int g_fail_allocs = 0;
+unsigned long long g_wait_limit_ns = 0;
 cudaEvent_t g_ev_start = nullptr;
 cudaEvent_t g_ev_stop = nullptr;
 // Ticket epoch of each call (never 0; 40 bits), so arrival tickets left by an
@@ -163,8 +168,10 @@ int library_workspace(DeviceState* st, size_t need, void** ws) {
       st->ws = nullptr;
       st->ws_bytes = 0;
     }
-    if (cudaMalloc(&st->ws, need) != cudaSuccess) {
-      cudaGetLastError();
+    const bool injected = g_fail_allocs > 0;  // a test hook stands in for a failing cudaMalloc
+    if (injected) --g_fail_allocs;
+    if (injected || cudaMalloc(&st->ws, need) != cudaSuccess) {
+      if (!injected) cudaGetLastError();
       st->ws = nullptr;
       return GQA_ERR_WORKSPACE;
     }
@@ -196,11 +203,13 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   gqa::PlanConfig cfg;
   cudaEvent_t ev0, ev1;
   void* ws = nullptr;
+  unsigned long long wait_limit_ns = gqa::kDefaultWaitLimitNs;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     rc = current_device(&dev, &st);
     if (rc != GQA_OK) return rc;
     tune = g_tune;
+    if (g_wait_limit_ns > 0) wait_limit_ns = g_wait_limit_ns;
     if (sj != nullptr) tune.kernel = KernelChoice{gqa::kGatherLsu, 4, 16, 2};  // the one sparse variant
     if (fp8) {  // FP8 caches: the FP8 variant; a cp.async tuning with 4 heads per CTA picks its depth
       const KernelChoice& k = tune.kernel;
@@ -280,6 +289,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   dp.plan = cfg;
   dp.scale_log2 = sm_scale * kLog2e;
   dp.num_pages_check = checked ? num_pages : 0;
+  dp.wait_limit_ns = wait_limit_ns;
 
   const bool profile = ev0 != nullptr && ev1 != nullptr;
   if (profile && cudaEventRecord(ev0, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
@@ -656,6 +666,19 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
   return gqa::launch_mla(mp, cache_seqlens, mla_kind, &maps, stream) == cudaSuccess
              ? GQA_OK
              : GQA_ERR_LAUNCH;
+}
+
+int gqa_paged_decode_test_fail_allocs(int count) {
+  if (count < 0) return GQA_ERR_INVALID_ARGUMENT;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_fail_allocs = count;
+  return GQA_OK;
+}
+
+int gqa_paged_decode_test_wait_limit_ns(uint64_t ns) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_wait_limit_ns = ns;
+  return GQA_OK;
 }
 
 int gqa_paged_decode_device_error(int* flags) {

@@ -22,9 +22,10 @@ namespace gqa {
 // a finite (masked) score, zero V contributes nothing. Never written.
 __device__ __align__(128) uint8_t g_zero_rows[kPageBytes];
 
-// Spin limit for every mbarrier wait: a wait that is still unsatisfied after
-// this long records an error and the CTA returns.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Spin limit of the drain before exit: the copies a CTA has in flight when it
+// gives up are waited for this long at most. The give-up limit of the other
+// waits is DecodeParams::wait_limit_ns (normally the same 2 s).
+constexpr uint64_t kWaitLimitNs = kDefaultWaitLimitNs;
 
 template <int NG, int TILE, int STAGES>
 struct TmaCfg {
@@ -46,16 +47,16 @@ struct TmaCfg {
 };
 
 // Bounded mbarrier wait. Returns false (after flagging `err_bit` once) when
-// the wait exceeds kWaitLimitNs or another role of the CTA already gave up.
+// the wait exceeds `limit_ns` or another role of the CTA already gave up.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_s, int* err,
-                                             int err_bit) {
+                                             int err_bit, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort_s) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         atomicOr(err, err_bit);
         *abort_s = 1;
         return false;
@@ -93,7 +94,7 @@ __device__ __forceinline__ void tma_producer(const DecodeParams& p, uint32_t sba
   auto emit = [&](int b, int hg, int tt, int cnt, int flags, int page, const SplitInfo& si) -> bool {
     const int stage = tiles % STAGES;
     const uint32_t par = (tiles / STAGES) & 1u;
-    if (!wait_bounded(empty0 + 8 * stage, par ^ 1u, abort_s, p.err, kErrTimeoutEmpty)) return false;
+    if (!wait_bounded(empty0 + 8 * stage, par ^ 1u, abort_s, p.err, kErrTimeoutEmpty, p.wait_limit_ns)) return false;
     const uint32_t sb = sbase + stage * C::kStageBytes;
     const uint32_t bar = full0 + 8 * stage;
     const int nrows = (cnt + 15) & ~15;
@@ -222,25 +223,31 @@ __device__ __forceinline__ void tma_producer(const DecodeParams& p, uint32_t sba
   }
   if (ok && u0 < u1 && lane == 0) write_split_rec(p.split_rec, blockIdx.x, p.epoch, last_b, last_hg, last_si);
 
+  bool placed = false;
   if (ok) {
     // end-of-work marker
     const int stage = tiles % STAGES;
     const uint32_t par = (tiles / STAGES) & 1u;
-    if (wait_bounded(empty0 + 8 * stage, par ^ 1u, abort_s, p.err, kErrTimeoutEmpty)) {
+    if (wait_bounded(empty0 + 8 * stage, par ^ 1u, abort_s, p.err, kErrTimeoutEmpty, p.wait_limit_ns)) {
       if (lane == 0) {
         const uint32_t sb = sbase + stage * C::kStageBytes;
         asm volatile("st.shared.v4.s32 [%0], {%1, %1, %2, %1};" ::"r"(sb + C::kHdrOff), "r"(0), "r"(F_DONE)
                      : "memory");
         mbar_arrive(full0 + 8 * stage);
       }
-      return;
+      placed = true;
     }
   }
-  // Gave up: make sure no bulk copy is still writing into this CTA's shared
-  // memory before it exits (bounded as well).
-  *abort_s = 1;
+  if (!placed) *abort_s = 1;  // gave up: the consumers stop at their next wait
+  // No bulk copy may still be writing into this CTA's shared memory when it
+  // exits. The consumers normally wait for every tile, but one that gave up
+  // (its wait ran out) has stopped, so the producer itself waits for the last
+  // tiles it issued (bounded as well). After the marker, its stage's earlier
+  // tile was released by the consumers and is not waited for again (the
+  // marker's arrival moved that barrier on by one more phase).
   if (lane == 0) {
-    const uint32_t first = tiles > STAGES ? tiles - STAGES : 0;
+    const uint32_t keep = placed ? STAGES - 1 : STAGES;
+    const uint32_t first = tiles > keep ? tiles - keep : 0;
     for (uint32_t i = first; i < tiles; ++i) {
       const uint32_t bar = full0 + 8 * (i % STAGES);
       const uint32_t par = (i / STAGES) & 1u;
@@ -275,7 +282,7 @@ __device__ __forceinline__ void tma_consumer(const DecodeParams& p, uint32_t sba
   for (uint32_t tiles = 0;; ++tiles) {
     const int stage = tiles % STAGES;
     const uint32_t par = (tiles / STAGES) & 1u;
-    if (!wait_bounded(full0 + 8 * stage, par, abort_s, p.err, kErrTimeoutFull)) return;
+    if (!wait_bounded(full0 + 8 * stage, par, abort_s, p.err, kErrTimeoutFull, p.wait_limit_ns)) return;
     const uint32_t sb = sbase + stage * C::kStageBytes;
     int hb, cnt, flags, hg;
     ld_shared_v4(sb + C::kHdrOff, hb, cnt, flags, hg);

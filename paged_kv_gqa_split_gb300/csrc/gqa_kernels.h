@@ -42,7 +42,11 @@ struct DecodeParams {
   float scale_log2;        // sm_scale * log2(e)
   int num_pages_check;     // > 0: page ids are range-checked against it
   int fuse_max_splits;     // split sequences of at most this many pieces are merged by the decode kernel
+  unsigned long long wait_limit_ns;  // TMA variant: give-up limit of a bounded mbarrier wait
 };
+
+// Default give-up limit of a bounded mbarrier wait (the drain before exit keeps it).
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
 
 // Default: every split sequence goes to the merge kernel, whose CTAs share the
 // work of one sequence; merging inside the decode kernel (the warp that brings
