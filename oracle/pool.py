@@ -75,8 +75,6 @@ def _sub_problem(q, k_cache, v_cache, indptr: np.ndarray, indices: np.ndarray, s
 
 def _worker(conn, sm_scale: float) -> None:
     """Receive one sub-problem, then answer every 'go' with the oracle's rows for it."""
-    for var in _THREAD_VARS:
-        os.environ[var] = "1"
     import torch
     torch.set_num_threads(1)
     from oracle.oracle import gqa_paged_decode_oracle
@@ -124,7 +122,13 @@ class OraclePool:
         self.cores = len(self.shares)
         ctx = mp.get_context("spawn")
         self._procs, self._conns = [], []
+        # A spawned worker imports numpy (and its BLAS) while it unpickles its
+        # target, before any of its own code runs, so the one-thread limit has
+        # to be in the environment it starts with.
+        saved = {var: os.environ.get(var) for var in _THREAD_VARS}
         try:
+            for var in _THREAD_VARS:
+                os.environ[var] = "1"
             for share in self.shares:
                 parent, child = ctx.Pipe()
                 p = ctx.Process(target=_worker, args=(child, float(sm_scale)), daemon=True)
@@ -132,12 +136,22 @@ class OraclePool:
                 child.close()
                 self._procs.append(p)
                 self._conns.append(parent)
+            for var, val in saved.items():
+                if val is None:
+                    os.environ.pop(var, None)
+                else:
+                    os.environ[var] = val
             for conn, share in zip(self._conns, self.shares):
                 conn.send(_sub_problem(q, k_cache, v_cache, indptr, indices, share))
             for conn in self._conns:
                 if conn.recv() != "ready":
                     raise RuntimeError("oracle worker failed to start")
         except BaseException:
+            for var, val in saved.items():
+                if val is None:
+                    os.environ.pop(var, None)
+                else:
+                    os.environ[var] = val
             self.close()
             raise
 

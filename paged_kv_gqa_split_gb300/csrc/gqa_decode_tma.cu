@@ -50,17 +50,20 @@ struct TmaCfg {
 // the wait exceeds `limit_ns` or another role of the CTA already gave up.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_s, int* err,
                                              int err_bit, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  // One try_wait may suspend the thread for a system-dependent time, which can
+  // outlast a limit below about a millisecond; such a limit spins on the
+  // non-blocking test_wait instead. The limit is checked after every attempt
+  // (the clock and the shared flag cost little next to it).
+  const bool spin = limit_ns < 1000000ull;
+  if (spin ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort_s) return false;
-      if (global_timer_ns() - t0 > limit_ns) {
-        atomicOr(err, err_bit);
-        *abort_s = 1;
-        return false;
-      }
+  for (;;) {
+    if (spin ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (*abort_s) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      atomicOr(err, err_bit);
+      *abort_s = 1;
+      return false;
     }
   }
 }
