@@ -229,6 +229,7 @@ def bench_workload_gpu(w, device, steps, warmup, world, with_hooks=True):
 
     for _ in range(warmup):
         call()
+    launches = _lib.gqa_paged_decode_last_launch_count()
     torch.cuda.synchronize()
     barrier(world, device)
     t_wall0 = time.perf_counter()
@@ -256,7 +257,7 @@ def bench_workload_gpu(w, device, steps, warmup, world, with_hooks=True):
         warm_ms = time_steps(call, steps, stream, lambda: None)
     del flush
     return {"step_ms": step_ms, "decode_ms": dec_ms, "warm_ms": warm_ms, "wall_s": wall, "gpu": g, "out": out,
-            "lse": lse}
+            "lse": lse, "launches_per_call": launches}
 
 
 def bench_e2e(w, device, steps, warmup):
@@ -541,6 +542,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="time every decode variant instead of the contract line")
+    ap.add_argument("--merge-mode", type=int, choices=[0, 1], default=0,
+                    help="0: decode grid + merge kernel (default); 1: one-wave decode with the merge inside the kernel")
     ap.add_argument("--only", choices=["fp8", "sparse", "mla", "mla-wide"], default=None,
                     help="time only the FP8-cache decode of --workload, or only the selected-token decode, and "
                          "print its result (for profiling a small case)")
@@ -563,6 +566,8 @@ def main():
         build()
     barrier(world, device)
     _lib.load()
+    if _lib.gqa_paged_decode_set_merge_mode(args.merge_mode) != 0:
+        raise SystemExit("bad --merge-mode")
 
     if args.sweep:
         sweep(device, args.steps, warmup, ["tiny", "mid", "long", "large", "skewed"])
@@ -596,6 +601,7 @@ def main():
     # the GPU result of the timed run, for the parity check of the CPU-baseline leg
     run_out, run_lse = r["out"].cpu(), r["lse"].cpu()
     step_ms_mean = statistics.mean(r["step_ms"])
+    launches_per_call = r["launches_per_call"]
     del r
 
     e2e = None
@@ -622,7 +628,8 @@ def main():
             table[name] = {"us_per_batch": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9,
                            "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak,
                            "us_per_batch_mean": statistics.mean(rr["step_ms"]) * 1e3,
-                           "decode_kernel_us": dm * 1e3, "batch": ww.batch, "total_tokens": ww.total_tokens,
+                           "decode_kernel_us": dm * 1e3, "launches_per_call": rr["launches_per_call"],
+                           "batch": ww.batch, "total_tokens": ww.total_tokens,
                            "counted_bytes": b, "us_per_batch_l2_warm": statistics.median(rr["warm_ms"]) * 1e3}
             del rr
             if ww is not w:
@@ -674,7 +681,8 @@ def main():
                      "algorithmic_bytes_per_launch": cb},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches_per_call * args.steps,
+        "launches_per_call": launches_per_call,
         "clocks": clocks,
         "parity": parity,
         "workloads": table,

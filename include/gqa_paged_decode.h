@@ -136,6 +136,36 @@ int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_p
                                 int tier2_min_units);
 
 /*
+ * How a call combines the split pieces of its sequences (process-wide, for
+ * tests and benchmarks):
+ * 0 - default: a grid of every tier-1 and tier-2 decode CTA, followed by the
+ *     LSE merge kernel (a programmatic dependent of the decode grid).
+ * 1 - one wave: the decode kernel is launched cooperatively with only its
+ *     tier-1 CTAs (one per resident slot); their warps take the tier-2 ranges
+ *     from counters in the workspace, publish a record of where each range's
+ *     last sequence is cut, and after their stream merge the sequences cut at
+ *     their share of the boundaries and write the empty sequences, so a call is
+ *     a single kernel. Used for the cp.async variants when the device holds
+ *     every tier-1 CTA at once and tier2_ctas is at most 15 per tier-1 CTA;
+ *     otherwise (and for the TMA-gather variant) a call runs as in 0. Its
+ *     stream is as fast as mode 0's decode kernel, but its in-kernel merge
+ *     (one warp per share, a chain of dependent round trips) ends later than
+ *     the merge kernel, so it is not the default.
+ * Returns GQA_ERR_INVALID_ARGUMENT for another value.
+ */
+int gqa_paged_decode_set_merge_mode(int mode);
+
+/*
+ * Kernels launched by the calling host thread's most recent call of
+ * gqa_paged_decode, _ws, _checked, _noalloc, _fp8 or gqa_sparse_paged_decode
+ * (0 if it launched none, for example batch == 0 or an error before launch):
+ * 2 with the merge kernel (the default), 1 in the one-wave mode, plus one for the slot
+ * resolution of a selected-token call and one for the checked call's
+ * validation. For tests and benchmarks.
+ */
+int gqa_paged_decode_last_launch_count(void);
+
+/*
  * Profiling hook: when both are non-NULL (cudaEvent_t handles), every later
  * call records `decode_start` just before and `decode_stop` just after the
  * decode kernel on its stream (the merge launch then waits for the decode
@@ -294,7 +324,10 @@ int gqa_sparse_paged_decode(const void* q, const void* k_cache, const void* v_ca
  * word: bit 1 / 2 = a pipeline wait of the TMA-gather decode variant or the
  * tensor-memory MLA kernel gave up (after ~2 s by default; the kernel drained
  * its copies in flight and returned early, so that call's outputs are not
- * valid), bit 4 = bad page id, bit 8 = bad kv_indptr. 0 means no error.
+ * valid), bit 4 = bad page id, bit 8 = bad kv_indptr, bit 16 = an arrival or
+ * range counter could not be claimed, bit 32 = an in-kernel merge gave up
+ * waiting for a sequence's pieces (that sequence's outputs are not valid).
+ * 0 means no error.
  */
 int gqa_paged_decode_device_error(int* flags);
 
@@ -308,12 +341,14 @@ int gqa_paged_decode_device_error(int* flags);
  * lse; the device workspace is left unallocated). 0 turns it off. Returns
  * GQA_ERR_INVALID_ARGUMENT for count < 0.
  *
- * gqa_paged_decode_test_wait_limit_ns(ns): the give-up limit of the bounded
- * mbarrier waits of the TMA-gather decode variant (gather = 1 in
- * gqa_paged_decode_set_tuning), in nanoseconds; 0 restores the default of
- * 2 s. A wait that runs out sets bit 1 or 2 of the device error word and the
- * CTA returns after its copies in flight have landed (that drain keeps the
- * 2 s limit), so a call made with a tiny limit completes, with outputs that
+ * gqa_paged_decode_test_wait_limit_ns(ns): the give-up limit, in
+ * nanoseconds, of the bounded waits of the decode kernels: the mbarrier waits
+ * of the TMA-gather variant (gather = 1 in gqa_paged_decode_set_tuning) and,
+ * in the one-wave mode, a warp's wait for the pieces of a sequence it merges.
+ * 0 restores the default of 2 s. A wait that runs out sets bit 1, 2 or 32 of
+ * the device error word; a TMA-variant CTA returns after its copies in flight
+ * have landed (that drain keeps the 2 s limit), a merging warp skips that
+ * merge. A call made with a tiny limit therefore completes, with outputs that
  * are not valid.
  */
 int gqa_paged_decode_test_fail_allocs(int count);

@@ -48,6 +48,8 @@ _SIGNATURES = {
     "gqa_paged_decode_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, ctypes.c_int, _vp]),
     "gqa_mla_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp] + [ctypes.c_int] * 6 + [_vp]),
     "gqa_mla_set_tuning": (ctypes.c_int, [ctypes.c_int]),
+    "gqa_paged_decode_set_merge_mode": (ctypes.c_int, [ctypes.c_int]),
+    "gqa_paged_decode_last_launch_count": (ctypes.c_int, []),
     "gqa_paged_decode_test_fail_allocs": (ctypes.c_int, [ctypes.c_int]),
     "gqa_paged_decode_test_wait_limit_ns": (ctypes.c_int, [ctypes.c_uint64]),
 }
@@ -147,6 +149,17 @@ def gqa_paged_decode_device_error() -> int:
     if rc != GQA_OK:
         raise GqaError(rc, "gqa_paged_decode_device_error")
     return flags.value
+
+
+MERGE_KERNEL, MERGE_ONE_WAVE = 0, 1
+
+
+def gqa_paged_decode_set_merge_mode(mode: int) -> int:
+    return load().gqa_paged_decode_set_merge_mode(mode)
+
+
+def gqa_paged_decode_last_launch_count() -> int:
+    return load().gqa_paged_decode_last_launch_count()
 
 
 def gqa_paged_decode_test_fail_allocs(count: int) -> int:

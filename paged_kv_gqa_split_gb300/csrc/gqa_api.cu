@@ -54,6 +54,7 @@ struct Tuning {
   int fuse_max_splits = gqa::kDefaultFuseMaxSplits;
   KernelChoice kernel = {gqa::kGatherLsu, 4, 16, 2};
   int mla_kernel = gqa::kMlaKernelDefault;
+  int merge_mode = 0;  // 0: decode grid + merge kernel; 1: one-wave decode with the merge inside it when possible
 };
 
 std::mutex g_mu;
@@ -64,6 +65,9 @@ Tuning g_tune;
 // give-up limit of the TMA variant's bounded waits (0: the default).
 int g_fail_allocs = 0;
 unsigned long long g_wait_limit_ns = 0;
+// Kernels launched by this host thread's latest decode call (see
+// gqa_paged_decode_last_launch_count).
+thread_local int t_last_launches = 0;
 cudaEvent_t g_ev_start = nullptr;
 cudaEvent_t g_ev_stop = nullptr;
 // Ticket epoch of each call (never 0; 40 bits), so arrival tickets left by an
@@ -130,11 +134,15 @@ size_t tickets_bytes(int num_ctas, int ng) { return static_cast<size_t>(num_ctas
 
 size_t split_rec_bytes(int num_ctas) { return static_cast<size_t>(num_ctas) * 16; }
 
-// Layout: partial O | partial LSE | arrival tickets | split records, each 256-byte aligned.
+// Tier-2 range counters of the one-wave mode: one 8-byte word per warp index.
+size_t grab_bytes() { return static_cast<size_t>(gqa::kKvHeads) * sizeof(unsigned long long); }
+
+// Layout: partial O | partial LSE | arrival tickets | split records | tier-2
+// range counters, each 256-byte aligned.
 size_t workspace_bytes(int num_ctas, int ng) {
   const size_t o = partial_o_floats(num_ctas, ng) * sizeof(float);
   return round256(o) + round256(partial_lse_bytes(num_ctas, ng)) + round256(tickets_bytes(num_ctas, ng)) +
-         round256(split_rec_bytes(num_ctas));
+         round256(split_rec_bytes(num_ctas)) + round256(grab_bytes());
 }
 
 int check_args(const void* q, const void* k, const void* v, const int32_t* indptr, const int32_t* indices,
@@ -193,6 +201,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
     if (rc0 != GQA_OK) return rc0;
   }
   int rc = GQA_OK;
+  t_last_launches = 0;
   if (batch == 0) return GQA_OK;
   if (checked && (num_pages <= 0 || dev_err == nullptr || !aligned(dev_err, 4))) return GQA_ERR_INVALID_ARGUMENT;
   const int64_t sparse_total = sj != nullptr ? static_cast<int64_t>(batch) * sj->topk : 0;
@@ -204,6 +213,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   cudaEvent_t ev0, ev1;
   void* ws = nullptr;
   unsigned long long wait_limit_ns = gqa::kDefaultWaitLimitNs;
+  bool one_wave = false;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     rc = current_device(&dev, &st);
@@ -228,6 +238,13 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
         cfg.tier2_ctas = cfg.tier2_ctas > drop ? cfg.tier2_ctas - drop : 0;
       }
     }
+    // one wave (the tier-1 CTAs, all resident; tier 2 taken by their warps;
+    // merge in the kernel) for the cp.async variants when the device holds the
+    // whole grid and the warps can take all of tier 2
+    if (tune.merge_mode == 1 && tune.kernel.gather != gqa::kGatherTma &&
+        cfg.tier2_ctas <= (gqa::kMaxWarpRanges - 1) * cfg.tier1_ctas &&
+        cfg.tier1_ctas <= gqa::decode_coresident_ctas(tune.kernel, sj != nullptr))
+      one_wave = true;
     const size_t need = workspace_bytes(cfg.tier1_ctas + cfg.tier2_ctas, ng) +
                         round256(static_cast<size_t>(sparse_total) * sizeof(int32_t));
     if (user_ws != nullptr) {
@@ -246,7 +263,10 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   float* part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + lse_off);
   const size_t tickets_off = lse_off + round256(partial_lse_bytes(ctas, ng));
   unsigned long long* tickets = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + tickets_off);
-  int4* split_rec = reinterpret_cast<int4*>(static_cast<char*>(ws) + tickets_off + round256(tickets_bytes(ctas, ng)));
+  const size_t rec_off = tickets_off + round256(tickets_bytes(ctas, ng));
+  int4* split_rec = reinterpret_cast<int4*>(static_cast<char*>(ws) + rec_off);
+  unsigned long long* grab =
+      reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + rec_off + round256(split_rec_bytes(ctas)));
   const unsigned long long epoch = (g_epoch.fetch_add(1) % ((1ull << 40) - 1)) + 1;
 
   if (sj != nullptr) {  // resolve every selected column to its slot first
@@ -290,15 +310,28 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   dp.scale_log2 = sm_scale * kLog2e;
   dp.num_pages_check = checked ? num_pages : 0;
   dp.wait_limit_ns = wait_limit_ns;
+  dp.inline_merge = one_wave ? 1 : 0;
+  dp.grab = grab;
+  if (one_wave) dp.fuse_max_splits = 1;  // every split sequence is merged by the in-kernel duties
 
   const bool profile = ev0 != nullptr && ev1 != nullptr;
   if (profile && cudaEventRecord(ev0, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
-  // selected-token mode: the decode is a programmatic dependent of the resolve
-  // kernel unless events (or the checked path's validation) sit between them
-  const cudaError_t le = sj != nullptr ? gqa::launch_decode_lsu_sparse(dp, ctas, stream, !profile && !checked)
-                                       : gqa::launch_decode(tune.kernel, dp, ctas, stream);
+  // one wave: the tier-1 CTAs only, launched cooperatively. Otherwise the whole
+  // grid; in selected-token mode the decode is then a programmatic dependent of
+  // the resolve kernel unless events (or the checked path's validation) sit
+  // between them.
+  const int grid = one_wave ? cfg.tier1_ctas : ctas;
+  const int launch = one_wave ? gqa::kLaunchCooperative
+                              : (sj != nullptr && !profile && !checked ? gqa::kLaunchPdl : gqa::kLaunchPlain);
+  const cudaError_t le = sj != nullptr ? gqa::launch_decode_lsu_sparse(dp, grid, stream, launch)
+                                       : gqa::launch_decode(tune.kernel, dp, grid, stream, launch);
   if (le != cudaSuccess) return GQA_ERR_LAUNCH;
   if (profile && cudaEventRecord(ev1, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
+  const int before = (sj != nullptr ? 1 : 0) + (checked ? 1 : 0);  // slot resolution, validation
+  if (one_wave) {  // the decode kernel merged the split sequences and wrote the empty ones
+    t_last_launches = before + 1;
+    return GQA_OK;
+  }
 
   gqa::MergeParams mp{};
   mp.kv_indptr = indptr;
@@ -316,6 +349,7 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
   mp.use_pdl = profile ? 0 : 1;
   mp.fuse_max_splits = tune.fuse_max_splits;
   if (gqa::launch_merge(ng, mp, stream) != cudaSuccess) return GQA_ERR_LAUNCH;
+  t_last_launches = before + 2;
   return GQA_OK;
 }
 
@@ -435,7 +469,17 @@ int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_p
   if (!valid_kernel(t.kernel)) return GQA_ERR_INVALID_ARGUMENT;
   std::lock_guard<std::mutex> lock(g_mu);
   t.mla_kernel = g_tune.mla_kernel;  // set by gqa_mla_set_tuning
+  t.merge_mode = g_tune.merge_mode;  // set by gqa_paged_decode_set_merge_mode
   g_tune = t;
+  return GQA_OK;
+}
+
+int gqa_paged_decode_last_launch_count(void) { return t_last_launches; }
+
+int gqa_paged_decode_set_merge_mode(int mode) {
+  if (mode != 0 && mode != 1) return GQA_ERR_INVALID_ARGUMENT;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_tune.merge_mode = mode;
   return GQA_OK;
 }
 

@@ -61,6 +61,46 @@ __device__ __forceinline__ int load_indptr_window(const int* __restrict__ indptr
   return pos <= batch ? __ldg(indptr + pos) : INT32_MAX;
 }
 
+// First round of warp_find_window for the whole table, which needs no token
+// position: the 32 entries it samples (batch > 32) or the window at 0 (batch
+// <= 32). Loading it together with kv_indptr[batch] puts both in one round trip.
+__device__ __forceinline__ int first_search_round(const int* __restrict__ indptr, int batch, int lane) {
+  if (batch > 32) {
+    const int step = (batch + 31) / 32;
+    const int pos = lane * step;
+    return pos < batch ? __ldg(indptr + pos) : INT32_MAX;
+  }
+  return lane <= batch ? __ldg(indptr + lane) : INT32_MAX;
+}
+
+// A 32-entry kv_indptr window win = kv_indptr[base + lane] (INT32_MAX past the
+// end) with kv_indptr[base] <= t, found with the 32-ary search of
+// warp_find_seq; its last round is the window itself, so no separate window
+// load follows. The sequence holding t is at window index 31 - clz(ballot(win
+// <= t)), unless every entry is <= t (then the window must move on). `pre`,
+// when has_pre, is first_search_round's value for this table. Returns base, or
+// -1 if kv_indptr[0] > t (a malformed table).
+__device__ __forceinline__ int warp_find_window(const int* __restrict__ indptr, int batch, int t, int lane,
+                                                bool has_pre, int pre, int& win) {
+  int lo = 0, hi = batch;
+  bool use_pre = has_pre;
+  while (hi - lo > 32) {
+    const int step = (hi - lo + 31) / 32;
+    const int pos = lo + lane * step;
+    const int val = use_pre ? pre : (pos < hi ? __ldg(indptr + pos) : INT32_MAX);
+    use_pre = false;
+    const unsigned m = __ballot_sync(0xffffffffu, val <= t);
+    if (m == 0) return -1;
+    const int k = 31 - __clz(m);
+    const int nlo = lo + k * step;
+    hi = min(nlo + step, hi);
+    lo = nlo;
+  }
+  win = use_pre ? pre : load_indptr_window(indptr, batch, lo, lane);
+  if (__ballot_sync(0xffffffffu, win <= t) == 0) return -1;
+  return lo;
+}
+
 // Online-softmax state of one warp (one KV head, 8 query heads) over a piece.
 struct HeadState {
   uint32_t qf[16];   // Q^T B-fragments: dims 16 kk + {0..7} (qf[2kk]) and {8..15} (qf[2kk+1])
@@ -287,21 +327,99 @@ struct SplitInfo {
   int first_slot;
 };
 
-// Arrival ticket of one split sequence (one per KV head): the word holds
-// (call epoch << 24) | pieces arrived. A word from an earlier call (another
-// epoch) counts as zero, so the tickets need no clearing between calls.
-// Returns the number of pieces arrived including this one, or 0 if the CAS
-// loop did not settle (then the merge kernel is not told and an error is set).
-__device__ __forceinline__ unsigned ticket_arrive(unsigned long long* ticket, unsigned long long epoch, int* err) {
-  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ticket);
-  for (int it = 0; it < (1 << 16); ++it) {
-    const unsigned long long nv = ((cur >> 24) == epoch) ? cur + 1 : ((epoch << 24) | 1ull);
-    const unsigned long long prev = atomicCAS(ticket, cur, nv);
-    if (prev == cur) return static_cast<unsigned>(nv & 0xffffffull);
-    cur = prev;
+// Epoch-tagged counter word: (call epoch << 24) | count. A word tagged with
+// another epoch (an earlier call's, or never-written memory) counts as zero, so
+// these counters need no clearing between calls.
+//
+// Adds one and returns the count before the addition. The first warp of a call
+// to find the word stale installs this call's tag with its own addition counted
+// (compare-and-swap); additions that other warps made to the stale word before
+// that are discarded and retried, so every count from 0 up is handed out exactly
+// once. Returns -1 (and sets kErrTicket) if the word could not be claimed, which
+// takes many thousands of competing writers.
+__device__ __forceinline__ long long tagged_fetch_add(unsigned long long* word, unsigned long long epoch, int* err) {
+  unsigned long long v = atomicAdd(word, 1ull);
+  for (int it = 0; (v >> 24) != epoch; ++it) {
+    if (it >= 64) {
+      atomicOr(err, kErrTicket);
+      return -1;
+    }
+    unsigned long long cur = v + 1;  // the word as this warp left it
+    for (int k = 0; k < 4096 && (cur >> 24) != epoch; ++k) {
+      const unsigned long long prev = atomicCAS(word, cur, (epoch << 24) | 1ull);
+      if (prev == cur) return 0;  // installed: this addition took count 0
+      cur = prev;
+    }
+    v = atomicAdd(word, 1ull);  // another warp installed the tag first
+  }
+  return static_cast<long long>(v & 0xffffffull);
+}
+
+// Polls of a counter word that is not installed yet, at 256 ns or more each:
+// the wait gives up after about a second.
+constexpr int kInstallWaitRounds = 1 << 22;
+
+// One-wave mode: the counter words (tier-2 range counters, arrival tickets)
+// each have one installer, a warp that resets the word to this call's tag
+// with count 0 at the start of the kernel (atomic exchange). Adds one and
+// returns the count before the addition; an addition that found the word
+// still stale (the installer had not run yet; every CTA is resident, so it
+// will) was discarded by the install, so the warp waits for the tag and adds
+// again. No compare-and-swap races: with hundreds of warps adding to one word
+// at once, claiming it by compare-and-swap thrashes. Returns -1 (and sets
+// kErrTicket) if the tag did not appear within kInstallWaitRounds polls.
+__device__ __forceinline__ void install_counter(unsigned long long* word, unsigned long long epoch) {
+  atomicExch(word, epoch << 24);
+}
+
+__device__ __forceinline__ long long installed_fetch_add(unsigned long long* word, unsigned long long epoch, int* err) {
+  for (int it = 0; it < kInstallWaitRounds; ++it) {
+    const unsigned long long v = atomicAdd(word, 1ull);
+    if ((v >> 24) == epoch) return static_cast<long long>(v & 0xffffffull);
+    // not installed yet: wait for the tag, then add again
+    while ((ld_acquire_u64(word) >> 24) != epoch && ++it < kInstallWaitRounds) __nanosleep(256);
   }
   atomicOr(err, kErrTicket);
-  return 0;
+  return -1;
+}
+
+// Arrival ticket of one split sequence (one per KV head): counts the pieces
+// that have written their partials. Returns the pieces arrived including this
+// one, or 0 if the ticket could not be claimed (an error is set).
+__device__ __forceinline__ unsigned ticket_arrive(unsigned long long* ticket, unsigned long long epoch, int* err) {
+  const long long before = tagged_fetch_add(ticket, epoch, err);
+  return before < 0 ? 0u : static_cast<unsigned>(before + 1);
+}
+
+// Bounded wait (lane 0 polls, the warp follows) until an arrival ticket reads
+// `pieces` arrivals in this call's epoch. The polls are relaxed loads with a
+// back-off (many warps may poll one ticket while the arrivals still land on
+// it); once the count shows, a fence orders the warp's later loads of the
+// partials after the writers' release (their fence before the arrival), and
+// __syncwarp carries that order to the other lanes. Returns false (and sets
+// kErrMergeWait) after limit_ns.
+__device__ __forceinline__ bool wait_ticket(const unsigned long long* ticket, unsigned long long epoch,
+                                            unsigned pieces, uint64_t limit_ns, int* err, int lane) {
+  int ok = 0;
+  if (lane == 0) {
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+      const unsigned long long v = ld_relaxed_u64(ticket);
+      if ((v >> 24) == epoch && (v & 0xffffffull) >= pieces) {
+        ok = 1;
+        break;
+      }
+      if (global_timer_ns() - t0 > limit_ns) {
+        atomicOr(err, kErrMergeWait);
+        break;
+      }
+      __nanosleep(256);
+    }
+    __threadfence();
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
 }
 
 // Merge the S fp32 partials of one split sequence for one KV head (8 query

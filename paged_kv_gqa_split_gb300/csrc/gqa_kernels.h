@@ -18,6 +18,7 @@ constexpr int kErrTimeoutEmpty = 2;  // the producer waited too long for a free 
 constexpr int kErrBadPage = 4;       // a kv_indices entry outside [0, num_pages)
 constexpr int kErrBadIndptr = 8;     // kv_indptr not starting at 0 / decreasing
 constexpr int kErrTicket = 16;       // a split sequence's arrival ticket did not settle
+constexpr int kErrMergeWait = 32;    // an in-kernel merge waited too long for a sequence's pieces
 
 struct DecodeParams {
   const void* q;
@@ -42,8 +43,17 @@ struct DecodeParams {
   float scale_log2;        // sm_scale * log2(e)
   int num_pages_check;     // > 0: page ids are range-checked against it
   int fuse_max_splits;     // split sequences of at most this many pieces are merged by the decode kernel
-  unsigned long long wait_limit_ns;  // TMA variant: give-up limit of a bounded mbarrier wait
+  unsigned long long wait_limit_ns;  // give-up limit of a bounded wait (TMA variant; in-kernel merge)
+  int inline_merge;             // one-wave mode: grid = tier-1 CTAs, tier 2 taken from `grab`, merge in-kernel
+  unsigned long long* grab;     // [NG] one-wave mode: tier-2 range counters (epoch-tagged)
 };
+
+// One-wave mode: a warp walks at most this many ranges (its tier-1 range and
+// tier-2 ranges); the host uses the mode only when P2 <= (this - 1) * P1.
+constexpr int kMaxWarpRanges = 16;
+
+// How a decode kernel is launched.
+enum : int { kLaunchPlain = 0, kLaunchPdl = 1, kLaunchCooperative = 2 };
 
 // Default give-up limit of a bounded mbarrier wait (the drain before exit keeps it).
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
@@ -136,10 +146,14 @@ struct KernelChoice {
 
 int lsu_smem_bytes(int ng, int stages);
 int lsu_f8_smem_bytes(int stages);
-cudaError_t launch_decode_lsu_f8(int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream);
-cudaError_t launch_decode_lsu(int ng, int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream);
+cudaError_t launch_decode_lsu_f8(int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream, int launch);
+cudaError_t launch_decode_lsu(int ng, int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream,
+                              int launch);
 // The selected-token variant (p.sparse_topk > 0): 4 KV heads per CTA, 2 stages.
-cudaError_t launch_decode_lsu_sparse(const DecodeParams& p, int num_ctas, cudaStream_t stream, bool pdl);
+cudaError_t launch_decode_lsu_sparse(const DecodeParams& p, int num_ctas, cudaStream_t stream, int launch);
+// CTAs of a cp.async variant (sparse: the selected-token one) that the current
+// device holds at once; 0 for the TMA variant or if unknown.
+int decode_coresident_ctas(const KernelChoice& k, bool sparse);
 // Resolve the selected columns of a sparse batch to slots (-1: invalid column).
 cudaError_t launch_sparse_resolve(const int* logical_indices, const int* block_table, const int* token_to_req,
                                   int* slots, int rows, int topk, int page_size, int page_table_width,
@@ -163,10 +177,11 @@ inline int decode_max_ctas_per_sm(const KernelChoice& k) {
   return k.gather == kGatherLsu ? 16 / k.heads_per_cta : 4 / k.heads_per_cta;
 }
 
-inline cudaError_t launch_decode(const KernelChoice& k, const DecodeParams& p, int num_ctas, cudaStream_t stream) {
-  if (k.gather == kGatherLsu) return launch_decode_lsu(k.heads_per_cta, k.stages, p, num_ctas, stream);
+inline cudaError_t launch_decode(const KernelChoice& k, const DecodeParams& p, int num_ctas, cudaStream_t stream,
+                                 int launch) {
+  if (k.gather == kGatherLsu) return launch_decode_lsu(k.heads_per_cta, k.stages, p, num_ctas, stream, launch);
   if (k.gather == kGatherTma) return launch_decode_tma(k.heads_per_cta, k.tile, k.stages, p, num_ctas, stream);
-  if (k.gather == kGatherLsuF8) return launch_decode_lsu_f8(k.stages, p, num_ctas, stream);
+  if (k.gather == kGatherLsuF8) return launch_decode_lsu_f8(k.stages, p, num_ctas, stream, launch);
   return cudaErrorInvalidValue;
 }
 

@@ -4,7 +4,8 @@
   workspace allocation fail exactly where a failing cudaMalloc would. The call
   must return GQA_ERR_WORKSPACE without writing its outputs, and the next call
   must allocate and give the oracle's result.
-* A bounded pipeline wait that runs out: the TMA-gather decode variant bounds
+* A bounded in-kernel merge wait that runs out (the one-wave decode), and a
+  bounded pipeline wait that runs out: the TMA-gather decode variant bounds
   every mbarrier wait. With the give-up limit shortened to a few nanoseconds
   (valid inputs, nothing else changed) its waits give up before the first copies
   land; the CTAs drain their copies in flight (that drain keeps its normal
@@ -23,7 +24,7 @@ from paged_kv_gqa_split_gb300.build import build
 pytestmark = pytest.mark.gpu
 
 O_ATOL, O_RTOL, LSE_ATOL = 2e-2, 2e-2, 1e-3
-ERR_TIMEOUT_FULL, ERR_TIMEOUT_EMPTY = 1, 2
+ERR_TIMEOUT_FULL, ERR_TIMEOUT_EMPTY, ERR_MERGE_WAIT = 1, 2, 32
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -88,6 +89,33 @@ def test_injected_failure_count_and_reset():
     out, lse = _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, w.sm_scale)
     torch.cuda.synchronize()
     _matches_oracle(w, out, lse)
+
+
+def test_in_kernel_merge_wait_gives_up_and_call_completes():
+    """The one-wave decode (an opt-in mode) merges a split sequence once all of its pieces have
+    arrived, waiting at most the give-up limit. With that limit at a few
+    nanoseconds, a merge of a sequence cut into hundreds of pieces gives up: the
+    call completes, bit 32 of the device error word is set, and a following call
+    with the normal limit is correct."""
+    w = wl.make_workload([60000, 0, 900, 40000], seed=64, pool_factor=1.1)
+    g = w.to("cuda")
+    assert _lib.gqa_paged_decode_device_error() == 0
+    assert _lib.gqa_paged_decode_set_merge_mode(_lib.MERGE_ONE_WAVE) == 0
+    try:
+        assert _lib.gqa_paged_decode_test_wait_limit_ns(5) == 0
+        _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, w.sm_scale)
+        torch.cuda.synchronize()
+        flags = _lib.gqa_paged_decode_device_error()
+        assert flags & ERR_MERGE_WAIT, flags
+        assert flags & ~ERR_MERGE_WAIT == 0, flags
+        assert _lib.gqa_paged_decode_test_wait_limit_ns(0) == 0
+        out, lse = _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, w.sm_scale)
+        torch.cuda.synchronize()
+        _matches_oracle(w, out, lse)
+        assert _lib.gqa_paged_decode_device_error() == 0
+    finally:
+        _lib.gqa_paged_decode_test_wait_limit_ns(0)
+        _lib.gqa_paged_decode_set_merge_mode(_lib.MERGE_KERNEL)
 
 
 @pytest.mark.parametrize("variant", [(0, 0, 4, 16, 5, 1), (0, 0, 4, 32, 3, 1), (0, 0, 1, 16, 4, 1)])

@@ -39,10 +39,20 @@ def tuning():
     assert _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0) == 0
 
 
+@pytest.fixture(params=[_lib.MERGE_KERNEL, _lib.MERGE_ONE_WAVE], ids=["merge_kernel", "one_wave"])
+def merge_mode(request):
+    """Run a test with the static grid followed by the merge kernel (the default)
+    and with the one-wave decode (merge inside the kernel)."""
+    assert _lib.gqa_paged_decode_set_merge_mode(request.param) == 0
+    yield request.param
+    assert _lib.gqa_paged_decode_set_merge_mode(_lib.MERGE_KERNEL) == 0
+
+
 def gpu_run(w, dev="cuda"):
     g = w.to(dev)
     out, lse = _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, w.sm_scale)
     torch.cuda.synchronize()
+    assert _lib.gqa_paged_decode_last_launch_count() in (1, 2)
     return out.float().cpu().double().numpy(), lse.cpu().double().numpy()
 
 
@@ -98,7 +108,7 @@ EDGE_LENS = {
 
 
 @pytest.mark.parametrize("name", sorted(EDGE_LENS))
-def test_edge_cases_default(name):
+def test_edge_cases_default(name, merge_mode):
     w = wl.make_workload(EDGE_LENS[name], seed=100 + len(name), pool_factor=1.5)
     out, lse = gpu_run(w)
     check(w, out, lse)
@@ -137,7 +147,7 @@ VARIANTS = {
 
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
 @pytest.mark.parametrize("case", ["ragged_mix", "leading_trailing_empty", "ramp_1_40"])
-def test_kernel_variants(tuning, variant, case):
+def test_kernel_variants(tuning, variant, case, merge_mode):
     tuning(*VARIANTS[variant])
     w = wl.make_workload(EDGE_LENS[case], seed=7, pool_factor=1.25)
     out, lse = gpu_run(w)
@@ -147,7 +157,7 @@ def test_kernel_variants(tuning, variant, case):
 @pytest.mark.parametrize("ng,stages", [(4, 3), (4, 2), (1, 2)])
 @pytest.mark.parametrize("fuse", [0, -1, 64, 2, 5])
 @pytest.mark.parametrize("num_ctas,min_units", [(152, 16), (40, 16), (300, 1), (3, 1), (90, 1), (1200, 1)])
-def test_split_and_merge_paths(tuning, num_ctas, min_units, fuse, ng, stages):
+def test_split_and_merge_paths(tuning, num_ctas, min_units, fuse, ng, stages, merge_mode):
     """One long and several short sequences cut into 2 to ~300 pieces, with the merge
     done in the decode kernel (up to `fuse` pieces; 0 = default 16, -1 = never; the
     warp stages 4 partials per round trip, so 5 and 16 take several batches) or by
@@ -163,7 +173,7 @@ def test_split_and_merge_paths(tuning, num_ctas, min_units, fuse, ng, stages):
                                      (90, 8, 4, 32, 3, 1), (300, 8, 4, 16, 5, 1), (200, 8, 4, 16, 3, 0, -1),
                                      (600, 8, 1, 16, 3, 0, 64), (300, 8, 4, 16, 5, 1, -1),
                                      (100, 8, 4, 16, 2, 0, 0, 700, 500, 4), (100, 8, 4, 16, 2, 0, -1, 700, 500, 4)])
-def test_token_count_exact_with_uniform_scores(tuning, variant):
+def test_token_count_exact_with_uniform_scores(tuning, variant, merge_mode):
     """q = 0 makes every score 0: lse must be log2(n) to fp32 precision, which a
     dropped or doubled token would break (1.44/n >> 2e-5 for n <= 9000), and O
     must be the mean of the sequence's V rows."""
@@ -180,13 +190,13 @@ def test_token_count_exact_with_uniform_scores(tuning, variant):
     check(w, out, lse)
 
 
-def test_peaky_softmax_large_scores():
+def test_peaky_softmax_large_scores(merge_mode):
     w = wl.make_workload([700, 64, 3], seed=44, q_std=30.0)
     out, lse = gpu_run(w)
     check(w, out, lse)
 
 
-def test_deterministic_bitwise():
+def test_deterministic_bitwise(merge_mode):
     w = wl.make_workload([1000, 0, 333, 4096], seed=45)
     g = w.to("cuda")
     o1, l1 = _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices)
@@ -195,7 +205,7 @@ def test_deterministic_bitwise():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_int64_page_addressing():
+def test_int64_page_addressing(merge_mode):
     """Pages above 2^21 sit more than 2^31 bytes into each 1 KB-per-page pool."""
     num_pages = (1 << 21) + 4096
     small = wl.make_workload([40, 0, 300], seed=46, pool_factor=1.0)
@@ -214,7 +224,7 @@ def test_int64_page_addressing():
 
 
 # ----------------------------------------------------------- entry variants
-def test_workspace_variant_matches_and_rejects_small():
+def test_workspace_variant_matches_and_rejects_small(merge_mode):
     w = wl.make_workload([2000, 5, 0, 700], seed=47)
     g = w.to("cuda")
     need = _lib.gqa_paged_decode_ws_size(w.batch, w.total_tokens)
@@ -230,7 +240,7 @@ def test_workspace_variant_matches_and_rejects_small():
     assert e.value.code == _lib.GQA_ERR_WORKSPACE
 
 
-def test_checked_valid_matches_unchecked():
+def test_checked_valid_matches_unchecked(merge_mode):
     w = wl.make_workload([129, 0, 64, 1000], seed=48, pool_factor=1.3)
     g = w.to("cuda")
     o1, l1 = _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices)
@@ -240,7 +250,7 @@ def test_checked_valid_matches_unchecked():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_checked_rejects_bad_page_before_reading():
+def test_checked_rejects_bad_page_before_reading(merge_mode):
     w = wl.make_workload([50, 20], seed=49)
     g = w.to("cuda")
     bad_idx = g.kv_indices.clone()
@@ -276,7 +286,7 @@ def test_non_default_stream():
 
 # ------------------------------------------------------ the five workloads
 @pytest.mark.parametrize("name", ["tiny", "mid", "long", "large", "skewed"])
-def test_workload_parity(name):
+def test_workload_parity(name, merge_mode):
     """Every sequence of every workload, element by element, against the float64
     oracle (evaluated across the host's cores; the rows are the single-process
     oracle's, bit for bit)."""
@@ -287,6 +297,29 @@ def test_workload_parity(name):
     print(f"{name}: max |dO| {o_err:.3e}, max |dlse| {l_err:.3e}, all {w.batch} sequences checked")
     assert np.all(np.isfinite(out))
     assert np.all(np.isfinite(lse) | np.isneginf(lse))
+
+
+@pytest.fixture
+def one_wave():
+    assert _lib.gqa_paged_decode_set_merge_mode(_lib.MERGE_ONE_WAVE) == 0
+    yield
+    assert _lib.gqa_paged_decode_set_merge_mode(_lib.MERGE_KERNEL) == 0
+
+
+@pytest.mark.parametrize("tier2", [(0, 0, 0), (-1, 0, 0), (4000, 900, 1), (912, 500, 8), (6840, 100, 0),
+                                   (8000, 500, 1)])
+def test_one_wave_tier2_shapes(tuning, tier2, one_wave):
+    """One-wave mode with the default tiers, one tier, 90% of the line in 4000
+    small tier-2 ranges (about 9 per warp), half the line in tier 2, and 15
+    tier-2 ranges per tier-1 CTA (the most a warp takes on a 152-SM part); 8000
+    tier-2 CTAs are more than the warps may take, so that call falls back to the
+    merge kernel. A long sequence, short ones and empties, against the oracle."""
+    t2, permille, min_units = tier2
+    tuning(0, 0, 4, 16, 2, 0, 0, t2, permille, min_units)
+    w = wl.make_workload([70000, 0, 3, 1, 5000, 0, 129, 16, 17, 2049], seed=52, pool_factor=1.3)
+    out, lse = gpu_run(w)
+    assert _lib.gqa_paged_decode_last_launch_count() == (2 if t2 == 8000 else 1)
+    check(w, out, lse)
 
 
 def test_no_device_error_flagged():
