@@ -145,9 +145,10 @@ int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_p
  *     from counters in the workspace, publish a record of where each range's
  *     last sequence is cut, and after their stream merge the sequences cut at
  *     their share of the boundaries and write the empty sequences, so a call is
- *     a single kernel. Used for the cp.async variants when the device holds
- *     every tier-1 CTA at once and tier2_ctas is at most 15 per tier-1 CTA;
- *     otherwise (and for the TMA-gather variant) a call runs as in 0. Its
+ *     a single kernel. Used for the bf16 cp.async variants (dense and
+ *     selected-token) when the device holds every tier-1 CTA at once and
+ *     tier2_ctas is at most 15 per tier-1 CTA; otherwise (and for the
+ *     TMA-gather variant and FP8 caches) a call runs as in 0. Its
  *     stream is as fast as mode 0's decode kernel, but its in-kernel merge
  *     (one warp per share, a chain of dependent round trips) ends later than
  *     the merge kernel, so it is not the default.

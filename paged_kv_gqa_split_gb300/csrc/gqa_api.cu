@@ -239,9 +239,9 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
       }
     }
     // one wave (the tier-1 CTAs, all resident; tier 2 taken by their warps;
-    // merge in the kernel) for the cp.async variants when the device holds the
-    // whole grid and the warps can take all of tier 2
-    if (tune.merge_mode == 1 && tune.kernel.gather != gqa::kGatherTma &&
+    // merge in the kernel) for the bf16 cp.async variants when the device holds
+    // the whole grid and the warps can take all of tier 2
+    if (tune.merge_mode == 1 && tune.kernel.gather == gqa::kGatherLsu &&
         cfg.tier2_ctas <= (gqa::kMaxWarpRanges - 1) * cfg.tier1_ctas &&
         cfg.tier1_ctas <= gqa::decode_coresident_ctas(tune.kernel, sj != nullptr))
       one_wave = true;

@@ -71,7 +71,7 @@ struct LsuCfg {
   static constexpr int kSkOff = kVOff + kTile * kV8Pitch;  // F8: K scales of the tile's tokens
   static constexpr int kSvOff = kSkOff + kTile * 4;         // F8: V scales
   static constexpr int kHdrOff = F8 ? kSvOff + kTile * 4 : 2 * kTile * kRowPitch;
-  static constexpr int kStageBytes = kHdrOff + 48;    // tile header: 12 ints
+  static constexpr int kStageBytes = kHdrOff + 32;    // tile header: 8 ints
   static constexpr int kIdsRing = 256;                // page ids held per warp (tokens)
   static constexpr int kIdsOff = D * kStageBytes;
   static constexpr int kPlanOff = kIdsOff + kIdsRing * 4;  // the warp's copy of the plan (SmemPlan)
@@ -457,11 +457,11 @@ __global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kern
   const uint8_t* __restrict__ kc = static_cast<const uint8_t*>(p.k_cache);
   const uint8_t* __restrict__ vc = static_cast<const uint8_t*>(p.v_cache);
   const __nv_bfloat16* __restrict__ qg = static_cast<const __nv_bfloat16*>(p.q);
-  const bool one_wave = p.inline_merge != 0;
+  const bool one_wave = !F8 && p.inline_merge != 0;  // the FP8 variants run the static grid only
   const int B = p.batch;
   // kv_indptr[B], the first round of the kv_indptr search and (one-wave mode)
   // this lane's empty-sequence check go out together: one round trip
-  const int pre = SP ? 0 : first_search_round(p.kv_indptr, B, lane);
+  const int pre = (SP || F8) ? 0 : first_search_round(p.kv_indptr, B, lane);
   const int T = SP ? p.sparse_total : __ldg(p.kv_indptr + B);
   if (!SP && one_wave) {
     for (int b0 = (blockIdx.x * NG + w) * 32; b0 < B; b0 += gridDim.x * NG * 32) {
@@ -523,7 +523,11 @@ __global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kern
     }
     return true;
   };
-  if (u0 < u1) open_segment(true);
+  // The bf16 variants open their first segment here, its search starting
+  // from the round loaded beside kv_indptr[B]; the FP8 variants open it in
+  // their first issue (measured: the early open slows their ALU-bound loop
+  // by about 5%).
+  if (!F8 && u0 < u1) open_segment(true);
 
   auto next_tile = [&](Tile& tl) -> bool {
     while (walk_ok) {
@@ -566,7 +570,7 @@ __global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kern
         tl.b = pb;
         tl.hg = hg;
         tl.tt = tt;
-        tl.vcta = splan->vcta;
+        tl.vcta = one_wave ? splan->vcta : static_cast<int>(blockIdx.x);
         tl.si = p_si;
         p_flags &= ~F_QLOAD;
         tt += tl.cnt;
@@ -692,8 +696,11 @@ __global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kern
       }
       if (lane == 0) {
         st_shared_v4(sb + C::kHdrOff, tl.b, tl.cnt, flags, tl.hg);
-        st_shared_v4(sb + C::kHdrOff + 16, tl.si.S, tl.si.first_cta, tl.vcta,
-                     static_cast<int>(mask) | (tl.si.first_slot << 16));
+        if constexpr (F8)  // the FP8 variants run the static grid: the virtual CTA is the CTA
+          st_shared_v4(sb + C::kHdrOff + 16, tl.si.S, tl.si.first_cta, tl.si.first_slot, static_cast<int>(mask));
+        else
+          st_shared_v4(sb + C::kHdrOff + 16, tl.si.S, tl.si.first_cta, tl.vcta,
+                       static_cast<int>(mask) | (tl.si.first_slot << 16));
       }
     } else if (more) {
       more = false;
@@ -731,9 +738,14 @@ __global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kern
     ld_shared_v4(sb + C::kHdrOff, hb, cnt, flags, thg);
     SplitInfo si;
     int tile_cta, tok_mask;
-    ld_shared_v4(sb + C::kHdrOff + 16, si.S, si.first_cta, tile_cta, tok_mask);
-    si.first_slot = tok_mask >> 16;
-    tok_mask &= 0xffff;
+    if constexpr (F8) {
+      ld_shared_v4(sb + C::kHdrOff + 16, si.S, si.first_cta, si.first_slot, tok_mask);
+      tile_cta = blockIdx.x;
+    } else {
+      ld_shared_v4(sb + C::kHdrOff + 16, si.S, si.first_cta, tile_cta, tok_mask);
+      si.first_slot = tok_mask >> 16;
+      tok_mask &= 0xffff;
+    }
     if (flags & F_DONE) break;
     const int h0 = (thg * NG + w) * kGroup;
     if (flags & F_QLOAD) {

@@ -121,11 +121,13 @@ def test_mla_without_lse():
     check(w, out, None)
 
 
-def test_mla_config_sampled_sequences():
-    w = wl.make_mla_config()
+@pytest.mark.parametrize("wide", [False, True])
+def test_mla_config_every_sequence(wide):
+    """The bench's MLA workloads (16 and 64 query heads) at full size, every
+    sequence against the oracle."""
+    w = wl.make_mla_config(wide)
     out, lse = gpu_mla(w)
-    lens = np.array(w.lens)
-    check(w, out, lse, sorted({0, int(np.argmax(lens)), w.batch // 2, w.batch - 1}))
+    check(w, out, lse)
 
 
 @pytest.mark.parametrize("kernel", [0, 1])
