@@ -383,6 +383,37 @@ def bench_fp8(w, g, device, steps, warmup, peak):
     return res
 
 
+# ------------------------------------------- mma.sync against CUDA cores
+def bench_cuda_cores(names, device, steps, warmup, peak, variant_only=False):
+    """The default decode (both contractions on mma.sync) against the same
+    pipeline with the contractions on the CUDA cores (gather 3), per workload:
+    µs per call and of the decode kernel alone, same timing method as the main
+    line. variant_only: time the CUDA-core variant only (for a profiler run)."""
+    res = {}
+    for name in names:
+        w = wl.make_config(name)
+        cb = counted_bytes(w.lens)
+        row = {}
+        for label, gather in (() if variant_only else (("mma_sync", 0),)) + (("cuda_cores", 3),):
+            assert _lib.gqa_paged_decode_set_tuning(0, 0, 4, 16, 2, gather) == 0
+            try:
+                r = bench_workload_gpu(w, device, steps, warmup, 1, with_hooks=not variant_only)
+            finally:
+                _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0)
+            ms = statistics.median(r["step_ms"])
+            row[label] = {"us_per_batch": ms * 1e3, "gbs": cb / (ms * 1e-3) / 1e9,
+                          "frac_of_peak": cb / (ms * 1e-3) / 1e9 / peak}
+            if r["decode_ms"]:
+                dm = statistics.median(r["decode_ms"])
+                row[label]["decode_kernel_us"] = dm * 1e3
+                row[label]["decode_frac_of_peak"] = cb / (dm * 1e-3) / 1e9 / peak
+            del r
+        if "mma_sync" in row:
+            row["cuda_cores_over_mma_sync"] = row["cuda_cores"]["us_per_batch"] / row["mma_sync"]["us_per_batch"]
+        res[name] = row
+    return res
+
+
 # ------------------------------------------------------------ MLA decode
 def bench_mla(device, steps, warmup, peak, wide: bool = False):
     """Dense MLA decode of the MLA workload (128 sequences of U[1024, 8192]
@@ -544,7 +575,7 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="time every decode variant instead of the contract line")
     ap.add_argument("--merge-mode", type=int, choices=[0, 1], default=0,
                     help="0: decode grid + merge kernel (default); 1: one-wave decode with the merge inside the kernel")
-    ap.add_argument("--only", choices=["fp8", "sparse", "mla", "mla-wide"], default=None,
+    ap.add_argument("--only", choices=["fp8", "sparse", "mla", "mla-wide", "cuda-cores"], default=None,
                     help="time only the FP8-cache decode of --workload, or only the selected-token decode, and "
                          "print its result (for profiling a small case)")
     args = ap.parse_args()
@@ -581,6 +612,8 @@ def main():
             res = bench_mla(device, args.steps, warmup, peak)
         elif args.only == "mla-wide":
             res = bench_mla(device, args.steps, warmup, peak, wide=True)
+        elif args.only == "cuda-cores":
+            res = bench_cuda_cores([args.workload], device, args.steps, warmup, peak, variant_only=True)
         else:
             res = bench_sparse(device, args.steps, warmup, peak)
         if rank == 0:
@@ -635,8 +668,9 @@ def main():
             if ww is not w:
                 del ww
 
-    append = sparse = fp8 = mla = mla_wide = None
+    append = sparse = fp8 = mla = mla_wide = cuda_cores = None
     if not args.no_workloads:
+        cuda_cores = bench_cuda_cores(["mid", "large"], device, args.steps, warmup, peak)
         append = bench_append(device, args.steps, warmup, w.batch, peak)
         sparse = bench_sparse(device, args.steps, warmup, peak)
         fp8 = bench_fp8(w, w.to(device), device, args.steps, warmup, peak)
@@ -691,6 +725,7 @@ def main():
         "fp8_decode": fp8,
         "mla_decode": mla,
         "mla_decode_64_heads": mla_wide,
+        "cuda_core_variant": cuda_cores,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -117,6 +117,9 @@ const char* gqa_paged_decode_strerror(int code);
  *   cp.async (default: heads 4, tile 16, stages 2, 3 CTAs per SM);
  *   1: one producer warp per CTA gathers whole page rows with TMA bulk copies
  *   (tile 16 or 32);
+ *   3: gather 0's pipeline (heads 4, tile 16, stages 2) with both contractions
+ *   on the CUDA cores (fp32 FMAs) instead of mma.sync, a variant kept for
+ *   comparing the two on this part;
  * fused_merge_max_splits - a sequence cut into at most this many pieces is
  *   merged by the decode kernel itself (the warp that finishes its last piece
  *   combines them); longer splits go to the merge kernel; default and -1: every

@@ -463,6 +463,9 @@ int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_p
   } else if (gather == gqa::kGatherTma) {
     t.kernel.tile = tile > 0 ? tile : 16;
     t.kernel.stages = stages > 0 ? stages : (t.kernel.tile == 32 ? 3 : (t.kernel.heads_per_cta == 4 ? 5 : 4));
+  } else if (gather == gqa::kGatherLsuCc) {
+    t.kernel.tile = tile > 0 ? tile : 16;
+    t.kernel.stages = stages > 0 ? stages : 2;
   } else {
     return GQA_ERR_INVALID_ARGUMENT;
   }

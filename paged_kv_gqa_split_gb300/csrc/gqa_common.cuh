@@ -294,6 +294,109 @@ __device__ __forceinline__ void attend_subtile_f8(HeadState& st, uint32_t k_addr
   }
 }
 
+// ------------------------------------------------- CUDA-core sub-tile
+// The same 16-token sub-tile with the two contractions on the CUDA cores
+// (fp32 FMAs) instead of mma.sync, for comparing the two on this part. Lane
+// (h = lane & 7, g = lane >> 3) holds query head h0 + h and dims 32 g .. 32 g
+// + 31: its Q slice in fp32, its slice of O, and the running max and sum of
+// head h (every lane of a head sees all 16 tokens, so m and l need no
+// reduction). Scores: 32 FMAs per token on the lane's K slice, then two xor
+// shuffles sum the four dim groups; P.V: 32 FMAs per token on its V slice,
+// with P in fp32.
+struct CcState {
+  float q[32];
+  float acc[32];
+  float m, l;
+  __device__ __forceinline__ void reset() {
+    m = -INFINITY;
+    l = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+  }
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// Q slice of lane (h, g) for query heads h0 .. h0 + 7 of sequence b, as 16 bf16 pairs.
+__device__ __forceinline__ void load_q_cc(uint32_t (&qf)[16], const __nv_bfloat16* q, int64_t b, int h0, int lane) {
+  const uint4* row =
+      reinterpret_cast<const uint4*>(q + (b * kQoHeads + h0 + (lane & 7)) * kHeadDim + 32 * (lane >> 3));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = __ldg(row + i);
+    qf[4 * i] = v.x;
+    qf[4 * i + 1] = v.y;
+    qf[4 * i + 2] = v.z;
+    qf[4 * i + 3] = v.w;
+  }
+}
+
+__device__ __forceinline__ void q_to_cc(CcState& cs, const uint32_t (&qf)[16]) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    cs.q[2 * k] = bf16_lo(qf[k]);
+    cs.q[2 * k + 1] = bf16_hi(qf[k]);
+  }
+}
+
+// k_rows / v_rows: shared address of token 0's K / V head row (pitch `pitch`).
+__device__ __forceinline__ void attend_subtile_cc(CcState& cs, uint32_t k_rows, uint32_t v_rows, int pitch,
+                                                  unsigned valid, float scale_log2, int lane) {
+  const int g = lane >> 3;
+  float s[16];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    uint32_t x[16];
+    const uint32_t a = k_rows + t * pitch + 64 * g;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ld_shared_u4(a + 16 * i, x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+    float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;  // four chains
+#pragma unroll
+    for (int k = 0; k < 16; k += 2) {
+      d0 = fmaf(cs.q[2 * k], bf16_lo(x[k]), d0);
+      d1 = fmaf(cs.q[2 * k + 1], bf16_hi(x[k]), d1);
+      d2 = fmaf(cs.q[2 * k + 2], bf16_lo(x[k + 1]), d2);
+      d3 = fmaf(cs.q[2 * k + 3], bf16_hi(x[k + 1]), d3);
+    }
+    s[t] = (d0 + d1) + (d2 + d3);
+  }
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    s[t] += __shfl_xor_sync(0xffffffffu, s[t], 8);
+    s[t] += __shfl_xor_sync(0xffffffffu, s[t], 16);
+    s[t] = ((valid >> t) & 1u) ? s[t] * scale_log2 : -INFINITY;
+  }
+  float mx = s[0];
+#pragma unroll
+  for (int t = 1; t < 16; ++t) mx = fmaxf(mx, s[t]);
+  const float mn = fmaxf(cs.m, mx);
+  const float sh = mn == -INFINITY ? 0.f : mn;  // nothing valid yet: 2^-inf = 0, not NaN
+  const float alpha = ex2(cs.m - sh);
+  cs.m = mn;
+  float psum = 0.f;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    s[t] = ex2(s[t] - sh);
+    psum += s[t];
+  }
+  cs.l = cs.l * alpha + psum;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) cs.acc[j] *= alpha;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    uint32_t x[16];
+    const uint32_t a = v_rows + t * pitch + 64 * g;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ld_shared_u4(a + 16 * i, x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      cs.acc[2 * k] = fmaf(s[t], bf16_lo(x[k]), cs.acc[2 * k]);
+      cs.acc[2 * k + 1] = fmaf(s[t], bf16_hi(x[k]), cs.acc[2 * k + 1]);
+    }
+  }
+}
+
 // FP8-cache path: turn bf16 Q fragments into f16 ones scaled by a power of two
 // chosen so that the group's largest |q| lands in [2^13, 2^14) (no f16
 // overflow; exact for every component down to 2^-27 of that maximum).
@@ -619,6 +722,32 @@ __device__ __forceinline__ bool finish_piece(const HeadState& st, bool final_pie
   }
   if (r == 0) *reinterpret_cast<float2*>(p.part_lse + (sid * NG + w) * kGroup + 2 * c) = make_float2(lse0, lse1);
   return si.S <= p.fuse_max_splits;  // else the merge kernel combines this sequence
+}
+
+// finish_piece for the CUDA-core sub-tile (same outputs and partial layout).
+template <int NG>
+__device__ __forceinline__ bool finish_piece_cc(const CcState& cs, bool final_piece, int64_t b, int h0, int64_t sid,
+                                                int w, const SplitInfo& si, const DecodeParams& p, int lane) {
+  const int h = lane & 7, g = lane >> 3;
+  const float inv = cs.l > 0.f ? 1.f / cs.l : 0.f;
+  const float lse_v = cs.l > 0.f ? cs.m + log2f(cs.l) : -INFINITY;
+  if (final_piece) {
+    uint4* ob = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (b * kQoHeads + h0 + h) * kHeadDim +
+                                         32 * g);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      ob[i] = make_uint4(pack_bf16(cs.acc[8 * i] * inv, cs.acc[8 * i + 1] * inv),
+                         pack_bf16(cs.acc[8 * i + 2] * inv, cs.acc[8 * i + 3] * inv),
+                         pack_bf16(cs.acc[8 * i + 4] * inv, cs.acc[8 * i + 5] * inv),
+                         pack_bf16(cs.acc[8 * i + 6] * inv, cs.acc[8 * i + 7] * inv));
+    if (g == 0 && p.lse != nullptr) p.lse[b * kQoHeads + h0 + h] = lse_v;
+    return false;
+  }
+  float* po = p.part_o + (sid * NG + w) * (kHeadDim * kGroup);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) po[(32 * g + j) * kGroup + h] = cs.acc[j] * inv;
+  if (g == 0) p.part_lse[(sid * NG + w) * kGroup + h] = lse_v;
+  return si.S <= p.fuse_max_splits;
 }
 
 // Split record of decode CTA `cta`: how the sequence holding the last unit of

@@ -435,8 +435,10 @@ __device__ __noinline__ void install_call_counters(const DecodeParams& p, int w,
 // slot of -1 (an invalid column) is masked out of the softmax.
 // F8: the K/V caches are FP8 rows (kGlobalRowBytes per token): e4m3 values of
 // the 4 KV heads, then their fp32 scales.
-template <int NG, int D, bool SP, bool F8 = false>
-__global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kernel(const DecodeParams p) {
+// CC: the contractions on the CUDA cores (attend_subtile_cc) instead of
+// mma.sync, a variant kept for comparing the two.
+template <int NG, int D, bool SP, bool F8 = false, bool CC = false>
+__global__ void __launch_bounds__(NG * 32, (F8 || CC) ? 3 : 16 / NG) gqa_decode_lsu_kernel(const DecodeParams p) {
   using C = LsuCfg<NG, D, F8>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int w = threadIdx.x >> 5;  // KV head within the head group
@@ -687,7 +689,10 @@ __global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kern
       if (flags & F_QLOAD) {
         const int h0 = (tl.hg * NG + w) * kGroup;
         if (!qn_busy) {
-          load_q_frags<F8>(qn, qg, tl.b, h0, lane);
+          if constexpr (CC)
+            load_q_cc(qn, qg, tl.b, h0, lane);
+          else
+            load_q_frags<F8>(qn, qg, tl.b, h0, lane);
           qn_busy = true;
           flags |= F_QREG;
         } else if (lane < 16) {
@@ -713,6 +718,8 @@ __global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kern
   // ------------------------------------------------------------ compute
   HeadState st;
   st.reset();
+  CcState cs;  // the CUDA-core variant's state (unused otherwise)
+  cs.reset();
 #pragma unroll
   for (int i = 0; i < 16; ++i) st.qf[i] = 0;
   // per-lane ldmatrix row addresses within a stage. F8: K row (lane >> 2) at
@@ -753,13 +760,23 @@ __global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kern
 #pragma unroll
         for (int i = 0; i < 16; ++i) st.qf[i] = qn[i];
         qn_busy = false;
+      } else if constexpr (CC) {
+        load_q_cc(st.qf, qg, hb, h0, lane);
       } else {
         load_q_frags<F8>(st.qf, qg, hb, h0, lane);
       }
-      st.reset();
+      if constexpr (CC) {
+        q_to_cc(cs, st.qf);
+        cs.reset();
+      } else {
+        st.reset();
+      }
       if constexpr (F8) st.qsc = q_frags_to_f16(st.qf);
     }
-    if constexpr (F8) {
+    if constexpr (CC) {
+      attend_subtile_cc(cs, sb + C::kKOff, sb + C::kVOff, C::kRowPitch, static_cast<unsigned>(tok_mask), p.scale_log2,
+                        lane);
+    } else if constexpr (F8) {
       const int r = lane >> 2;
       const float sk_lo = ld_shared_f32(sb + C::kSkOff + r * 4), sk_hi = ld_shared_f32(sb + C::kSkOff + (r + 8) * 4);
       const float sv_lo = ld_shared_f32(sb + C::kSvOff + r * 4), sv_hi = ld_shared_f32(sb + C::kSvOff + (r + 8) * 4);
@@ -769,8 +786,14 @@ __global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kern
       attend_subtile(st, sb + k_lane, sb + v_lane, static_cast<unsigned>(tok_mask), p.scale_log2, lane);
     }
     if (flags & F_END) {
-      if (finish_piece<NG, F8>(st, (flags & F_FINAL) != 0, hb, h0, slot_id(tile_cta, (flags & F_SLOT1) ? 1 : 0),
-                               w, si, p, lane, F8 ? st.cv : 1.f)) {
+      bool owes;
+      if constexpr (CC)
+        owes = finish_piece_cc<NG>(cs, (flags & F_FINAL) != 0, hb, h0, slot_id(tile_cta, (flags & F_SLOT1) ? 1 : 0), w,
+                                   si, p, lane);
+      else
+        owes = finish_piece<NG, F8>(st, (flags & F_FINAL) != 0, hb, h0, slot_id(tile_cta, (flags & F_SLOT1) ? 1 : 0),
+                                    w, si, p, lane, F8 ? st.cv : 1.f);
+      if (owes) {
         pend[n_pend < 2 ? n_pend : 1] = {si, hb, h0};
         n_pend = min(n_pend + 1, 2);
       }
@@ -818,15 +841,15 @@ __global__ void __launch_bounds__(NG * 32, F8 ? 3 : 16 / NG) gqa_decode_lsu_kern
 // launch: kLaunchPlain, kLaunchPdl (a programmatic dependent of the kernel
 // before it on the stream) or kLaunchCooperative (the one-wave mode: every CTA
 // resident at once, which the in-kernel merge's waits rely on).
-template <int NG, int D, bool SP, bool F8 = false>
+template <int NG, int D, bool SP, bool F8 = false, bool CC = false>
 static cudaError_t launch_lsu(const DecodeParams& p, int num_ctas, cudaStream_t stream, int launch) {
   using C = LsuCfg<NG, D, F8>;
   static std::atomic<int> configured[kMaxDevices];
   const cudaError_t e = set_smem_limit_once(
-      configured, reinterpret_cast<const void*>(gqa_decode_lsu_kernel<NG, D, SP, F8>), C::kSmemBytes);
+      configured, reinterpret_cast<const void*>(gqa_decode_lsu_kernel<NG, D, SP, F8, CC>), C::kSmemBytes);
   if (e != cudaSuccess) return e;
   if (launch == kLaunchPlain) {
-    gqa_decode_lsu_kernel<NG, D, SP, F8><<<num_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
+    gqa_decode_lsu_kernel<NG, D, SP, F8, CC><<<num_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -844,7 +867,7 @@ static cudaError_t launch_lsu(const DecodeParams& p, int num_ctas, cudaStream_t 
   }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gqa_decode_lsu_kernel<NG, D, SP, F8>, p);
+  return cudaLaunchKernelEx(&cfg, gqa_decode_lsu_kernel<NG, D, SP, F8, CC>, p);
 }
 
 // CTAs of a variant that the current device holds at once (0 if it cannot be
@@ -912,6 +935,14 @@ cudaError_t launch_decode_lsu_f8(int stages, const DecodeParams& p, int num_ctas
   GQA_LSU_F8_VARIANTS(X)
 #undef X
   return cudaErrorInvalidValue;
+}
+
+// The CUDA-core comparison variant: 4 KV heads per CTA, 2 stages (the
+// default's shape), static grid.
+int lsu_cc_smem_bytes() { return LsuCfg<4, 2>::kSmemBytes; }
+
+cudaError_t launch_decode_lsu_cc(const DecodeParams& p, int num_ctas, cudaStream_t stream) {
+  return launch_lsu<4, 2, false, false, true>(p, num_ctas, stream, kLaunchPlain);
 }
 
 int decode_coresident_ctas(const KernelChoice& k, bool sparse) {

@@ -142,6 +142,9 @@ VARIANTS = {
     "lsu_few_ctas_tier2": (7, 0, 4, 16, 2, 0, 0, 13, 400, 4),
     "lsu_tier2_unfused": (40, 8, 4, 16, 2, 0, -1, 0, 600, 8),
     "tma_tier2": (40, 8, 4, 16, 5, 1, 0, 0, 300, 16),
+    # the contractions on the CUDA cores (comparison variant)
+    "cuda_cores": (0, 0, 4, 16, 2, 3),
+    "cuda_cores_split": (40, 8, 4, 16, 2, 3, 0, 0, 300, 16),
 }
 
 
@@ -304,6 +307,16 @@ def one_wave():
     assert _lib.gqa_paged_decode_set_merge_mode(_lib.MERGE_ONE_WAVE) == 0
     yield
     assert _lib.gqa_paged_decode_set_merge_mode(_lib.MERGE_KERNEL) == 0
+
+
+@pytest.mark.parametrize("name", ["mid", "skewed"])
+def test_cuda_core_variant_full_workload(tuning, name):
+    """The CUDA-core comparison variant on full workloads, every sequence."""
+    tuning(0, 0, 4, 16, 2, 3)
+    w = wl.make_config(name)
+    out, lse = gpu_run(w)
+    ref = gqa_paged_decode_oracle_parallel(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices, w.sm_scale)
+    check(w, out, lse, ref=ref)
 
 
 @pytest.mark.parametrize("tier2", [(0, 0, 0), (-1, 0, 0), (4000, 900, 1), (912, 500, 8), (6840, 100, 0),
