@@ -467,6 +467,8 @@ def bench_mla(device, steps, warmup, peak, wide: bool = False):
 # wall time on the host's cores.
 ORACLE_TARGET_CPU_S = 12.0
 ORACLE_MAX_ROUNDS = 20
+# rounds of the oracle per workload-table row (median reported)
+TABLE_ORACLE_ROUNDS = 3
 
 
 def oracle_rounds(w, rounds=None, target_cpu_s=ORACLE_TARGET_CPU_S):
@@ -665,6 +667,11 @@ def main():
                            "batch": ww.batch, "total_tokens": ww.total_tokens,
                            "counted_bytes": b, "us_per_batch_l2_warm": statistics.median(rr["warm_ms"]) * 1e3}
             del rr
+            if rank == 0 and not args.no_cpu_baseline and name != args.workload:
+                # the oracle over the same batch on the host's cores (the headline
+                # workload's figure comes from the CPU-baseline leg below)
+                _, _, times, cores = oracle_rounds(ww, rounds=TABLE_ORACLE_ROUNDS)
+                table[name].update({"oracle_s_per_batch": statistics.median(times), "oracle_cores": cores})
             if ww is not w:
                 del ww
 
@@ -680,6 +687,9 @@ def main():
     cpu, parity = None, None
     if rank == 0 and not args.no_cpu_baseline:
         cpu, parity = cpu_baseline(w, run_out, run_lse)
+        if args.workload in table:
+            table[args.workload].update({"oracle_s_per_batch": statistics.median(cpu["rounds_s"]),
+                                         "oracle_cores": cpu["cores"]})
 
     if rank != 0:
         if world > 1:
