@@ -357,8 +357,9 @@ def bench_fp8(w, g, device, steps, warmup, peak):
     """Decode of workload w over an FP8 copy of its cache (528-byte rows: 4 KV
     heads x 128 e4m3 codes + 4 fp32 scales, quantized on the device from the
     bf16 cache already in HBM, outside the timed region). Counted bytes: 1056 B
-    per token (K and V rows) + 16,512 B of q, O and LSE per sequence. Times the
-    default ring depth and the other two compiled ones."""
+    per token (K and V rows) + 16,512 B of q, O and LSE per sequence. Times every
+    compiled FP8 variant (16-token stages in rings of 2, 3 and 4; 32-token stages in
+    a ring of 2) and the default."""
     k8 = wl.quantize_fp8_rows(g.k_cache)
     v8 = wl.quantize_fp8_rows(g.v_cache)
     out = torch.empty_like(g.q)
@@ -367,18 +368,22 @@ def bench_fp8(w, g, device, steps, warmup, peak):
     flush = L2Flush(device)
     b = 1056 * w.total_tokens + 16512 * w.batch
     res = {"workload": w.name, "counted_bytes": b, "bytes_vs_bf16": b / counted_bytes(w.lens)}
-    for stages in (2, 3, 4):
-        _lib.gqa_paged_decode_set_tuning(0, 0, 4, 16, stages, 0)
+    variants = [("stages_2", (0, 0, 4, 16, 2, _lib.GATHER_LSU_F8)), ("stages_3", (0, 0, 4, 16, 3, _lib.GATHER_LSU_F8)),
+                ("stages_4", (0, 0, 4, 16, 4, _lib.GATHER_LSU_F8)), ("stage32", (0, 0, 4, 32, 2, _lib.GATHER_LSU_F8)),
+                ("default", (0, 0, 0, 0, 0, 0))]
+    for key, tuning in variants:
+        if _lib.gqa_paged_decode_set_tuning(*tuning) != 0:
+            raise RuntimeError(f"FP8 tuning {tuning} rejected")
 
         def call():
             _lib.run_fp8(g.q, k8, v8, g.kv_indptr, g.kv_indices, w.sm_scale, out=out, lse=lse, stream=stream)
         for _ in range(warmup):
             call()
         ms = statistics.median(time_steps(call, steps, stream, flush))
-        res[f"stages_{stages}"] = {"us_per_batch": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9,
-                                   "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
+        res[key] = {"us_per_batch": ms * 1e3, "gbs": b / (ms * 1e-3) / 1e9,
+                    "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
     _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0)
-    res.update(res["stages_2"])  # the default depth
+    res.update(res["default"])
     del k8, v8, out, lse, flush
     return res
 

@@ -110,7 +110,7 @@ def gqa_paged_decode_strerror(code: int) -> str:
 strerror = gqa_paged_decode_strerror
 
 
-GATHER_LSU, GATHER_TMA, GATHER_LSU_CUDA_CORES = 0, 1, 3
+GATHER_LSU, GATHER_TMA, GATHER_LSU_F8, GATHER_LSU_CUDA_CORES = 0, 1, 2, 3
 
 
 def gqa_paged_decode_set_tuning(num_ctas=0, min_units_per_cta=0, heads_per_cta=0, tile=0, stages=0,

@@ -32,6 +32,8 @@ constexpr int kDefaultTier2PerTier1 = 2;
 constexpr int kDefaultTier2Permille = 100;
 constexpr int kDefaultTier2MinUnits = 64;
 constexpr int kMaxTier2Ctas = 1 << 16;
+// Tokens per pipeline stage of the FP8-cache decode with a 2-deep ring.
+constexpr int kDefaultF8Tile = 16;
 constexpr int kSmemPerSm = 228 * 1024;
 constexpr int kSmemReservedPerCta = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -223,8 +225,13 @@ int run(const void* q, const void* k, const void* v, const int32_t* indptr, cons
     if (sj != nullptr) tune.kernel = KernelChoice{gqa::kGatherLsu, 4, 16, 2};  // the one sparse variant
     if (fp8) {  // FP8 caches: the FP8 variant; a cp.async tuning with 4 heads per CTA picks its depth
       const KernelChoice& k = tune.kernel;
-      const bool pick = k.gather == gqa::kGatherLsu && k.heads_per_cta == 4 && k.stages >= 2 && k.stages <= 4;
-      tune.kernel = KernelChoice{gqa::kGatherLsuF8, 4, 16, pick ? k.stages : 2};
+      if (k.gather != gqa::kGatherLsuF8) {
+        const bool pick = k.gather == gqa::kGatherLsu && k.heads_per_cta == 4 && k.stages >= 2 && k.stages <= 4;
+        const int stages = pick ? k.stages : 2;
+        tune.kernel = KernelChoice{gqa::kGatherLsuF8, 4, stages == 2 ? kDefaultF8Tile : 16, stages};
+      }
+    } else if (tune.kernel.gather == gqa::kGatherLsuF8) {  // an FP8 tuning: bf16 caches take the default
+      tune.kernel = KernelChoice{gqa::kGatherLsu, 4, 16, 2};
     }
     ev0 = g_ev_start;
     ev1 = g_ev_stop;
@@ -465,6 +472,9 @@ int gqa_paged_decode_set_tuning(int num_ctas, int min_units_per_cta, int heads_p
     t.kernel.stages = stages > 0 ? stages : (t.kernel.tile == 32 ? 3 : (t.kernel.heads_per_cta == 4 ? 5 : 4));
   } else if (gather == gqa::kGatherLsuCc) {
     t.kernel.tile = tile > 0 ? tile : 16;
+    t.kernel.stages = stages > 0 ? stages : 2;
+  } else if (gather == gqa::kGatherLsuF8) {
+    t.kernel.tile = tile > 0 ? tile : kDefaultF8Tile;
     t.kernel.stages = stages > 0 ? stages : 2;
   } else {
     return GQA_ERR_INVALID_ARGUMENT;

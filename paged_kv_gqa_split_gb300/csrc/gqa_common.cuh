@@ -204,6 +204,9 @@ __device__ __forceinline__ void attend_subtile(HeadState& st, uint32_t k_addr, u
   }
 }
 
+// 1 / x for x = 2^k with a normal reciprocal (exact: the exponent is negated).
+__device__ __forceinline__ float pow2_recip(float x) { return __uint_as_float((254u << 23) - __float_as_uint(x)); }
+
 // FP8-cache form of attend_subtile, straight from the staged e4m3 rows (no
 // conversion pass through shared memory; e4m3 -> f16 is exact):
 // - K (rows = tokens at a 192-byte pitch): lane (r, c) reads 16 bytes of rows
@@ -263,20 +266,22 @@ __device__ __forceinline__ void attend_subtile_f8(HeadState& st, uint32_t k_addr
   st.m0 = mn0;
   st.m1 = mn1;
   const float cv_new = fmaxf(st.cv, vm > 0.f ? pow2_ceil(vm) : 0.f);
-  const float cr = cv_new > 0.f ? st.cv / cv_new : 1.f;  // exact: both are powers of two (or st.cv = 0)
-  const float iv = cv_new > 0.f ? 1.f / cv_new : 0.f;
+  const float iv = cv_new > 0.f ? pow2_recip(cv_new) : 0.f;
+  const float cr = cv_new > 0.f ? st.cv * iv : 1.f;  // exact: powers of two (or st.cv = 0)
   st.cv = cv_new;
   const float p0 = ex2(s[0] - sh0), p1 = ex2(s[1] - sh1);  // token r
   const float p2 = ex2(s[2] - sh0), p3 = ex2(s[3] - sh1);  // token r + 8
   st.l0 = st.l0 * a0 + (p0 + p2);
   st.l1 = st.l1 * a1 + (p1 + p3);
   const float b_a0 = a0 * cr, b_a1 = a1 * cr;
+  if (__any_sync(0xffffffffu, b_a0 != 1.f || b_a1 != 1.f)) {  // skipped while no max and no V bound moved
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    st.acc[mt][0] *= b_a0;
-    st.acc[mt][1] *= b_a1;
-    st.acc[mt][2] *= b_a0;
-    st.acc[mt][3] *= b_a1;
+    for (int mt = 0; mt < 8; ++mt) {
+      st.acc[mt][0] *= b_a0;
+      st.acc[mt][1] *= b_a1;
+      st.acc[mt][2] *= b_a0;
+      st.acc[mt][3] *= b_a1;
+    }
   }
   const float w_lo = sv_lo * iv, w_hi = sv_hi * iv;
   const uint32_t b0 = movmatrix_trans(pack_f16(p0 * w_lo, p1 * w_lo));
@@ -291,6 +296,112 @@ __device__ __forceinline__ void attend_subtile_f8(HeadState& st, uint32_t k_addr
     mma_f16_16816(st.acc[2 * mp + 1], cvt_e4m3x2_f16x2(__byte_perm(t2, 0, 0x0020)),
                   cvt_e4m3x2_f16x2(__byte_perm(t2, 0, 0x0031)), cvt_e4m3x2_f16x2(__byte_perm(t3, 0, 0x0020)),
                   cvt_e4m3x2_f16x2(__byte_perm(t3, 0, 0x0031)), b0, b1);
+  }
+}
+
+// attend_subtile_f8 over a 32-token stage: two 16-token halves (rows 0-15 and
+// 16-31 of the staged K and V) share one softmax step, so the max reduction,
+// the V-scale bound and the rescale of acc happen once per 32 tokens, and the
+// two halves' score contractions run as independent mma chains. sk[i] / sv[i]
+// are the scales of this lane's tokens r + 8 i (i = 0..3) for this KV head;
+// valid holds one bit per token. The fragment layouts are those of
+// attend_subtile_f8, half by half.
+__device__ __forceinline__ void attend_tile32_f8(HeadState& st, uint32_t k_addr, uint32_t v_addr, unsigned valid,
+                                                 float scale_log2, const float (&sk)[4], const float (&sv)[4], int lane,
+                                                 int k_pitch, int v_pitch) {
+  const int r = lane >> 2;
+  float s[2][4];
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[hf][i] = 0.f;
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb) {
+    uint32_t x[2][4], y[2][4];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const uint32_t a = k_addr + hf * 16 * k_pitch + kb * 64;
+      ld_shared_u4(a, x[hf][0], x[hf][1], x[hf][2], x[hf][3]);                // row 16 hf + r
+      ld_shared_u4(a + 8 * k_pitch, y[hf][0], y[hf][1], y[hf][2], y[hf][3]);  // row 16 hf + r + 8
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int t = 4 * kb + j;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+        mma_f16_16816(s[hf], cvt_e4m3x2_f16x2(x[hf][j]), cvt_e4m3x2_f16x2(y[hf][j]),
+                      cvt_e4m3x2_f16x2(x[hf][j] >> 16), cvt_e4m3x2_f16x2(y[hf][j] >> 16), st.qf[2 * t],
+                      st.qf[2 * t + 1]);
+    }
+  }
+  float mx0 = -INFINITY, mx1 = -INFINITY, vm = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // token r + 8 i: half i / 2, accumulator pair 2 (i % 2)
+    const bool v = (valid >> (r + 8 * i)) & 1u;
+    const float c = scale_log2 * st.qsc * sk[i];
+    float& e0 = s[i >> 1][2 * (i & 1)];
+    float& e1 = s[i >> 1][2 * (i & 1) + 1];
+    e0 = v ? e0 * c : -INFINITY;
+    e1 = v ? e1 * c : -INFINITY;
+    mx0 = fmaxf(mx0, e0);
+    mx1 = fmaxf(mx1, e1);
+    vm = fmaxf(vm, v ? fabsf(sv[i]) : 0.f);
+  }
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+  }
+  const float mn0 = fmaxf(st.m0, mx0);
+  const float mn1 = fmaxf(st.m1, mx1);
+  const float sh0 = mn0 == -INFINITY ? 0.f : mn0;
+  const float sh1 = mn1 == -INFINITY ? 0.f : mn1;
+  const float a0 = ex2(st.m0 - sh0);
+  const float a1 = ex2(st.m1 - sh1);
+  st.m0 = mn0;
+  st.m1 = mn1;
+  const float cv_new = fmaxf(st.cv, vm > 0.f ? pow2_ceil(vm) : 0.f);
+  const float iv = cv_new > 0.f ? pow2_recip(cv_new) : 0.f;
+  const float cr = cv_new > 0.f ? st.cv * iv : 1.f;  // exact: powers of two (or st.cv = 0)
+  st.cv = cv_new;
+  float pr[2][4];
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    pr[hf][0] = ex2(s[hf][0] - sh0);
+    pr[hf][1] = ex2(s[hf][1] - sh1);
+    pr[hf][2] = ex2(s[hf][2] - sh0);
+    pr[hf][3] = ex2(s[hf][3] - sh1);
+  }
+  st.l0 = st.l0 * a0 + ((pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]));
+  st.l1 = st.l1 * a1 + ((pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]));
+  const float b_a0 = a0 * cr, b_a1 = a1 * cr;
+  if (__any_sync(0xffffffffu, b_a0 != 1.f || b_a1 != 1.f)) {  // skipped while no max and no V bound moved
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      st.acc[mt][0] *= b_a0;
+      st.acc[mt][1] *= b_a1;
+      st.acc[mt][2] *= b_a0;
+      st.acc[mt][3] *= b_a1;
+    }
+  }
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    const float w_lo = sv[2 * hf] * iv, w_hi = sv[2 * hf + 1] * iv;
+    const uint32_t b0 = movmatrix_trans(pack_f16(pr[hf][0] * w_lo, pr[hf][1] * w_lo));
+    const uint32_t b1 = movmatrix_trans(pack_f16(pr[hf][2] * w_hi, pr[hf][3] * w_hi));
+    const uint32_t va = v_addr + hf * 16 * v_pitch;
+#pragma unroll
+    for (int mp = 0; mp < 4; ++mp) {  // m-tiles 2 mp and 2 mp + 1
+      uint32_t t0, t1, t2, t3;
+      ldsm_x4_trans(va + mp * 32, t0, t1, t2, t3);
+      mma_f16_16816(st.acc[2 * mp], cvt_e4m3x2_f16x2(__byte_perm(t0, 0, 0x0020)),
+                    cvt_e4m3x2_f16x2(__byte_perm(t0, 0, 0x0031)), cvt_e4m3x2_f16x2(__byte_perm(t1, 0, 0x0020)),
+                    cvt_e4m3x2_f16x2(__byte_perm(t1, 0, 0x0031)), b0, b1);
+      mma_f16_16816(st.acc[2 * mp + 1], cvt_e4m3x2_f16x2(__byte_perm(t2, 0, 0x0020)),
+                    cvt_e4m3x2_f16x2(__byte_perm(t2, 0, 0x0031)), cvt_e4m3x2_f16x2(__byte_perm(t3, 0, 0x0020)),
+                    cvt_e4m3x2_f16x2(__byte_perm(t3, 0, 0x0031)), b0, b1);
+    }
   }
 }
 

@@ -55,11 +55,12 @@ namespace gqa {
 // (F8 = true): each stage holds the tile's 128-byte e4m3 head rows of K (at a
 // 192-byte pitch: the 128-bit row reads of attend_subtile_f8 then hit 8
 // distinct bank groups) and of V (at a 144-byte pitch, for ldmatrix), plus
-// their per-token scales.
-template <int NG, int D, bool F8 = false>
+// their per-token scales. TT: tokens per stage (16, one mma sub-tile; the FP8
+// cache also has a 32-token form).
+template <int NG, int D, bool F8 = false, int TT = 16>
 struct LsuCfg {
   static constexpr int kHG = kKvHeads / NG;           // head groups on the unit line
-  static constexpr int kTile = 16;                    // tokens per stage (one mma sub-tile)
+  static constexpr int kTile = TT;                    // tokens per stage
   static constexpr int kRowPitch = kHeadDim * 2 + 16; // 256 B head row + 16 B: ldmatrix rows hit all banks
   static constexpr int kRowBytes8 = kHeadDim;         // e4m3 head row
   // global row of one token (all 4 KV heads): 1 KB of bf16, or 512 B of e4m3 + 4 fp32 scales
@@ -86,6 +87,7 @@ struct LsuCfg {
   static_assert(D >= 2, "at least double buffering");
   static_assert(kStageBytes % 16 == 0 && kWarpBytes % 16 == 0, "16-byte aligned stages");
   static_assert(kSmemBytes <= 227 * 1024, "ring exceeds shared memory");
+  static_assert(TT == 16 || (F8 && TT == 32), "32-token stages exist for the FP8 cache only");
 };
 
 // What the walker needs of the plan when a piece starts (where the piece's
@@ -437,9 +439,10 @@ __device__ __noinline__ void install_call_counters(const DecodeParams& p, int w,
 // the 4 KV heads, then their fp32 scales.
 // CC: the contractions on the CUDA cores (attend_subtile_cc) instead of
 // mma.sync, a variant kept for comparing the two.
-template <int NG, int D, bool SP, bool F8 = false, bool CC = false>
-__global__ void __launch_bounds__(NG * 32, (F8 || CC) ? 3 : 16 / NG) gqa_decode_lsu_kernel(const DecodeParams p) {
-  using C = LsuCfg<NG, D, F8>;
+template <int NG, int D, bool SP, bool F8 = false, bool CC = false, int TT = 16>
+__global__ void __launch_bounds__(NG * 32, (F8 || CC) ? (TT == 32 ? 2 : 3) : 16 / NG)
+    gqa_decode_lsu_kernel(const DecodeParams p) {
+  using C = LsuCfg<NG, D, F8, TT>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int w = threadIdx.x >> 5;  // KV head within the head group
   const int lane = threadIdx.x & 31;
@@ -629,11 +632,11 @@ __global__ void __launch_bounds__(NG * 32, (F8 || CC) ? 3 : 16 / NG) gqa_decode_
       const int64_t hoff = static_cast<int64_t>(tl.hg * NG + w) * (F8 ? kHeadDim : kHeadDim * 2);
       const int pc = lane & 15;  // 16-byte column of the 256-byte head row
       // tokens that enter the softmax: the first cnt, less (sparse mode) masked columns
-      unsigned mask = tl.cnt >= 16 ? 0xffffu : ((1u << tl.cnt) - 1u);
+      unsigned mask = tl.cnt >= 32 ? 0xffffffffu : ((1u << tl.cnt) - 1u);
       if constexpr (F8) {
-        // 16 tokens x 8 16-byte chunks of the 128-byte e4m3 head row, for K and V
+        // kTile tokens x 8 16-byte chunks of the 128-byte e4m3 head row, for K and V
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < C::kTile / 4; ++i) {
           const int tok = 4 * i + (lane >> 3), ch = lane & 7;
           bool valid = tok < tl.cnt;
           int pg = valid ? ids[(tl.tt + tok) & (C::kIdsRing - 1)] : 0;
@@ -648,8 +651,8 @@ __global__ void __launch_bounds__(NG * 32, (F8 || CC) ? 3 : 16 / NG) gqa_decode_
           cp_async_16(sb + C::kKOff + tok * C::kK8Pitch + ch * 16, kc + off, nbytes);
           cp_async_16(sb + C::kVOff + tok * C::kV8Pitch + ch * 16, vc + off, nbytes);
         }
-        {  // the per-token scales of this KV head: lanes 0-15 K, 16-31 V
-          const int tok = lane & 15;
+        {  // the per-token scales of this KV head: 16 tokens: lanes 0-15 K, 16-31 V; 32: K and V of token lane
+          const int tok = C::kTile == 16 ? (lane & 15) : lane;
           bool valid = tok < tl.cnt;
           int pg = valid ? ids[(tl.tt + tok) & (C::kIdsRing - 1)] : 0;
           if (valid && p.num_pages_check > 0 &&
@@ -659,8 +662,13 @@ __global__ void __launch_bounds__(NG * 32, (F8 || CC) ? 3 : 16 / NG) gqa_decode_
           }
           const int64_t off = static_cast<int64_t>(pg) * C::kGlobalRowBytes + kKvHeads * kHeadDim +
                               (tl.hg * NG + w) * 4;
-          cp_async_4(sb + (lane < 16 ? C::kSkOff : C::kSvOff) + tok * 4, (lane < 16 ? kc : vc) + off,
-                     valid ? 4u : 0u);
+          if constexpr (C::kTile == 16) {
+            cp_async_4(sb + (lane < 16 ? C::kSkOff : C::kSvOff) + tok * 4, (lane < 16 ? kc : vc) + off,
+                       valid ? 4u : 0u);
+          } else {
+            cp_async_4(sb + C::kSkOff + tok * 4, kc + off, valid ? 4u : 0u);
+            cp_async_4(sb + C::kSvOff + tok * 4, vc + off, valid ? 4u : 0u);
+          }
         }
       }
 #pragma unroll
@@ -776,6 +784,16 @@ __global__ void __launch_bounds__(NG * 32, (F8 || CC) ? 3 : 16 / NG) gqa_decode_
     if constexpr (CC) {
       attend_subtile_cc(cs, sb + C::kKOff, sb + C::kVOff, C::kRowPitch, static_cast<unsigned>(tok_mask), p.scale_log2,
                         lane);
+    } else if constexpr (F8 && C::kTile == 32) {
+      const int r = lane >> 2;
+      float sk[4], sv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        sk[i] = ld_shared_f32(sb + C::kSkOff + (r + 8 * i) * 4);
+        sv[i] = ld_shared_f32(sb + C::kSvOff + (r + 8 * i) * 4);
+      }
+      attend_tile32_f8(st, sb + k_lane, sb + v_lane, static_cast<unsigned>(tok_mask), p.scale_log2, sk, sv, lane,
+                       C::kK8Pitch, C::kV8Pitch);
     } else if constexpr (F8) {
       const int r = lane >> 2;
       const float sk_lo = ld_shared_f32(sb + C::kSkOff + r * 4), sk_hi = ld_shared_f32(sb + C::kSkOff + (r + 8) * 4);
@@ -841,15 +859,15 @@ __global__ void __launch_bounds__(NG * 32, (F8 || CC) ? 3 : 16 / NG) gqa_decode_
 // launch: kLaunchPlain, kLaunchPdl (a programmatic dependent of the kernel
 // before it on the stream) or kLaunchCooperative (the one-wave mode: every CTA
 // resident at once, which the in-kernel merge's waits rely on).
-template <int NG, int D, bool SP, bool F8 = false, bool CC = false>
+template <int NG, int D, bool SP, bool F8 = false, bool CC = false, int TT = 16>
 static cudaError_t launch_lsu(const DecodeParams& p, int num_ctas, cudaStream_t stream, int launch) {
-  using C = LsuCfg<NG, D, F8>;
+  using C = LsuCfg<NG, D, F8, TT>;
   static std::atomic<int> configured[kMaxDevices];
   const cudaError_t e = set_smem_limit_once(
-      configured, reinterpret_cast<const void*>(gqa_decode_lsu_kernel<NG, D, SP, F8, CC>), C::kSmemBytes);
+      configured, reinterpret_cast<const void*>(gqa_decode_lsu_kernel<NG, D, SP, F8, CC, TT>), C::kSmemBytes);
   if (e != cudaSuccess) return e;
   if (launch == kLaunchPlain) {
-    gqa_decode_lsu_kernel<NG, D, SP, F8, CC><<<num_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
+    gqa_decode_lsu_kernel<NG, D, SP, F8, CC, TT><<<num_ctas, C::kThreads, C::kSmemBytes, stream>>>(p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -867,21 +885,21 @@ static cudaError_t launch_lsu(const DecodeParams& p, int num_ctas, cudaStream_t 
   }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gqa_decode_lsu_kernel<NG, D, SP, F8, CC>, p);
+  return cudaLaunchKernelEx(&cfg, gqa_decode_lsu_kernel<NG, D, SP, F8, CC, TT>, p);
 }
 
 // CTAs of a variant that the current device holds at once (0 if it cannot be
 // queried), cached per device.
-template <int NG, int D, bool SP, bool F8 = false>
+template <int NG, int D, bool SP, bool F8 = false, int TT = 16>
 static int coresident_lsu() {
-  using C = LsuCfg<NG, D, F8>;
+  using C = LsuCfg<NG, D, F8, TT>;
   static std::atomic<int> configured[kMaxDevices];
   static std::atomic<int> cached[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   const int c = cached[dev].load(std::memory_order_acquire);
   if (c > 0) return c;
-  const void* fn = reinterpret_cast<const void*>(gqa_decode_lsu_kernel<NG, D, SP, F8>);
+  const void* fn = reinterpret_cast<const void*>(gqa_decode_lsu_kernel<NG, D, SP, F8, false, TT>);
   if (set_smem_limit_once(configured, fn, C::kSmemBytes) != cudaSuccess) return 0;
   int per_sm = 0, sms = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, C::kThreads, C::kSmemBytes) != cudaSuccess ||
@@ -918,20 +936,22 @@ cudaError_t launch_decode_lsu_sparse(const DecodeParams& p, int num_ctas, cudaSt
   return launch_lsu<4, 2, true>(p, num_ctas, stream, launch);
 }
 
-// FP8-cache variants: 4 KV heads per CTA, 2, 3 or 4 stages.
-#define GQA_LSU_F8_VARIANTS(X) X(4, 2) X(4, 3) X(4, 4)
+// FP8-cache variants: 4 KV heads per CTA; 16-token stages in a ring of 2, 3
+// or 4, or 32-token stages in a ring of 2.
+#define GQA_LSU_F8_VARIANTS(X) X(4, 2, 16) X(4, 3, 16) X(4, 4, 16) X(4, 2, 32)
 
-int lsu_f8_smem_bytes(int stages) {
-#define X(NG, D) \
-  if (stages == D) return LsuCfg<NG, D, true>::kSmemBytes;
+int lsu_f8_smem_bytes(int stages, int tile) {
+#define X(NG, D, TT) \
+  if (stages == D && tile == TT) return LsuCfg<NG, D, true, TT>::kSmemBytes;
   GQA_LSU_F8_VARIANTS(X)
 #undef X
   return -1;
 }
 
-cudaError_t launch_decode_lsu_f8(int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream, int launch) {
-#define X(NG, D) \
-  if (stages == D) return launch_lsu<NG, D, false, true>(p, num_ctas, stream, launch);
+cudaError_t launch_decode_lsu_f8(int stages, int tile, const DecodeParams& p, int num_ctas, cudaStream_t stream,
+                                 int launch) {
+#define X(NG, D, TT) \
+  if (stages == D && tile == TT) return launch_lsu<NG, D, false, true, false, TT>(p, num_ctas, stream, launch);
   GQA_LSU_F8_VARIANTS(X)
 #undef X
   return cudaErrorInvalidValue;
@@ -948,8 +968,8 @@ cudaError_t launch_decode_lsu_cc(const DecodeParams& p, int num_ctas, cudaStream
 int decode_coresident_ctas(const KernelChoice& k, bool sparse) {
   if (sparse) return coresident_lsu<4, 2, true>();
   if (k.gather == kGatherLsuF8) {
-#define X(NG, D) \
-  if (k.stages == D) return coresident_lsu<NG, D, false, true>();
+#define X(NG, D, TT) \
+  if (k.stages == D && k.tile == TT) return coresident_lsu<NG, D, false, true, TT>();
     GQA_LSU_F8_VARIANTS(X)
 #undef X
     return 0;

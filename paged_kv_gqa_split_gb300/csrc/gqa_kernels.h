@@ -147,10 +147,11 @@ struct KernelChoice {
 };
 
 int lsu_smem_bytes(int ng, int stages);
-int lsu_f8_smem_bytes(int stages);
+int lsu_f8_smem_bytes(int stages, int tile);
 int lsu_cc_smem_bytes();
 cudaError_t launch_decode_lsu_cc(const DecodeParams& p, int num_ctas, cudaStream_t stream);
-cudaError_t launch_decode_lsu_f8(int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream, int launch);
+cudaError_t launch_decode_lsu_f8(int stages, int tile, const DecodeParams& p, int num_ctas, cudaStream_t stream,
+                                 int launch);
 cudaError_t launch_decode_lsu(int ng, int stages, const DecodeParams& p, int num_ctas, cudaStream_t stream,
                               int launch);
 // The selected-token variant (p.sparse_topk > 0): 4 KV heads per CTA, 2 stages.
@@ -169,7 +170,7 @@ cudaError_t launch_decode_tma(int ng, int tile, int stages, const DecodeParams& 
 inline int decode_smem_bytes(const KernelChoice& k) {
   if (k.gather == kGatherLsu) return k.tile == 16 ? lsu_smem_bytes(k.heads_per_cta, k.stages) : -1;
   if (k.gather == kGatherTma) return tma_smem_bytes(k.heads_per_cta, k.tile, k.stages);
-  if (k.gather == kGatherLsuF8) return k.heads_per_cta == 4 && k.tile == 16 ? lsu_f8_smem_bytes(k.stages) : -1;
+  if (k.gather == kGatherLsuF8) return k.heads_per_cta == 4 ? lsu_f8_smem_bytes(k.stages, k.tile) : -1;
   if (k.gather == kGatherLsuCc) return k.heads_per_cta == 4 && k.tile == 16 && k.stages == 2 ? lsu_cc_smem_bytes() : -1;
   return -1;
 }
@@ -177,8 +178,10 @@ inline int decode_smem_bytes(const KernelChoice& k) {
 // Warps a variant runs per CTA and the most CTAs per SM worth launching.
 inline int decode_max_ctas_per_sm(const KernelChoice& k) {
   // LSU: up to 16 gathering warps per SM; TMA: up to 4 consumer warps per SM; FP8 and the
-  // CUDA-core variant: 3 CTAs (their launch bounds leave 170 registers per thread).
-  if (k.gather == kGatherLsuF8 || k.gather == kGatherLsuCc) return 3;
+  // CUDA-core variant: 3 CTAs (their launch bounds leave 170 registers per thread); FP8 with
+  // 32-token stages: 2 (shared memory).
+  if (k.gather == kGatherLsuF8) return k.tile == 32 ? 2 : 3;
+  if (k.gather == kGatherLsuCc) return 3;
   return k.gather == kGatherLsu ? 16 / k.heads_per_cta : 4 / k.heads_per_cta;
 }
 
@@ -186,7 +189,7 @@ inline cudaError_t launch_decode(const KernelChoice& k, const DecodeParams& p, i
                                  int launch) {
   if (k.gather == kGatherLsu) return launch_decode_lsu(k.heads_per_cta, k.stages, p, num_ctas, stream, launch);
   if (k.gather == kGatherTma) return launch_decode_tma(k.heads_per_cta, k.tile, k.stages, p, num_ctas, stream);
-  if (k.gather == kGatherLsuF8) return launch_decode_lsu_f8(k.stages, p, num_ctas, stream, launch);
+  if (k.gather == kGatherLsuF8) return launch_decode_lsu_f8(k.stages, k.tile, p, num_ctas, stream, launch);
   if (k.gather == kGatherLsuCc) return launch_decode_lsu_cc(p, num_ctas, stream);
   return cudaErrorInvalidValue;
 }

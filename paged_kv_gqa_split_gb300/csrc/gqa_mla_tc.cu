@@ -377,18 +377,16 @@ __global__ void __launch_bounds__(TcCfg<R>::kThreads, 1)
       for (int u = 0; u < kVUnits; ++u) {
         int s;
         if (!take_unit(s)) return false;
-        if (lane == 0) {
-          // V^T block u: M = 128 dims over the unit's two regions (LBO), K = tokens in 8-row groups (SBO)
-          const uint64_t dv = tc_sdesc(base + s * kUnitBytes, kRegionBytes, 1024, kSwizzle128B);
+        // V^T block u: M = 128 dims over the unit's two regions (LBO), K = tokens in 8-row groups (SBO);
+        // the whole warp forms the (uniform) descriptors, one elected lane issues
+        const uint64_t dv = tc_sdesc(base + s * kUnitBytes, kRegionBytes, 1024, kSwizzle128B);
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            tc_mma_bf16(tmem + 2 * R + R * u, dv + ((kk * 2048) >> 4), dp + ((kk * 256) >> 4), idesc_o,
-                        (p_first && kk == 0) ? 0u : 1u);
-          tc_commit(bar(C::B_EMPTY + s));
-        }
-        __syncwarp();
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          tc_mma_bf16_warp(tmem + 2 * R + R * u, dv + ((kk * 2048) >> 4), dp + ((kk * 256) >> 4), idesc_o,
+                           (p_first && kk == 0) ? 0u : 1u);
+        tc_commit_warp(bar(C::B_EMPTY + s));
       }
-      if (lane == 0) tc_commit(bar(C::B_PVDONE + (pj & 1)));
+      tc_commit_warp(bar(C::B_PVDONE + (pj & 1)));
       __syncwarp();
       return true;
     };
@@ -413,25 +411,20 @@ __global__ void __launch_bounds__(TcCfg<R>::kThreads, 1)
           good = false;
           break;
         }
-        if (lane == 0) {
-          // K rows as A (tensor-copied data: the full barrier alone orders it before the MMA):
-          // M = 128 tokens (SBO 1024), K-major, 128-byte swizzle, 16 KB per region
-          const uint64_t dk = tc_sdesc(base + s * kUnitBytes, 16, 1024, kSwizzle128B);
-          const int nreg = u < 4 ? 2 : 1;
-          for (int g = 0; g < nreg; ++g)
+        // K rows as A (tensor-copied data: the full barrier alone orders it before the MMA):
+        // M = 128 tokens (SBO 1024), K-major, 128-byte swizzle, 16 KB per region
+        const uint64_t dk = tc_sdesc(base + s * kUnitBytes, 16, 1024, kSwizzle128B);
+        const int nreg = u < 4 ? 2 : 1;
+        for (int g = 0; g < nreg; ++g)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma_bf16(tmem + R * sb, dk + ((g * kRegionBytes + kk * 32) >> 4),
-                          dq + (((2 * u + g) * C::kQRegion + kk * 32) >> 4), idesc_s, (u | g | kk) ? 1u : 0u);
-          tc_commit(bar(C::B_EMPTY + s));
-        }
-        __syncwarp();
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16_warp(tmem + R * sb, dk + ((g * kRegionBytes + kk * 32) >> 4),
+                             dq + (((2 * u + g) * C::kQRegion + kk * 32) >> 4), idesc_s, (u | g | kk) ? 1u : 0u);
+        tc_commit_warp(bar(C::B_EMPTY + s));
       }
       if (!good) break;
-      if (lane == 0) {
-        tc_commit(bar(C::B_SFULL + sb));
-        if (tl.flags & F_END) tc_commit(bar(C::B_QFREE));
-      }
+      tc_commit_warp(bar(C::B_SFULL + sb));
+      if (tl.flags & F_END) tc_commit_warp(bar(C::B_QFREE));
       __syncwarp();
       if (pj >= 0 && !issue_pv()) {
         good = false;

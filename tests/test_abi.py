@@ -90,11 +90,11 @@ def test_ws_variant_needs_workspace(lib):
 
 
 @pytest.mark.parametrize("tuning", [(0, 0, 3, 0, 0, 0), (0, 0, 4, 24, 0, 0), (0, 0, 4, 16, 9, 0), (-1, 0, 0, 0, 0, 0),
-                                    (0, 0, 4, 32, 3, 0), (0, 0, 4, 16, 3, 2), (0, 0, 2, 16, 5, 1), (2000, 0, 0, 0, 0, 0),
+                                    (0, 0, 4, 32, 3, 0), (0, 0, 4, 32, 3, 2), (0, 0, 2, 16, 5, 1), (2000, 0, 0, 0, 0, 0),
                                     (0, 0, 0, 0, 0, 0, -2), (0, 0, 0, 0, 0, 0, 0, -2), (0, 0, 0, 0, 0, 0, 0, 70000),
                                     (0, 0, 0, 0, 0, 0, 0, 0, 901), (0, 0, 0, 0, 0, 0, 0, 0, -1),
                                     (0, 0, 0, 0, 0, 0, 0, 0, 0, -1), (0, 0, 4, 16, 3, 3), (0, 0, 2, 16, 2, 3),
-                                    (0, 0, 0, 0, 0, 4)])
+                                    (0, 0, 0, 0, 0, 4), (0, 0, 2, 16, 2, 2), (0, 0, 4, 24, 2, 2), (0, 0, 4, 16, 5, 2)])
 def test_unsupported_tuning_rejected(lib, tuning):
     assert _lib.gqa_paged_decode_set_tuning(*tuning) == _lib.GQA_ERR_INVALID_ARGUMENT
 
@@ -103,7 +103,8 @@ def test_unsupported_tuning_rejected(lib, tuning):
                                     (0, 0, 4, 32, 3, 1), (0, 0, 4, 16, 5, 1), (64, 32, 2, 16, 5, 0),
                                     (0, 0, 0, 0, 0, 0, -1), (0, 0, 0, 0, 0, 0, 64), (0, 0, 0, 0, 0, 0, 0, -1),
                                     (0, 0, 0, 0, 0, 0, 0, 5000, 900, 1), (0, 0, 0, 0, 0, 0, 0, 0, 50, 128),
-                                    (0, 0, 4, 16, 2, 3), (0, 0, 0, 0, 0, 3)])
+                                    (0, 0, 4, 16, 2, 3), (0, 0, 0, 0, 0, 3), (0, 0, 4, 16, 3, 2), (0, 0, 4, 32, 2, 2),
+                                    (0, 0, 0, 0, 0, 2)])
 def test_supported_tuning_accepted(lib, tuning):
     assert _lib.gqa_paged_decode_set_tuning(*tuning) == 0
     assert _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0) == 0

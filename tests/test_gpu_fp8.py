@@ -25,6 +25,13 @@ def _defaults(cuda_device):
     _lib.gqa_paged_decode_set_tuning(0, 0, 0, 0, 0, 0)
 
 
+@pytest.fixture(params=[16, 32], ids=["stage16", "stage32"])
+def f8_stage(request):
+    """Both FP8 stage sizes (16 or 32 tokens per pipeline stage, 2-deep ring)."""
+    assert _lib.gqa_paged_decode_set_tuning(0, 0, 4, request.param, 2, _lib.GATHER_LSU_F8) == 0
+    return request.param
+
+
 def gpu_fp8(w):
     g = w.to("cuda")
     out, lse = _lib.run_fp8(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, w.sm_scale)
@@ -47,7 +54,7 @@ def check(w, out, lse, seqs=None):
 
 @pytest.mark.parametrize("lens", [[1], [0], [0, 0, 3], [15, 16, 17], [255, 256, 257, 0, 129],
                                   [3, 1000, 0, 77, 2049, 1, 16, 600], list(range(1, 41))])
-def test_fp8_edge_and_ragged(lens):
+def test_fp8_edge_and_ragged(lens, f8_stage):
     w = wl.make_fp8_workload(lens, seed=len(lens) + 300, pool_factor=1.5)
     out, lse = gpu_fp8(w)
     check(w, out, lse)
@@ -55,7 +62,10 @@ def test_fp8_edge_and_ragged(lens):
 
 @pytest.mark.parametrize("tuning", [(0, 0, 4, 16, 2, 0), (0, 0, 4, 16, 3, 0), (0, 0, 4, 16, 4, 0),
                                     (40, 8, 4, 16, 2, 0, 0, 0, 500, 16), (7, 1, 4, 16, 3, 0, 0, 13, 400, 4),
-                                    (300, 1, 4, 16, 2, 0, 4), (60, 8, 4, 16, 4, 0, -1, -1)])
+                                    (300, 1, 4, 16, 2, 0, 4), (60, 8, 4, 16, 4, 0, -1, -1),
+                                    (0, 0, 4, 32, 2, 2), (0, 0, 4, 16, 3, 2), (40, 8, 4, 32, 2, 2, 0, 0, 500, 16),
+                                    (7, 1, 4, 32, 2, 2, 0, 13, 400, 4), (300, 1, 4, 32, 2, 2, 4),
+                                    (60, 8, 4, 32, 2, 2, -1, -1), (5, 40, 4, 32, 2, 2, 0, 3, 300, 33)])
 def test_fp8_variants_and_splits(tuning):
     assert _lib.gqa_paged_decode_set_tuning(*tuning) == 0
     w = wl.make_fp8_workload([5000, 3, 17, 0, 900, 1, 64], seed=301, pool_factor=1.1)
@@ -63,7 +73,7 @@ def test_fp8_variants_and_splits(tuning):
     check(w, out, lse)
 
 
-def test_fp8_large_queries():
+def test_fp8_large_queries(f8_stage):
     """|q| near 1e4: the f16 form of Q needs its power-of-two rescale."""
     w = wl.make_fp8_workload([700, 64, 3], seed=302, q_std=1.0)
     w.q.mul_(8192.0)                                   # exact in bf16 (a power of two)
@@ -79,7 +89,7 @@ def _scale_rows(cache, up, down):
     cache[:, 512:] = sc.view(torch.uint8)
 
 
-def test_fp8_extreme_and_zero_scales():
+def test_fp8_extreme_and_zero_scales(f8_stage):
     """K scales 2^4 up and down on some tokens (sharp softmax), V scales 2^5 up
     and down on others (the P operand's running normaliser), all-zero rows
     elsewhere. Much larger spreads leave the test's absolute tolerances, not
@@ -97,7 +107,7 @@ def test_fp8_extreme_and_zero_scales():
 
 
 @pytest.mark.parametrize("name", ["mid", "skewed"])
-def test_fp8_named_workloads_every_sequence(name):
+def test_fp8_named_workloads_every_sequence(name, f8_stage):
     """The mid and skewed batches over an FP8 copy of their caches, every
     sequence against the FP8 oracle."""
     w = wl.make_fp8_config(name)
@@ -105,7 +115,7 @@ def test_fp8_named_workloads_every_sequence(name):
     check(w, out, lse)
 
 
-def test_fp8_int64_page_addressing():
+def test_fp8_int64_page_addressing(f8_stage):
     """Pages above 2^31 / 528 sit more than 2^31 bytes into each 528-byte-per-page pool."""
     base = (1 << 31) // _lib.FP8_ROW_BYTES + 1
     num_pages = base + 4096
@@ -121,3 +131,20 @@ def test_fp8_int64_page_addressing():
     torch.cuda.synchronize()
     check(small, out.float().cpu().double().numpy(), lse.cpu().double().numpy())
     del k, v
+
+
+def test_bf16_call_under_fp8_tuning():
+    """An FP8 tuning leaves bf16-cache calls on the default bf16 kernel."""
+    import oracle
+    assert _lib.gqa_paged_decode_set_tuning(0, 0, 4, 32, 2, _lib.GATHER_LSU_F8) == 0
+    w = wl.make_workload([300, 0, 17, 2000], seed=304)
+    g = w.to("cuda")
+    out, lse = _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, w.sm_scale)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.gqa_paged_decode_oracle(w.q, w.k_cache, w.v_cache, w.kv_indptr, w.kv_indices, w.sm_scale)
+    o = out.float().cpu().double().numpy()
+    assert np.all(np.abs(o - o_ref) <= O_ATOL + O_RTOL * np.abs(o_ref))
+    l = lse.cpu().double().numpy()
+    fin = np.isfinite(l_ref)
+    assert np.array_equal(np.isneginf(l), np.isneginf(l_ref))
+    assert np.all(np.abs(l[fin] - l_ref[fin]) <= LSE_ATOL)
