@@ -614,6 +614,11 @@ __global__ void __launch_bounds__(NG * 32, (F8 || CC) ? (TT == 32 ? 2 : 3) : 16 
   };
 
   // -------------------------------------------------------------- issue
+  // bf16 K/V head rows are read once: they leave L2 first, ahead of the page ids, Q and the split
+  // partials (measured: about 10 us less per call on the large batch, 6 us on the skewed one). Not
+  // for the FP8 rows: a 528-byte token row puts the 128-byte head chunks of neighbouring warps in
+  // shared sectors, which the hint then evicts between the two reads (280 -> 296 us on large).
+  const uint64_t stream_pol = F8 ? 0ull : l2_policy_evict_first();
   uint32_t qn[16];        // Q fragments of the next piece, loaded at issue time
   bool qn_busy = false;
   int issued = 0;
@@ -691,8 +696,8 @@ __global__ void __launch_bounds__(NG * 32, (F8 || CC) ? (TT == 32 ? 2 : 3) : 16 
         }
         const int64_t off = static_cast<int64_t>(pg) * kPageBytes + hoff + pc * 16;
         const uint32_t nbytes = valid ? 16u : 0u;
-        cp_async_16(sb + C::kKOff + tok * C::kRowPitch + pc * 16, kc + off, nbytes);
-        cp_async_16(sb + C::kVOff + tok * C::kRowPitch + pc * 16, vc + off, nbytes);
+        cp_async_16_hint(sb + C::kKOff + tok * C::kRowPitch + pc * 16, kc + off, nbytes, stream_pol);
+        cp_async_16_hint(sb + C::kVOff + tok * C::kRowPitch + pc * 16, vc + off, nbytes, stream_pol);
       }
       if (flags & F_QLOAD) {
         const int h0 = (tl.hg * NG + w) * kGroup;

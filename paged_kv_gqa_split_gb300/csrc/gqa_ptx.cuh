@@ -83,7 +83,7 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // ------------------------------------------------------------ TMA bulk copy
-// L2 policy for data read exactly once (the KV pages): evict first.
+// L2 policy for data read exactly once (the K/V rows): evict first.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -115,6 +115,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 // reads nothing. Completion is tracked per thread with commit/wait_group.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// cp_async_16 with an L2 cache policy (e.g. l2_policy_evict_first for data read once).
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src),
+               "r"(src_bytes), "l"(pol)
+               : "memory");
 }
 
 // 4 bytes global -> shared (src_bytes == 0 writes zeros).
