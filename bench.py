@@ -420,6 +420,38 @@ def bench_cuda_cores(names, device, steps, warmup, peak, variant_only=False):
 
 
 # ------------------------------------------------------------ MLA decode
+def bench_mla_heads(device, steps, warmup, peak, heads=(16, 32, 64, 128)):
+    """Both MLA kernels on the MLA batch's lengths and cache with h_q query heads each:
+    where the tensor-memory kernel overtakes the mma.sync one."""
+    res = {}
+    for h in heads:
+        w = wl.make_mla_config(h_q=h)
+        g = w.to(device)
+        rows = int(w.q.shape[1] * w.q.shape[2])
+        out = torch.empty((w.batch, w.q.shape[1], w.q.shape[2], 512), dtype=torch.bfloat16, device=device)
+        lse = torch.empty((w.batch, w.q.shape[2], w.q.shape[1]), dtype=torch.float32, device=device)
+        stream = torch.cuda.current_stream(device)
+        flush = L2Flush(device)
+        b = 1152 * w.total_tokens + (1152 + 1024 + 4) * rows * w.batch
+        r = {"counted_bytes": b}
+        for kernel, key in ((1, "tensor_memory"), (3, "mma_sync")):
+            _lib.gqa_mla_set_tuning(kernel)
+            try:
+                def call():
+                    _lib.mla_run(g.q, g.kv_cache, g.block_table, g.cache_seqlens, w.softmax_scale, out=out, lse=lse,
+                                 stream=stream)
+                for _ in range(warmup):
+                    call()
+                ms = statistics.median(time_steps(call, steps, stream, flush))
+            finally:
+                _lib.gqa_mla_set_tuning(0)
+            r[key] = {"us_per_batch": ms * 1e3, "frac_of_peak": b / (ms * 1e-3) / 1e9 / peak}
+        r["default"] = "tensor_memory" if rows % 32 == 0 else "mma_sync"
+        res[f"h_q={h}"] = r
+        del g, out, lse, flush
+    return res
+
+
 def bench_mla(device, steps, warmup, peak, wide: bool = False):
     """Dense MLA decode of the MLA workload (128 sequences of U[1024, 8192]
     cached tokens, 16 query heads, blocks of 64; with `wide`, 64 query heads on
@@ -454,12 +486,12 @@ def bench_mla(device, steps, warmup, peak, wide: bool = False):
                 "tflops": flops / (ms * 1e-3) / 1e12}
     tc = timed(1)   # the tensor-memory (tcgen05) kernel: 16- or 64-row pieces
     mma = timed(3)  # the mma.sync kernel: 16-row pieces
-    default_tc = rows % 64 == 0 and w.page_size % 32 == 0
+    default_tc = rows % 32 == 0 and w.page_size % 32 == 0
     d = tc if default_tc else mma
     res = {"batch": w.batch, "h_q": int(w.q.shape[2]), "s_q": int(w.q.shape[1]), "page_size": w.page_size,
            "total_tokens": t, "us_per_batch": d["us_per_batch"], "gbs": d["gbs"], "frac_of_peak": d["frac_of_peak"],
            "tflops": d["tflops"], "counted_bytes": b,
-           "kernel": ("tensor memory, %d-row pieces" % (64 if rows % 64 == 0 else 16)) if default_tc
+           "kernel": ("tensor memory, %d-row pieces" % (64 if rows % 64 == 0 else 32)) if default_tc
            else "mma.sync, 3-stage ring",
            "tensor_memory_kernel": dict(tc, launches_per_call=3), "mma_sync_kernel": dict(mma, launches_per_call=4)}
     del g, out, lse, flush
@@ -582,7 +614,7 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="time every decode variant instead of the contract line")
     ap.add_argument("--merge-mode", type=int, choices=[0, 1], default=0,
                     help="0: decode grid + merge kernel (default); 1: one-wave decode with the merge inside the kernel")
-    ap.add_argument("--only", choices=["fp8", "sparse", "mla", "mla-wide", "cuda-cores"], default=None,
+    ap.add_argument("--only", choices=["fp8", "sparse", "mla", "mla-wide", "mla-heads", "cuda-cores"], default=None,
                     help="time only the FP8-cache decode of --workload, or only the selected-token decode, and "
                          "print its result (for profiling a small case)")
     args = ap.parse_args()
@@ -619,6 +651,8 @@ def main():
             res = bench_mla(device, args.steps, warmup, peak)
         elif args.only == "mla-wide":
             res = bench_mla(device, args.steps, warmup, peak, wide=True)
+        elif args.only == "mla-heads":
+            res = bench_mla_heads(device, args.steps, warmup, peak)
         elif args.only == "cuda-cores":
             res = bench_cuda_cores([args.workload], device, args.steps, warmup, peak, variant_only=True)
         else:

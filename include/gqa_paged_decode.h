@@ -267,13 +267,14 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
 
 /*
  * Kernel choice of gqa_mla_decode for tests and benchmarks (process-wide):
- * 0 - default: the tensor-memory kernel when s_q * h_q is a multiple of 64 and
- *     page_size a multiple of 32 (one pass over the latent rows serves 64
- *     query rows); otherwise the mma.sync kernel with a 3-stage ring;
+ * 0 - default: the tensor-memory kernel when s_q * h_q is a multiple of 32 and
+ *     page_size a multiple of 32 (one pass over the latent rows serves 32 or
+ *     64 query rows); otherwise the mma.sync kernel with a 3-stage ring;
  * 1 - the tensor-memory kernel (tcgen05 MMAs into tensor memory with 128
  *     tokens on M, 2D tensor copies of the latent rows, one CTA per SM; pieces
- *     of 64 query rows when s_q * h_q is a multiple of 64, else 16) when
- *     page_size is a multiple of 32, else the mma.sync kernel;
+ *     of 64 query rows when s_q * h_q is a multiple of 64, else 32 when it is a
+ *     multiple of 32, else 16) when page_size is a multiple of 32, else the
+ *     mma.sync kernel;
  * 3, 4 - the mma.sync kernel (16-row pieces) with a 3-stage ring (three CTAs
  *     per SM) or a 4-stage ring (two CTAs per SM).
  * The tier settings of gqa_paged_decode_set_tuning (tier-1 CTAs, smallest

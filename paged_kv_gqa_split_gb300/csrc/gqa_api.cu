@@ -672,11 +672,12 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
     if (rc != GQA_OK) return rc;
     const Tuning& t = g_tune;
     mla_kind = t.mla_kernel;
-    // default: the tensor-memory kernel when a sequence's rows come in multiples of 64 (one pass over the
-    // latent rows serves 64 rows, where the mma.sync kernel reads them once per 16); mma.sync otherwise
+    // default: the tensor-memory kernel when a sequence's rows come in multiples of 32 (one pass over the
+    // latent rows serves 32 or 64 rows, where the mma.sync kernel reads them once per 16; measured faster
+    // from 32 rows up), mma.sync otherwise (faster at 16 rows)
     mp.piece_rows = 16;
     if (mla_kind == gqa::kMlaKernelDefault)
-      mla_kind = rows % 64 == 0 ? gqa::kMlaKernelTensorMemory : gqa::kMlaKernelMma3;
+      mla_kind = rows % 32 == 0 ? gqa::kMlaKernelTensorMemory : gqa::kMlaKernelMma3;
     if (mla_kind == gqa::kMlaKernelTensorMemory) {
       // where the block size allows it (and Q rows fit the 32-bit box coordinates); else the mma.sync kernel
       mp.piece_rows = gqa::mla_tc_piece_rows(static_cast<int>(rows));

@@ -114,7 +114,7 @@ struct MlaParams {
   float scale_log2;
   const int* block_table;  // [batch][width]
   int width, page_size, num_blocks;
-  int piece_rows;  // query rows per piece (row group): 16, or 64 for the tensor-memory kernel's wide tiles
+  int piece_rows;  // query rows per piece (row group): 16, or 32 / 64 for the tensor-memory kernel's wide tiles
 };
 
 // MLA decode kernels: the tensor-memory kernel (block sizes that are a
@@ -128,7 +128,7 @@ struct MlaTcMaps {  // 2D tensor maps of the latent cache (boxes of 64 x 32) and
   CUtensorMap q;
 };
 bool mla_tc_supported(int page_size);
-int mla_tc_piece_rows(int rows);  // 64 when the rows of a sequence come in multiples of 64, else 16
+int mla_tc_piece_rows(int rows);  // 64 / 32 when the rows of a sequence come in multiples of 64 / 32, else 16
 bool mla_tc_encode(const MlaParams& p, MlaTcMaps* maps);
 cudaError_t launch_mla_tc_decode(const MlaParams& p, const MlaTcMaps& maps, int ctas, cudaStream_t stream);
 cudaError_t launch_mla(const MlaParams& p, const int* cache_seqlens, int kind, const MlaTcMaps* maps,

@@ -5,8 +5,9 @@
 // multiple of 32 tokens.
 //
 // A tcgen05.mma costs about 45-80 cycles at small shapes, so the tiles put 128
-// tokens on M and the R query rows of a piece (16, or 64 when the rows of a
-// sequence come in multiples of 64) on N: S^T = K Q^T (M = 128 tokens, N = R,
+// tokens on M and the R query rows of a piece (64 when the rows of a sequence
+// come in multiples of 64, else 32 when in multiples of 32, else 16) on N:
+// S^T = K Q^T (M = 128 tokens, N = R,
 // K = 576: 36 MMAs) and O^T += V^T P^T (M = 128 dims x 4 blocks, N = R,
 // K = 128 tokens: 32 MMAs) per 128-token tile. With R = 64 one pass over the
 // latent rows serves 64 heads, where 16-row pieces would read them four times.
@@ -14,7 +15,8 @@
 // through a ring of 32 KB units (two 64-dim regions of the 128 rows, loaded by
 // 2D tensor copies with 128-byte swizzle): five units feed S^T, and the four V
 // units are loaded again (from L2) for the P.V of the tile once its softmax is
-// done.
+// done. The ring holds 6 units at R = 16, 5 at R = 32 and 4 at R = 64, beside
+// Q (R rows x 576) and the P^T buffers.
 //
 // One CTA per SM, in roles:
 //   softmax groups (4 warps each, one per 32-lane quarter of tensor memory):
@@ -62,8 +64,8 @@ struct TcCfg {
   static constexpr int kMmaWarp = kSoftWarps;
   static constexpr int kProdWarp = kSoftWarps + 1;
   static constexpr int kThreads = (kSoftWarps + 2) * 32;
-  static constexpr int kRing = R == 16 ? 6 : 4;
-  static constexpr int kPBufs = R == 16 ? 2 : 1;    // P^T buffers (one at R = 64 leaves room for a 4th unit)
+  static constexpr int kRing = R == 16 ? 6 : (R == 32 ? 5 : 4);
+  static constexpr int kPBufs = R == 64 ? 1 : 2;    // P^T buffers (one at R = 64 leaves room for a 4th unit)
   static constexpr int kQRegion = R * 128;           // R rows x 64 dims
   static constexpr int kPBytes = R * kTile * 2;      // P^T: R rows x 128 tokens
   static constexpr int kQOff = kRing * kUnitBytes;
@@ -87,7 +89,7 @@ struct TcCfg {
   static constexpr int kSlotOff = kBarOff + kBars * 8;
   static constexpr int kAbortOff = kSlotOff + 4;
   static constexpr int kSmemBytes = kAbortOff + 4 + 1024;  // the base is rounded up to 1024 B (swizzle atoms)
-  static constexpr uint32_t kCols = R == 16 ? 128 : 512;  // S^T at columns 0 and R, O^T block mb at 2R + R mb
+  static constexpr uint32_t kCols = R == 16 ? 128 : (R == 32 ? 256 : 512);  // S^T at 0 and R, O^T block mb at 2R + R mb
   static_assert(kSmemBytes <= 227 * 1024, "tensor-memory MLA decode exceeds shared memory");
   static_assert(kQOff % 1024 == 0 && kPOff % 1024 == 0, "swizzle atoms need 1024-byte alignment");
   static_assert(2 * R + 4 * R <= static_cast<int>(kCols), "tensor memory columns");
@@ -678,7 +680,7 @@ cudaError_t launch_tc(const MlaParams& p, const MlaTcMaps& maps, int ctas, cudaS
 
 bool mla_tc_supported(int page_size) { return page_size > 0 && page_size % 32 == 0; }
 
-int mla_tc_piece_rows(int rows) { return rows % 64 == 0 ? 64 : 16; }
+int mla_tc_piece_rows(int rows) { return rows % 64 == 0 ? 64 : (rows % 32 == 0 ? 32 : 16); }
 
 bool mla_tc_encode(const MlaParams& p, MlaTcMaps* maps) {
   return encode_rows(&maps->kv, p.kv, static_cast<int64_t>(p.num_blocks) * p.page_size, box_rows_for(p.page_size)) &&
@@ -689,6 +691,8 @@ cudaError_t launch_mla_tc_decode(const MlaParams& p, const MlaTcMaps& maps, int 
   const bool br64 = box_rows_for(p.page_size) == 64;
   if (p.piece_rows == 64)
     return br64 ? launch_tc<64, 64>(p, maps, ctas, stream) : launch_tc<32, 64>(p, maps, ctas, stream);
+  if (p.piece_rows == 32)
+    return br64 ? launch_tc<64, 32>(p, maps, ctas, stream) : launch_tc<32, 32>(p, maps, ctas, stream);
   return br64 ? launch_tc<64, 16>(p, maps, ctas, stream) : launch_tc<32, 16>(p, maps, ctas, stream);
 }
 

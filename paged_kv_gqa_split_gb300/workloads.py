@@ -449,9 +449,13 @@ MLA_CONFIG = dict(batch=128, h_q=16, s_q=1, page_size=64, len_lo=1024, len_hi=81
 MLA_WIDE_CONFIG = dict(MLA_CONFIG, h_q=64)
 
 
-def make_mla_config(wide: bool = False) -> MlaWorkload:
+def make_mla_config(wide: bool = False, h_q: Optional[int] = None) -> MlaWorkload:
+    """The MLA batch (16 query heads), its 64-head form (`wide`), or the same lengths and
+    cache with `h_q` query heads."""
     c = MLA_WIDE_CONFIG if wide else MLA_CONFIG
+    heads = c["h_q"] if h_q is None else int(h_q)
     g = torch.Generator().manual_seed(c["seed"])
     lens = torch.randint(c["len_lo"], c["len_hi"] + 1, (c["batch"],), generator=g).tolist()
-    return make_mla_workload(lens, c["h_q"], c["s_q"], c["page_size"], c["seed"] + 1000,
-                             pool_factor=c["pool_factor"], name="mla_wide" if wide else "mla")
+    name = "mla_wide" if wide else "mla"
+    return make_mla_workload(lens, heads, c["s_q"], c["page_size"], c["seed"] + 1000,
+                             pool_factor=c["pool_factor"], name=name if h_q is None else f"mla_h{heads}")

@@ -178,10 +178,15 @@ def test_mla_tensor_memory_shapes(lens, h_q, s_q, ps, seed, ctas):
     ([600, 33, 128], 32, 2, 32, 43, 0, 1),                # 2 query tokens x 32 heads, 32-row copies
     ([3000, 5, 2000], 64, 1, 128, 44, 9, 1),              # few CTAs: several pieces and Q reloads per CTA
     ([4096, 4096, 4095], 64, 1, 64, 45, 300, 1),          # many pieces per sequence: the merge's long chains
+    ([900, 1, 0, 130], 32, 1, 64, 47, 0, 1),              # 32-row pieces
+    ([700, 257, 33], 16, 2, 64, 48, 0, 1),                # 2 query tokens x 16 heads: 32-row pieces
+    ([600, 129], 96, 1, 32, 49, 0, 1),                    # three 32-row groups, 32-row copies
+    ([3000, 5, 2000], 32, 1, 128, 50, 9, 1),              # 32-row pieces, few CTAs: Q reloads per CTA
+    ([4096, 4095], 32, 1, 64, 51, 300, 1),                # 32-row pieces, many pieces per sequence
 ])
 def test_mla_wide_pieces(lens, h_q, s_q, ps, seed, ctas, kernel):
-    """64-row pieces of the tensor-memory kernel (a sequence's rows in multiples of 64), against the
-    oracle and against the mma.sync kernel (16-row pieces) on the same inputs."""
+    """64- and 32-row pieces of the tensor-memory kernel (a sequence's rows in multiples of 64 or 32),
+    against the oracle and against the mma.sync kernel (16-row pieces) on the same inputs."""
     w = wl.make_mla_workload(lens, h_q, s_q, ps, seed)
     assert _lib.gqa_paged_decode_set_tuning(ctas, 0, 0, 0, 0, 0) == 0
     assert _lib.gqa_mla_set_tuning(kernel) == 0
