@@ -4,6 +4,7 @@ Tolerance (stated for this path): |dO| <= 2e-2 + 2e-2 * |O_ref| elementwise and
 |dlse| <= 1e-3 absolute, with -inf == -inf for empty sequences.
 """
 import json
+import itertools
 import math
 import os
 
@@ -183,6 +184,34 @@ def test_token_count_exact_with_uniform_scores(tuning, variant, merge_mode):
     tuning(*variant)
     lens = [9000, 1, 2, 3, 4000, 0, 17, 1023, 1024, 1025, 5]
     w = wl.make_workload(lens, seed=33, pool_factor=1.0)
+    w.q.zero_()
+    out, lse = gpu_run(w)
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert np.all(np.isneginf(lse[b]))
+        else:
+            assert np.abs(lse[b] - math.log2(n)).max() < 2e-5, (b, n, lse[b][:4])
+    check(w, out, lse)
+
+
+@pytest.mark.parametrize("ng", [4, 2, 1])
+@pytest.mark.parametrize("pieces", [17, 32, 33, 34, 64, 65, 97, 150, 300])
+def test_block_merge_piece_counts(tuning, ng, pieces):
+    """Sequences cut into more than 16 pieces go to the merge kernel's block path, whose block width
+    halves as the piece count doubles (32 dims at 17 pieces, 16 past 32, ..., 1 past 256) and whose
+    rows walk the pieces in batches. One tier of pieces x (4 / ng) CTAs cuts the long sequence into
+    about `pieces` pieces per head group (around those edges, checked on the host plan), for every
+    head-group shape; then the same with q = 0, where lse must be log2(n) exactly (a piece dropped or
+    folded twice shows) and O the mean of the V rows."""
+    lens = [4160, 3, 0, 1]
+    ctas = pieces * (4 // ng)
+    plan = _lib.gqa_paged_decode_plan([0] + list(itertools.accumulate(lens)), ctas, 1, ng, 0, 0, 0)
+    cut = max(sum(1 for x in plan if x[1] == 0 and x[2] == hg) for hg in range(4 // ng))
+    assert abs(cut - pieces) <= 1 + pieces // 16, cut
+    tuning(ctas, 1, ng, 16, 2, 0, 0, -1)
+    w = wl.make_workload(lens, seed=90 + pieces, pool_factor=1.1)
+    out, lse = gpu_run(w)
+    check(w, out, lse)
     w.q.zero_()
     out, lse = gpu_run(w)
     for b, n in enumerate(lens):
