@@ -92,7 +92,7 @@ def test_replicas_gloo_two_ranks():
 
 
 def test_reference_arm_under_torchrun_two_ranks():
-    """`bench.py --impl reference` launched as the driver launches N > 1: rank 0 alone prints
+    """`bench.py --impl reference` launched under torch.distributed.run with N = 2: rank 0 alone prints
     one line (the oracle on the host's cores); the other rank exits 0 without work."""
     import json
     import subprocess
