@@ -616,8 +616,8 @@ __global__ void __launch_bounds__(NG * 32, (F8 || CC) ? (TT == 32 ? 2 : 3) : 16 
   // -------------------------------------------------------------- issue
   // bf16 K/V head rows are read once: they leave L2 first, ahead of the page ids, Q and the split
   // partials (measured: about 10 us less per call on the large batch, 6 us on the skewed one). Not
-  // for the FP8 rows: a 528-byte token row puts the 128-byte head chunks of neighbouring warps in
-  // shared sectors, which the hint then evicts between the two reads (280 -> 296 us on large).
+  // for the FP8 rows, whose issue-bound loop measured slower with the hint (280 -> 296 us on large;
+  // 356 us with it kept off the sectors that neighbouring heads' chunks share).
   const uint64_t stream_pol = F8 ? 0ull : l2_policy_evict_first();
   uint32_t qn[16];        // Q fragments of the next piece, loaded at issue time
   bool qn_busy = false;

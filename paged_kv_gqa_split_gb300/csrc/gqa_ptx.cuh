@@ -124,6 +124,16 @@ __device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void* src, 
                : "memory");
 }
 
+// cp_async_16 with an evict-first L2 policy formed inside the instruction
+// sequence (no policy register held across the caller's code).
+__device__ __forceinline__ void cp_async_16_evict_first(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 pol;\n\tcreatepolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+      "cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, pol;\n\t}" ::"r"(dst),
+      "l"(src), "r"(src_bytes)
+      : "memory");
+}
+
 // 4 bytes global -> shared (src_bytes == 0 writes zeros).
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
