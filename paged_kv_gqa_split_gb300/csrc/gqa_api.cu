@@ -32,6 +32,10 @@ constexpr int kDefaultTier2PerTier1 = 2;
 constexpr int kDefaultTier2Permille = 100;
 constexpr int kDefaultTier2MinUnits = 64;
 constexpr int kMaxTier2Ctas = 1 << 16;
+// Tokens of work an extra piece adds to a CTA of the MLA tensor-memory kernel (the Q reload, the
+// drained pipeline and the O epilogue at a sequence boundary: about 16 us at 64 rows, where a
+// 128-token tile takes about 5 us), used to balance its CTA ranges.
+constexpr int kMlaTcPieceCost = 400;
 // Tokens per pipeline stage of the FP8-cache decode with a 2-deep ring.
 constexpr int kDefaultF8Tile = 16;
 constexpr int kSmemPerSm = 228 * 1024;
@@ -654,7 +658,8 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
   int dev = 0;
   gqa::PlanConfig cfg;
   void* ws = nullptr;
-  size_t off_indptr = 0, off_slots = 0, off_po = 0, off_pl = 0, off_rec = 0;
+  size_t off_indptr = 0, off_slots = 0, off_po = 0, off_pl = 0, off_rec = 0, off_cost = 0, off_bounds = 0;
+  bool balanced = false;
   gqa::MlaParams mp{};
   mp.q = q;
   mp.kv = kv_cache;
@@ -699,7 +704,11 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
     const size_t pr = static_cast<size_t>(mp.piece_rows);
     off_pl = off_po + round256(2 * ctas * pr * 512 * sizeof(float));
     off_rec = off_pl + round256(2 * ctas * pr * sizeof(float));
-    const size_t need = off_rec + round256(2 * ctas * 16);
+    // the tensor-memory kernel with one tier: CTA ranges balanced by the scan for the cost of pieces
+    balanced = mla_kind == gqa::kMlaKernelTensorMemory && cfg.tier2_ctas == 0;
+    off_cost = off_rec + round256(2 * ctas * 16);
+    off_bounds = off_cost + round256(static_cast<size_t>(batch + 1) * 4);
+    const size_t need = off_bounds + round256((ctas + 1) * sizeof(int64_t));
     rc = library_workspace(st, need, &ws);
     if (rc != GQA_OK) return rc;
   }
@@ -715,6 +724,9 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
   mp.part_o = reinterpret_cast<float*>(wsb + off_po);
   mp.part_lse = reinterpret_cast<float*>(wsb + off_pl);
   mp.split_rec = reinterpret_cast<int4*>(wsb + off_rec);
+  mp.cost_ptr = reinterpret_cast<int*>(wsb + off_cost);
+  mp.bounds = balanced ? reinterpret_cast<int64_t*>(wsb + off_bounds) : nullptr;
+  mp.piece_cost = kMlaTcPieceCost;
   mp.err = err_word;
   mp.plan = cfg;
   mp.epoch = (g_epoch.fetch_add(1) % ((1ull << 40) - 1)) + 1;

@@ -115,6 +115,12 @@ struct MlaParams {
   const int* block_table;  // [batch][width]
   int width, page_size, num_blocks;
   int piece_rows;  // query rows per piece (row group): 16, or 32 / 64 for the tensor-memory kernel's wide tiles
+  // tensor-memory kernel, one tier: the first unit of each of the P1 CTAs (and the unit count at
+  // [P1]), placed by the scan so that every CTA carries the same tokens plus piece_cost per sequence
+  // start; NULL: the plan's equal ranges
+  int64_t* bounds;
+  int* cost_ptr;   // [B + 1] scratch of the scan: prefix of (length + piece_cost) over non-empty sequences
+  int piece_cost;  // tokens one extra piece costs a CTA of the tensor-memory kernel
 };
 
 // MLA decode kernels: the tensor-memory kernel (block sizes that are a

@@ -72,15 +72,14 @@ struct MlaSmemPlan {
 // kv_indptr = exclusive prefix sum of the lengths, each clamped to [0, cap]
 // (cap = the block table's width * page_size: tokens past the table have no
 // block, and the slot buffer holds batch * cap entries); one CTA.
-__global__ void __launch_bounds__(1024) gqa_mla_scan_kernel(const int* __restrict__ seqlens, int batch, int cap,
-                                                            int* __restrict__ indptr) {
-  __shared__ int warp_sum[32];
-  pdl_launch_dependents();
+// Exclusive prefix over the batch of f(b) into out[0..batch] (one CTA of 1024 threads).
+template <typename F>
+__device__ __forceinline__ void block_exclusive_scan(int batch, F f, int* __restrict__ out, int* warp_sum) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (batch + 1023) / 1024;
   const int lo = tid * per, hi = min(batch, lo + per);
   int mine = 0;
-  for (int i = lo; i < hi; ++i) mine += min(max(__ldg(seqlens + i), 0), cap);
+  for (int i = lo; i < hi; ++i) mine += f(i);
   int x = mine;  // inclusive warp scan of the chunk sums
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -101,10 +100,64 @@ __global__ void __launch_bounds__(1024) gqa_mla_scan_kernel(const int* __restric
   __syncthreads();
   int run = x - mine + (warp > 0 ? warp_sum[warp - 1] : 0);  // exclusive prefix of this chunk
   for (int i = lo; i < hi; ++i) {
-    indptr[i] = run;
-    run += min(max(__ldg(seqlens + i), 0), cap);
+    out[i] = run;
+    run += f(i);
   }
-  if (tid == 1023) indptr[batch] = warp_sum[31];
+  if (tid == 1023) out[batch] = warp_sum[31];
+  __syncthreads();  // warp_sum is reused by the next scan
+}
+
+// kv_indptr = exclusive prefix sum of the lengths, each clamped to [0, cap]
+// (cap = the block table's width * page_size: tokens past the table have no
+// block, and the slot buffer holds batch * cap entries); one CTA. With bounds,
+// also the tensor-memory kernel's cost-balanced tier-1 ranges: a sequence
+// costs its tokens plus piece_cost (the work an extra piece adds to a CTA), the
+// cost line of each row group is cut into P1 equal parts, and each cut is moved
+// to the unit it falls on (the first token of a sequence when it falls in that
+// sequence's piece cost).
+__global__ void __launch_bounds__(1024) gqa_mla_scan_kernel(const int* __restrict__ seqlens, int batch, int cap,
+                                                            int* __restrict__ indptr, int* __restrict__ cost_ptr,
+                                                            int64_t* __restrict__ bounds, int P1, int HG,
+                                                            int piece_cost) {
+  __shared__ int warp_sum[32];
+  pdl_launch_dependents();
+  auto len = [&](int i) { return min(max(__ldg(seqlens + i), 0), cap); };
+  block_exclusive_scan(batch, len, indptr, warp_sum);
+  if (bounds == nullptr) return;
+  block_exclusive_scan(batch, [&](int i) { const int n = len(i); return n > 0 ? n + piece_cost : 0; }, cost_ptr,
+                       warp_sum);
+  __threadfence_block();
+  __syncthreads();
+  const int64_t T = indptr[batch], Z = cost_ptr[batch];
+  const int64_t Ztot = Z * HG;
+  for (int c = threadIdx.x; c <= P1; c += blockDim.x) {
+    int64_t u = T * HG;  // the last cut: every unit
+    if (c < P1 && Z > 0) {
+      const int64_t target = Ztot * c / P1;
+      const int64_t hg = target / Z, tr = target - hg * Z;
+      int lo = 0, hi = batch;  // the last b with cost_ptr[b] <= tr
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cost_ptr[mid] <= tr) lo = mid; else hi = mid;
+      }
+      const int n = indptr[lo + 1] - indptr[lo];
+      const int64_t off = tr - cost_ptr[lo] - (n > 0 ? piece_cost : 0);
+      u = hg * T + indptr[lo] + (off > 0 ? off : 0);
+    } else if (c < P1) {
+      u = 0;
+    }
+    bounds[c] = u;
+  }
+  __threadfence_block();
+  __syncthreads();
+  if (threadIdx.x == 0) {  // strictly increasing up to the unit count: no empty range but at the end
+    int64_t prev = bounds[0];
+    for (int c = 1; c < P1; ++c) {
+      const int64_t v = min(max(bounds[c], prev + 1), T * HG);
+      bounds[c] = v;
+      prev = v;
+    }
+  }
 }
 
 // slots[indptr[b] + t] = block_table[b, t / page_size] * page_size + t % page_size, or -1.
@@ -530,7 +583,7 @@ __global__ void __launch_bounds__(kMlaMergeThreads) gqa_mla_merge_kernel(const M
   }
   const int HG = p.rows / R;
   const Plan pl = make_plan(static_cast<int64_t>(T) * HG, p.plan);
-  if (!boundary || pl.begin(j + 1) >= pl.W) return;
+  if (!boundary || (p.bounds != nullptr ? p.bounds[j + 1] : pl.begin(j + 1)) >= pl.W) return;
   if (static_cast<unsigned>(rec0.x) != static_cast<unsigned>(p.epoch)) return;
   const int b = rec0.y, S = rec0.w, hg = rec1.x;
   const int first_cta = rec0.z, first_slot = rec1.y;
@@ -641,7 +694,8 @@ cudaError_t launch_mla(const MlaParams& p, const int* cache_seqlens, int kind, c
                        cudaStream_t stream) {
   int width = p.width, page_size = p.page_size, num_blocks = p.num_blocks;
   const int cap = width * page_size;
-  gqa_mla_scan_kernel<<<1, 1024, 0, stream>>>(cache_seqlens, p.batch, cap, p.kv_indptr_mut);
+  gqa_mla_scan_kernel<<<1, 1024, 0, stream>>>(cache_seqlens, p.batch, cap, p.kv_indptr_mut, p.cost_ptr, p.bounds,
+                                              p.plan.tier1_ctas, p.rows / p.piece_rows, p.piece_cost);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int ctas = p.plan.tier1_ctas + p.plan.tier2_ctas;

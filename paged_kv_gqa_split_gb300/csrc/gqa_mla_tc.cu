@@ -109,6 +109,7 @@ struct TcTile {
 // boundaries of the sequence.
 struct TcWalker {
   const int* indptr;
+  const int64_t* bounds;  // cost-balanced CTA ranges (one tier), or NULL for the plan's ranges
   int B, T;
   Plan pl;
   int64_t u0, u1, u_next;
@@ -116,13 +117,26 @@ struct TcWalker {
   bool seg_open, ok;
   SplitInfo p_si;
 
-  __device__ void init(const int* ip, int batch, int total, const Plan& plan, int cta) {
+  __device__ int64_t begin_of(int64_t c) const { return bounds != nullptr ? __ldg(bounds + c) : pl.begin(c); }
+  // CTA whose range holds unit u: with bounds, the last c with bounds[c] <= u (ranges may be empty)
+  __device__ int64_t cta_of(int64_t u) const {
+    if (bounds == nullptr) return pl.cta_of(u);
+    int lo = 0, hi = pl.P1;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(bounds + mid) <= u) lo = mid; else hi = mid;
+    }
+    return lo;
+  }
+
+  __device__ void init(const int* ip, const int64_t* cuts, int batch, int total, const Plan& plan, int cta) {
     indptr = ip;
+    bounds = cuts;
     B = batch;
     T = total;
     pl = plan;
-    u0 = plan.begin(cta);
-    u1 = plan.end(cta);
+    u0 = cuts != nullptr ? __ldg(cuts + cta) : plan.begin(cta);
+    u1 = cuts != nullptr ? __ldg(cuts + cta + 1) : plan.end(cta);
     u_next = u0;
     hg = tt = t_stop = p_lo = p_hi = p_flags = pb = wb = win = 0;
     seg_open = false;
@@ -153,10 +167,10 @@ struct TcWalker {
           p_hi = min(seq_hi, t_stop);
           const int64_t base_u = static_cast<int64_t>(hg) * T;
           p_flags = F_QLOAD | ((tt == p_lo && p_hi == seq_hi) ? F_FINAL : 0) | ((base_u + tt != u0) ? F_SLOT1 : 0);
-          const SeqSplit sp = seq_split(pl, base_u + p_lo, base_u + seq_hi);
-          p_si.S = static_cast<int>(sp.last_cta - sp.first_cta + 1);
-          p_si.first_cta = static_cast<int>(sp.first_cta);
-          p_si.first_slot = sp.first_slot;
+          const int64_t c_first = cta_of(base_u + p_lo), c_last = cta_of(base_u + seq_hi - 1);
+          p_si.S = static_cast<int>(c_last - c_first + 1);
+          p_si.first_cta = static_cast<int>(c_first);
+          p_si.first_slot = (base_u + p_lo == begin_of(c_first)) ? 0 : 1;
         }
         const int t_loc = tt - p_lo;
         const int lim = tt + (kTile - (t_loc & (kTile - 1)));
@@ -296,7 +310,7 @@ __global__ void __launch_bounds__(TcCfg<R>::kThreads, 1)
   const int HG = p.rows / R;
   const Plan pl = make_plan(static_cast<int64_t>(T) * HG, p.plan);
   TcWalker wk;
-  wk.init(p.kv_indptr, p.batch, T, pl, blockIdx.x);
+  wk.init(p.kv_indptr, p.bounds, p.batch, T, pl, blockIdx.x);
   TcTile tl;
   int* err = p.err;
 
