@@ -705,7 +705,9 @@ int gqa_mla_decode(const void* q, const void* kv_cache, const int32_t* block_tab
     off_pl = off_po + round256(2 * ctas * pr * 512 * sizeof(float));
     off_rec = off_pl + round256(2 * ctas * pr * sizeof(float));
     // the tensor-memory kernel with one tier: CTA ranges balanced by the scan for the cost of pieces
-    balanced = mla_kind == gqa::kMlaKernelTensorMemory && cfg.tier2_ctas == 0;
+    // (the scan's 32-bit cost prefix must hold every token plus the piece cost of every sequence)
+    balanced = mla_kind == gqa::kMlaKernelTensorMemory && cfg.tier2_ctas == 0 &&
+               max_tokens + static_cast<int64_t>(batch) * kMlaTcPieceCost <= INT32_MAX;
     off_cost = off_rec + round256(2 * ctas * 16);
     off_bounds = off_cost + round256(static_cast<size_t>(batch + 1) * 4);
     const size_t need = off_bounds + round256((ctas + 1) * sizeof(int64_t));
