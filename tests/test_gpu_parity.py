@@ -115,6 +115,30 @@ def test_edge_cases_default(name, merge_mode):
     check(w, out, lse)
 
 
+@pytest.mark.parametrize("case", ["5000_short", "3000_empty"])
+def test_batch_past_merge_grid(case, merge_mode):
+    """More sequences than merge CTAs (and than one-wave warps x 32): every empty sequence is still
+    written (O = 0, LSE = -inf) over outputs that start as garbage, and a CTA range walks hundreds of
+    sequences."""
+    if case == "5000_short":
+        lens = torch.randint(0, 9, (5000,), generator=torch.Generator().manual_seed(5)).tolist()
+    else:
+        lens = [0] * 3000
+    w = wl.make_workload(lens, seed=6, pool_factor=1.25)
+    g = w.to("cuda")
+    out = torch.full_like(g.q, 7.0)
+    lse = torch.full((w.batch, 32), 7.0, dtype=torch.float32, device="cuda")
+    _lib.run(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, w.sm_scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    o = out.float().cpu().double().numpy()
+    l = lse.cpu().double().numpy()
+    empty = [b for b, n in enumerate(lens) if n == 0]
+    assert len(empty) > 1367 or case == "5000_short"
+    assert np.all(o[empty] == 0.0) and np.all(np.isneginf(l[empty]))
+    if sum(lens):
+        check(w, o, l)
+
+
 # (num_ctas, min_units_per_cta, heads_per_cta, tile, stages, gather[, fused_merge_max_splits, tier2_ctas,
 #  tier2_permille, tier2_min_units]): gather 0 = cp.async, 1 = TMA bulk; tier2_ctas -1 = one tier
 VARIANTS = {
