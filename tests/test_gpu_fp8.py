@@ -148,3 +148,20 @@ def test_bf16_call_under_fp8_tuning():
     fin = np.isfinite(l_ref)
     assert np.array_equal(np.isneginf(l), np.isneginf(l_ref))
     assert np.all(np.abs(l[fin] - l_ref[fin]) <= LSE_ATOL)
+
+
+def test_fp8_batch_past_merge_grid(f8_stage):
+    """5000 sequences of 0-8 tokens over outputs that start as garbage: every empty sequence is written
+    (O = 0, LSE = -inf) and the rest match the oracle."""
+    lens = torch.randint(0, 9, (5000,), generator=torch.Generator().manual_seed(81)).tolist()
+    w = wl.make_fp8_workload(lens, seed=82, pool_factor=1.25)
+    g = w.to("cuda")
+    out = torch.full_like(g.q, 7.0)
+    lse = torch.full((w.batch, 32), 7.0, dtype=torch.float32, device="cuda")
+    _lib.run_fp8(g.q, g.k_cache, g.v_cache, g.kv_indptr, g.kv_indices, w.sm_scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    o = out.float().cpu().double().numpy()
+    l = lse.cpu().double().numpy()
+    empty = [b for b, n in enumerate(lens) if n == 0]
+    assert empty and np.all(o[empty] == 0.0) and np.all(np.isneginf(l[empty]))
+    check(w, o, l)

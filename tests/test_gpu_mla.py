@@ -206,3 +206,23 @@ def test_mla_wide_holes_and_long_lengths():
     assert _lib.gqa_mla_set_tuning(1) == 0
     out, lse = gpu_mla(w)
     check(w, out, lse)
+
+
+@pytest.mark.parametrize("kernel,h_q", [(0, 16), (1, 16), (0, 64), (1, 64)])
+def test_mla_batch_past_grid(kernel, h_q):
+    """2000 sequences of 0-69 tokens, more than either kernel has CTAs: every empty sequence is written
+    (O = 0, LSE = -inf) over outputs that start as garbage, and each CTA range walks many sequences."""
+    assert _lib.gqa_mla_set_tuning(kernel) == 0
+    lens = torch.randint(0, 70, (2000,), generator=torch.Generator().manual_seed(61)).tolist()
+    lens[:3] = [0, 0, 0]
+    w = wl.make_mla_workload(lens, h_q, 1, 64, 62)
+    g = w.to("cuda")
+    out = torch.full((w.batch, 1, h_q, 512), 7.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((w.batch, h_q, 1), 7.0, dtype=torch.float32, device="cuda")
+    _lib.mla_run(g.q, g.kv_cache, g.block_table, g.cache_seqlens, w.softmax_scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    o = out.float().cpu().double().numpy()
+    l = lse.cpu().double().numpy()
+    empty = [b for b, n in enumerate(lens) if n == 0]
+    assert np.all(o[empty] == 0.0) and np.all(np.isneginf(l[empty]))
+    check(w, o, l)

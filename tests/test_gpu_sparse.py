@@ -112,3 +112,21 @@ def test_sparse_config_every_row():
     w = wl.make_sparse_config()
     out, lse = gpu_sparse(w)
     check(w, out, lse)
+
+
+def test_sparse_rows_past_grid():
+    """3000 rows, more than the decode and merge grids: rows of empty requests (every column -1) are
+    written as O = 0, LSE = -inf over outputs that start as garbage; the rest match the oracle."""
+    lens = torch.randint(0, 40, (3000,), generator=torch.Generator().manual_seed(71)).tolist()
+    w = wl.make_sparse_workload(lens, 16, 16, 72)
+    g = w.to("cuda")
+    out = torch.full_like(g.q, 7.0)
+    lse = torch.full((w.rows, 32), 7.0, dtype=torch.float32, device="cuda")
+    _lib.sparse_run(g.q, g.k_cache, g.v_cache, g.logical_indices, g.block_table, g.token_to_req, w.sm_scale,
+                    out=out, lse=lse)
+    torch.cuda.synchronize()
+    o = out.float().cpu().double().numpy()
+    l = lse.cpu().double().numpy()
+    empty = [r for r, n in enumerate(lens) if n == 0]
+    assert empty and np.all(o[empty] == 0.0) and np.all(np.isneginf(l[empty]))
+    check(w, o, l)
