@@ -24,10 +24,10 @@
 //              scores; the running max of a row moves only when a score
 //              passes it by more than 2^8 (a vote over the group decides), so
 //              P = 2^(s - m) < 256 in bf16 and the row sums stay per thread
-//              until the end of a piece; R / RG groups;
-//   4 correction warps: rescale O^T when a max moved, and write O (or the
-//              fp32 partial) at the end of a piece;
-//   1 MMA warp (one thread issues), 1 producer warp (tensor copies).
+//              until the end of a piece; R / RG groups. A group also
+//              rescales its rows of O^T when a max moved, and writes them
+//              out (O, or the fp32 partial) at the end of a piece;
+//   1 MMA warp (an elected lane issues), 1 producer warp (tensor copies).
 // Every hand-off is an mbarrier (or a named barrier inside a softmax group);
 // every wait is bounded: on a timeout the CTA flags kErrTimeoutFull or
 // kErrTimeoutEmpty and returns after draining its copies and MMAs.
